@@ -1,0 +1,913 @@
+// C ABI of the denoiser stage: model object, weight arena, workspace and the
+// per-block / per-step launch schedule.  All arithmetic runs in the kernels
+// of this library; this file validates arguments, lays out device memory and
+// enqueues launches on the caller's stream.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/dit.h"
+#include "kernels.h"
+
+using namespace dit;
+
+// ============================================================== error state
+static thread_local char g_last_error[512] = "";
+static int g_fail_alloc_after = 0;  // test hook: fail the n-th next allocation
+
+static dit_status fail(dit_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+#define CU_TRY(expr)                                                                                    \
+  do {                                                                                                  \
+    cudaError_t e_ = (expr);                                                                            \
+    if (e_ != cudaSuccess) return fail(DIT_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+#define DIT_TRY(expr)                 \
+  do {                                \
+    dit_status s_ = (expr);           \
+    if (s_ != DIT_OK) return s_;      \
+  } while (0)
+
+static dit_status dev_alloc(void** p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) return DIT_OK;
+  if (g_fail_alloc_after > 0 && --g_fail_alloc_after == 0)
+    return fail(DIT_ERR_OOM, "device allocation of %zu bytes failed (injected)", bytes);
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return fail(e == cudaErrorMemoryAllocation ? DIT_ERR_OOM : DIT_ERR_CUDA, "cudaMalloc(%zu) failed: %s", bytes,
+                cudaGetErrorString(e));
+  }
+  return DIT_OK;
+}
+
+// ============================================================== parameters
+struct ParamSpec {
+  std::string name;
+  std::vector<int64_t> shape;
+};
+
+static std::vector<ParamSpec> param_specs(const dit_config& c) {
+  const int64_t D = c.hidden, F = c.mlp, Dc = c.cond_dim, fq = c.freq_dim;
+  const int64_t P = (int64_t)c.in_channels * c.patch[0] * c.patch[1] * c.patch[2];
+  std::vector<ParamSpec> s = {{"patch_embed.weight", {D, P}},      {"patch_embed.bias", {D}},
+                              {"time_mlp.fc1.weight", {D, fq}},    {"time_mlp.fc1.bias", {D}},
+                              {"time_mlp.fc2.weight", {6 * D, D}}, {"time_mlp.fc2.bias", {6 * D}}};
+  for (int b = 0; b < c.depth; ++b) {
+    const std::string p = "blocks." + std::to_string(b) + ".";
+    const int nstreams = c.cond_mode == DIT_COND_CROSS ? 1 : 2;
+    for (int st = 0; st < nstreams; ++st) {
+      const std::string q = p + (st ? "ctx." : "");
+      s.push_back({q + "mod_table", {6, D}});
+      s.push_back({q + "attn.qkv.weight", {3 * D, D}});
+      s.push_back({q + "attn.qkv.bias", {3 * D}});
+      s.push_back({q + "attn.out.weight", {D, D}});
+      s.push_back({q + "attn.out.bias", {D}});
+      if (st == 0 && c.cond_mode == DIT_COND_CROSS) {
+        s.push_back({p + "cross.q.weight", {D, D}});
+        s.push_back({p + "cross.q.bias", {D}});
+        s.push_back({p + "cross.kv.weight", {2 * D, Dc}});
+        s.push_back({p + "cross.kv.bias", {2 * D}});
+        s.push_back({p + "cross.out.weight", {D, D}});
+        s.push_back({p + "cross.out.bias", {D}});
+      }
+      s.push_back({q + "mlp.fc1.weight", {F, D}});
+      s.push_back({q + "mlp.fc1.bias", {F}});
+      s.push_back({q + "mlp.fc2.weight", {D, F}});
+      s.push_back({q + "mlp.fc2.bias", {D}});
+    }
+  }
+  s.push_back({"head.mod_table", {2, D}});
+  s.push_back({"head.weight", {P, D}});
+  s.push_back({"head.bias", {P}});
+  return s;
+}
+
+static dit_status validate_config(const dit_config* c) {
+  if (!c) return fail(DIT_ERR_INVALID_ARG, "config is NULL");
+  if (c->in_channels <= 0 || c->patch[0] <= 0 || c->patch[1] <= 0 || c->patch[2] <= 0 || c->hidden <= 0 ||
+      c->heads <= 0 || c->head_dim <= 0 || c->mlp <= 0 || c->depth <= 0 || c->cond_dim <= 0 || c->freq_dim <= 0)
+    return fail(DIT_ERR_INVALID_ARG, "config sizes must be positive");
+  if (c->heads * c->head_dim != c->hidden)
+    return fail(DIT_ERR_SHAPE, "hidden (%d) != heads (%d) * head_dim (%d)", c->hidden, c->heads, c->head_dim);
+  if (c->freq_dim % 2) return fail(DIT_ERR_INVALID_ARG, "freq_dim must be even");
+  if (c->cond_mode != DIT_COND_CROSS && c->cond_mode != DIT_COND_JOINT)
+    return fail(DIT_ERR_INVALID_ARG, "unknown cond_mode %d", c->cond_mode);
+  if (c->precision != DIT_PREC_BF16 && c->precision != DIT_PREC_F32)
+    return fail(DIT_ERR_INVALID_ARG, "unknown precision %d", c->precision);
+  const int ra = c->rope_axes[0] + c->rope_axes[1] + c->rope_axes[2];
+  for (int i = 0; i < 3; ++i)
+    if (c->rope_axes[i] < 0 || c->rope_axes[i] % 2)
+      return fail(DIT_ERR_INVALID_ARG, "rope_axes must be even and non-negative");
+  if (ra != 0 && ra != c->head_dim)
+    return fail(DIT_ERR_INVALID_ARG, "rope_axes sum %d must equal head_dim %d (or 0 for no rotation)", ra,
+                c->head_dim);
+  if (c->cond_mode == DIT_COND_JOINT && c->cond_dim != c->hidden)
+    return fail(DIT_ERR_SHAPE, "joint mode needs cond_dim == hidden");
+  if (!(c->ln_eps >= 0.f) || !(c->rope_theta > 0.f) || !(c->timestep_scale > 0.f))
+    return fail(DIT_ERR_INVALID_ARG, "ln_eps >= 0, rope_theta > 0 and timestep_scale > 0 required");
+  if (c->hidden % 4) return fail(DIT_ERR_SHAPE, "hidden must be a multiple of 4");
+  if (c->precision == DIT_PREC_BF16) {
+    if (c->head_dim != 128) return fail(DIT_ERR_SHAPE, "bf16 precision requires head_dim 128");
+    if (c->mlp % 8 || c->cond_dim % 8)
+      return fail(DIT_ERR_SHAPE, "bf16 precision requires mlp and cond_dim multiples of 8");
+    const int P = c->in_channels * c->patch[0] * c->patch[1] * c->patch[2];
+    if (P % 8) return fail(DIT_ERR_SHAPE, "bf16 precision requires C*pt*ph*pw to be a multiple of 8");
+  } else {
+    if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128)
+      return fail(DIT_ERR_SHAPE, "fp32 precision supports head_dim 32, 64 or 128");
+  }
+  return DIT_OK;
+}
+
+// ============================================================== model
+struct Param {
+  ParamSpec spec;
+  bool matrix;  // linear weight: stored in the activation dtype
+  size_t offset;
+  int64_t numel;
+  bool loaded;
+};
+
+struct Workspace {
+  void* base = nullptr;
+  size_t bytes = 0;
+  size_t used = 0;
+  void* take(size_t n) {
+    n = (n + 255) & ~size_t(255);
+    void* p = static_cast<char*>(base) + used;
+    used += n;
+    return p;
+  }
+};
+
+struct dit_model {
+  dit_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  bool bf16 = true;
+  size_t act = 2;  // bytes per activation element
+  std::vector<Param> params;
+  std::unordered_map<std::string, int> index;
+  char* arena = nullptr;
+  size_t arena_bytes = 0;
+  size_t tables_off = 0, ctx_tables_off = 0;  // contiguous [depth][6][D] fp32
+  int n_loaded = 0;
+  int* d_err = nullptr;
+  float* d_t = nullptr;
+  int d_t_cap = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  float2* rope = nullptr;
+  int rope_grid[3] = {0, 0, 0};
+  size_t rope_bytes = 0;
+
+  const void* W(const std::string& n) const { return arena + params[index.at(n)].offset; }
+  const float* V(const std::string& n) const {
+    return reinterpret_cast<const float*>(arena + params[index.at(n)].offset);
+  }
+  std::string blk(int b, const char* suffix) const { return "blocks." + std::to_string(b) + "." + suffix; }
+};
+
+static bool is_matrix(const std::string& n) {
+  return n.size() > 7 && n.compare(n.size() - 7, 7, ".weight") == 0;
+}
+
+extern "C" int dit_num_params(const dit_config* cfg) {
+  if (validate_config(cfg) != DIT_OK) return -1;
+  return (int)param_specs(*cfg).size();
+}
+
+extern "C" dit_status dit_param_info(const dit_config* cfg, int i, char* name_buf, int buf_len, int32_t* ndim,
+                                     int64_t shape[4]) {
+  DIT_TRY(validate_config(cfg));
+  const auto s = param_specs(*cfg);
+  if (i < 0 || i >= (int)s.size()) return fail(DIT_ERR_INVALID_ARG, "parameter index %d out of range", i);
+  if (!name_buf || buf_len <= (int)s[i].name.size() || !ndim || !shape)
+    return fail(DIT_ERR_INVALID_ARG, "output buffers missing or too small");
+  memcpy(name_buf, s[i].name.c_str(), s[i].name.size() + 1);
+  *ndim = (int32_t)s[i].shape.size();
+  for (int d = 0; d < 4; ++d) shape[d] = d < *ndim ? s[i].shape[d] : 1;
+  return DIT_OK;
+}
+
+extern "C" void dit_debug_fail_alloc_after(int n) { g_fail_alloc_after = n; }
+
+extern "C" const char* dit_status_string(dit_status s) {
+  switch (s) {
+    case DIT_OK: return "ok";
+    case DIT_ERR_INVALID_ARG: return "invalid argument";
+    case DIT_ERR_SHAPE: return "shape error";
+    case DIT_ERR_NOT_LOADED: return "weights not loaded";
+    case DIT_ERR_OOM: return "out of device memory";
+    case DIT_ERR_CUDA: return "CUDA error";
+    case DIT_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+extern "C" const char* dit_last_error(void) { return g_last_error; }
+
+extern "C" void dit_destroy(dit_model* m) {
+  if (!m) return;
+  int prev = 0;
+  if (cudaGetDevice(&prev) == cudaSuccess) cudaSetDevice(m->device);
+  cudaFree(m->arena);
+  cudaFree(m->d_err);
+  cudaFree(m->d_t);
+  cudaFree(m->ws);
+  cudaFree(m->rope);
+  cudaSetDevice(prev);
+  delete m;
+}
+
+extern "C" dit_status dit_create(const dit_config* cfg, int device, dit_model** out) {
+  g_last_error[0] = 0;
+  if (!out) return fail(DIT_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  DIT_TRY(validate_config(cfg));
+  dit_model* m = new dit_model();
+  m->cfg = *cfg;
+  m->device = device;
+  m->bf16 = cfg->precision == DIT_PREC_BF16;
+  m->act = m->bf16 ? 2 : 4;
+  // arena layout: block modulation tables first, contiguous per stream
+  const int64_t D = cfg->hidden;
+  const size_t tab_bytes = (size_t)cfg->depth * 6 * D * sizeof(float);
+  size_t off = 0;
+  m->tables_off = off;
+  off += (tab_bytes + 255) & ~size_t(255);
+  if (cfg->cond_mode == DIT_COND_JOINT) {
+    m->ctx_tables_off = off;
+    off += (tab_bytes + 255) & ~size_t(255);
+  }
+  for (auto& sp : param_specs(*cfg)) {
+    Param p;
+    p.spec = sp;
+    p.matrix = is_matrix(sp.name);
+    p.numel = 1;
+    for (auto d : sp.shape) p.numel *= d;
+    p.loaded = false;
+    const std::string& n = sp.name;
+    const bool table = n.size() > 9 && n.compare(n.size() - 9, 9, "mod_table") == 0 && n.rfind("blocks.", 0) == 0;
+    if (table) {
+      const int b = atoi(n.c_str() + 7);
+      const bool ctx = n.find(".ctx.") != std::string::npos;
+      p.offset = (ctx ? m->ctx_tables_off : m->tables_off) + (size_t)b * 6 * D * sizeof(float);
+    } else {
+      p.offset = off;
+      const size_t bytes = (size_t)p.numel * (p.matrix ? m->act : sizeof(float));
+      off += (bytes + 255) & ~size_t(255);
+    }
+    m->index[n] = (int)m->params.size();
+    m->params.push_back(p);
+  }
+  m->arena_bytes = off;
+  cudaError_t e = cudaSetDevice(device);
+  if (e != cudaSuccess) {
+    delete m;
+    return fail(DIT_ERR_CUDA, "cudaSetDevice(%d) failed: %s", device, cudaGetErrorString(e));
+  }
+  e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, device);
+  int major = 0, minor = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+  if (e != cudaSuccess) {
+    delete m;
+    return fail(DIT_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
+  }
+  if (major * 10 + minor != 103) {
+    delete m;
+    return fail(DIT_ERR_CUDA, "libdit.so is built for sm_103a; device %d is sm_%d%d", device, major, minor);
+  }
+  dit_status st = dev_alloc(reinterpret_cast<void**>(&m->arena), m->arena_bytes);
+  if (st == DIT_OK) st = dev_alloc(reinterpret_cast<void**>(&m->d_err), sizeof(int));
+  if (st != DIT_OK) {
+    dit_destroy(m);
+    return st;
+  }
+  if (cudaMemset(m->d_err, 0, sizeof(int)) != cudaSuccess) {
+    dit_destroy(m);
+    return fail(DIT_ERR_CUDA, "cudaMemset failed");
+  }
+  if (getenv("DIT_VERBOSE"))
+    fprintf(stderr,
+            "dit: hidden=%d heads=%d head_dim=%d mlp=%d depth=%d cond=%s precision=%s params=%zu arena=%.1f MB\n",
+            cfg->hidden, cfg->heads, cfg->head_dim, cfg->mlp, cfg->depth,
+            cfg->cond_mode == DIT_COND_CROSS ? "cross" : "joint", m->bf16 ? "bf16" : "fp32", m->params.size(),
+            m->arena_bytes / 1e6);
+  *out = m;
+  return DIT_OK;
+}
+
+extern "C" int64_t dit_device_bytes(const dit_model* m) {
+  if (!m) return 0;
+  return (int64_t)(m->arena_bytes + m->ws_bytes + m->rope_bytes + sizeof(int) + m->d_t_cap * sizeof(float));
+}
+
+extern "C" dit_status dit_load_weights(dit_model* m, const dit_tensor* t, int n) {
+  g_last_error[0] = 0;
+  if (!m || (n > 0 && !t) || n < 0) return fail(DIT_ERR_INVALID_ARG, "NULL model or tensor list");
+  // validate the whole call first: nothing is kept if any entry is wrong
+  std::vector<int> idx(n);
+  std::unordered_map<std::string, int> seen;
+  for (int i = 0; i < n; ++i) {
+    if (!t[i].name) return fail(DIT_ERR_SHAPE, "tensor %d has no name", i);
+    auto it = m->index.find(t[i].name);
+    if (it == m->index.end()) return fail(DIT_ERR_SHAPE, "unknown parameter '%s'", t[i].name);
+    if (seen.count(t[i].name) || m->params[it->second].loaded)
+      return fail(DIT_ERR_SHAPE, "parameter '%s' given twice", t[i].name);
+    seen[t[i].name] = i;
+    const Param& p = m->params[it->second];
+    bool shape_ok = t[i].ndim == (int)p.spec.shape.size();
+    for (int d = 0; shape_ok && d < t[i].ndim; ++d) shape_ok = t[i].shape[d] == p.spec.shape[d];
+    if (!shape_ok) return fail(DIT_ERR_SHAPE, "parameter '%s' has the wrong shape", t[i].name);
+    if (t[i].dtype != DIT_DTYPE_F32 && t[i].dtype != DIT_DTYPE_BF16)
+      return fail(DIT_ERR_INVALID_ARG, "parameter '%s' has an unknown dtype", t[i].name);
+    if (!t[i].data) return fail(DIT_ERR_INVALID_ARG, "parameter '%s' has no data", t[i].name);
+    idx[i] = it->second;
+  }
+  CU_TRY(cudaSetDevice(m->device));
+  // staging buffer for dtype conversion (largest tensor needing it)
+  size_t stage_bytes = 0;
+  for (int i = 0; i < n; ++i) {
+    const Param& p = m->params[idx[i]];
+    const bool want_bf16 = p.matrix && m->bf16;
+    const bool have_bf16 = t[i].dtype == DIT_DTYPE_BF16;
+    if (want_bf16 != have_bf16) stage_bytes = std::max(stage_bytes, (size_t)p.numel * (have_bf16 ? 2 : 4));
+  }
+  void* stage = nullptr;
+  DIT_TRY(dev_alloc(&stage, stage_bytes));
+  dit_status st = DIT_OK;
+  for (int i = 0; i < n && st == DIT_OK; ++i) {
+    Param& p = m->params[idx[i]];
+    char* dst = m->arena + p.offset;
+    const bool want_bf16 = p.matrix && m->bf16;
+    const bool have_bf16 = t[i].dtype == DIT_DTYPE_BF16;
+    const size_t src_bytes = (size_t)p.numel * (have_bf16 ? 2 : 4);
+    cudaError_t e;
+    if (want_bf16 == have_bf16) {
+      e = cudaMemcpy(dst, t[i].data, src_bytes, cudaMemcpyDefault);
+    } else {
+      e = cudaMemcpy(stage, t[i].data, src_bytes, cudaMemcpyDefault);
+      if (e == cudaSuccess)
+        e = want_bf16 ? f32_to_bf16(static_cast<const float*>(stage), dst, p.numel, 0)
+                      : bf16_to_f32(stage, reinterpret_cast<float*>(dst), p.numel, 0);
+      if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    }
+    if (e != cudaSuccess) st = fail(DIT_ERR_CUDA, "copying '%s' failed: %s", t[i].name, cudaGetErrorString(e));
+  }
+  cudaFree(stage);
+  if (st != DIT_OK) return st;
+  for (int i = 0; i < n; ++i) {
+    m->params[idx[i]].loaded = true;
+    ++m->n_loaded;
+  }
+  return DIT_OK;
+}
+
+// ============================================================== helpers
+static dit_status require_loaded(const dit_model* m) {
+  if (!m) return fail(DIT_ERR_INVALID_ARG, "model is NULL");
+  if (m->n_loaded != (int)m->params.size())
+    return fail(DIT_ERR_NOT_LOADED, "%d of %zu parameters loaded", m->n_loaded, m->params.size());
+  return DIT_OK;
+}
+
+static dit_status ensure_ws(dit_model* m, size_t bytes) {
+  if (bytes <= m->ws_bytes) return DIT_OK;
+  if (m->ws) {
+    CU_TRY(cudaDeviceSynchronize());
+    cudaFree(m->ws);
+    m->ws = nullptr;
+    m->ws_bytes = 0;
+  }
+  DIT_TRY(dev_alloc(&m->ws, bytes));
+  m->ws_bytes = bytes;
+  return DIT_OK;
+}
+
+// rotary table [N][hd/2] of (cos, sin) for a token grid, built in double on
+// the host once per grid shape
+static dit_status ensure_rope(dit_model* m, const int32_t g[3]) {
+  const dit_config& c = m->cfg;
+  if (c.rope_axes[0] + c.rope_axes[1] + c.rope_axes[2] == 0) return DIT_OK;
+  if (m->rope && g[0] == m->rope_grid[0] && g[1] == m->rope_grid[1] && g[2] == m->rope_grid[2]) return DIT_OK;
+  const int64_t N = (int64_t)g[0] * g[1] * g[2];
+  const int half = c.head_dim / 2;
+  std::vector<float2> tab((size_t)N * half);
+  int64_t n = 0;
+  for (int it = 0; it < g[0]; ++it)
+    for (int ih = 0; ih < g[1]; ++ih)
+      for (int iw = 0; iw < g[2]; ++iw, ++n) {
+        const int pos[3] = {it, ih, iw};
+        int p = 0;
+        for (int a = 0; a < 3; ++a)
+          for (int j = 0; j < c.rope_axes[a] / 2; ++j, ++p) {
+            const double ang = pos[a] * pow((double)c.rope_theta, -2.0 * j / c.rope_axes[a]);
+            tab[(size_t)n * half + p] = make_float2((float)cos(ang), (float)sin(ang));
+          }
+      }
+  if (m->rope) {
+    CU_TRY(cudaDeviceSynchronize());
+    cudaFree(m->rope);
+    m->rope = nullptr;
+  }
+  const size_t bytes = tab.size() * sizeof(float2);
+  DIT_TRY(dev_alloc(reinterpret_cast<void**>(&m->rope), bytes));
+  m->rope_bytes = bytes;
+  CU_TRY(cudaMemcpy(m->rope, tab.data(), bytes, cudaMemcpyHostToDevice));
+  memcpy(m->rope_grid, g, sizeof(m->rope_grid));
+  return DIT_OK;
+}
+
+static dit_status do_gemm(dit_model* m, const void* A, int64_t M, int K, int64_t lda, const void* W, int N,
+                          const EpiParams& ep, cudaStream_t s) {
+  GemmArgs g;
+  g.A = A;
+  g.M = M;
+  g.K = K;
+  g.lda = lda;
+  g.W = W;
+  g.N = N;
+  g.epi = ep;
+  g.epi.M = (int)M;
+  g.epi.N = N;
+  cudaError_t e = m->bf16 ? gemm_bf16_tc(g, m->d_err, m->num_sms, s) : gemm_f32(g, s);
+  if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "GEMM launch (M=%lld N=%d K=%d) failed: %s", (long long)M, N, K,
+                                    cudaGetErrorString(e));
+  return DIT_OK;
+}
+
+static dit_status do_attn(dit_model* m, const void* q, const void* k, const void* v, int B, int Lq, int Lk,
+                          void* o1, void* o2, int split, cudaStream_t s) {
+  AttnArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.B = B;
+  a.H = m->cfg.heads;
+  a.Lq = Lq;
+  a.Lk = Lk;
+  a.hd = m->cfg.head_dim;
+  a.o1 = o1;
+  a.o2 = o2;
+  a.split = split;
+  cudaError_t e = m->bf16 ? attention_bf16_tc(a, m->d_err, s) : attention_f32(a, s);
+  if (e != cudaSuccess)
+    return fail(DIT_ERR_CUDA, "attention launch (Lq=%d Lk=%d) failed: %s", Lq, Lk, cudaGetErrorString(e));
+  return DIT_OK;
+}
+
+#define K_TRY(expr)                                                                                       \
+  do {                                                                                                    \
+    cudaError_t e_ = (expr);                                                                              \
+    if (e_ != cudaSuccess) return fail(DIT_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_));   \
+  } while (0)
+
+static EpiParams epi_heads(const dit_model* m, const float* bias, void* d0, void* d1, void* d2, int rpb, int seq_total,
+                           int tok_off, int rope_mask) {
+  EpiParams e;
+  e.kind = EPI_HEADS;
+  e.bias = bias;
+  e.dst[0] = d0;
+  e.dst[1] = d1;
+  e.dst[2] = d2;
+  e.D = m->cfg.hidden;
+  e.hd = m->cfg.head_dim;
+  e.H = m->cfg.heads;
+  e.rows_per_batch = rpb;
+  e.seq_total = seq_total;
+  e.tok_off = tok_off;
+  e.rope_mask = m->rope ? rope_mask : 0;
+  e.rope = m->rope;
+  return e;
+}
+static EpiParams epi_resid(const float* bias, float* x, const float* gate, int64_t gate_bstride, int rpb) {
+  EpiParams e;
+  e.kind = EPI_RESID;
+  e.bias = bias;
+  e.x = x;
+  e.gate = gate;
+  e.gate_bstride = gate_bstride;
+  e.rows_per_batch = rpb;
+  return e;
+}
+static EpiParams epi_store(int kind, const float* bias, void* out, int64_t ldo) {
+  EpiParams e;
+  e.kind = kind;
+  e.bias = bias;
+  e.out = out;
+  e.ldo = ldo;
+  return e;
+}
+
+// Scratch buffers of one block evaluation.
+struct BlockBufs {
+  void* h;         // [B, max(N, L), D] act (LN output)
+  void* q;         // [B, H, S, hd] act, S = N (cross) or L + N (joint)
+  void* k;
+  void* v;
+  void* a;         // [B, N, D] act attention output (image stream)
+  void* ac;        // [B, L, D] act (joint: condition stream)
+  void* g;         // [B, max(N, L), F] act MLP hidden
+  void* cond_act;  // [B, L, Dc] act (cross mode, bf16 copy of the condition)
+  void* kc;        // [B, H, L, hd] act (cross mode, this block's keys)
+  void* vc;
+};
+
+static size_t block_ws_bytes(const dit_model* m, int B, int N, int L) {
+  const dit_config& c = m->cfg;
+  const size_t a = m->act;
+  const int64_t NL = std::max(N, L);
+  const int64_t S = c.cond_mode == DIT_COND_JOINT ? (int64_t)N + L : N;
+  size_t t = 0;
+  auto add = [&](int64_t elems, size_t es) { t += ((size_t)elems * es + 255) & ~size_t(255); };
+  add((int64_t)B * NL * c.hidden, a);      // h
+  for (int i = 0; i < 3; ++i) add((int64_t)B * S * c.hidden, a);  // q k v
+  add((int64_t)B * N * c.hidden, a);       // a
+  add((int64_t)B * L * c.hidden, a);       // ac
+  add((int64_t)B * NL * c.mlp, a);         // g
+  add((int64_t)B * L * c.cond_dim, a);     // cond_act
+  add((int64_t)B * L * c.hidden, a);       // kc
+  add((int64_t)B * L * c.hidden, a);       // vc
+  return t;
+}
+
+static BlockBufs carve_block(const dit_model* m, Workspace& w, int B, int N, int L) {
+  const dit_config& c = m->cfg;
+  const size_t a = m->act;
+  const int64_t NL = std::max(N, L);
+  const int64_t S = c.cond_mode == DIT_COND_JOINT ? (int64_t)N + L : N;
+  BlockBufs b;
+  b.h = w.take((size_t)B * NL * c.hidden * a);
+  b.q = w.take((size_t)B * S * c.hidden * a);
+  b.k = w.take((size_t)B * S * c.hidden * a);
+  b.v = w.take((size_t)B * S * c.hidden * a);
+  b.a = w.take((size_t)B * N * c.hidden * a);
+  b.ac = w.take((size_t)B * L * c.hidden * a);
+  b.g = w.take((size_t)B * NL * c.mlp * a);
+  b.cond_act = w.take((size_t)B * L * c.cond_dim * a);
+  b.kc = w.take((size_t)B * L * c.hidden * a);
+  b.vc = w.take((size_t)B * L * c.hidden * a);
+  return b;
+}
+
+// Cross-attention keys/values of the condition tokens for one block:
+// [B*L, Dc] x W_kv^T -> head-major kc, vc.
+static dit_status cross_kv(dit_model* m, int blk, const void* cond_act, int B, int L, void* kc, void* vc,
+                           cudaStream_t s) {
+  const dit_config& c = m->cfg;
+  EpiParams ep = epi_heads(m, m->V(m->blk(blk, "cross.kv.bias")), kc, vc, nullptr, L, L, 0, 0);
+  return do_gemm(m, cond_act, (int64_t)B * L, c.cond_dim, c.cond_dim, m->W(m->blk(blk, "cross.kv.weight")),
+                 2 * c.hidden, ep, s);
+}
+
+// One DiT block on the residual stream(s).  mod/modc point at this block's
+// [6][D] modulation (plus b * mod_bstride per batch element).
+static dit_status run_block(dit_model* m, int blk, float* x, float* xc, const float* mod, const float* modc,
+                            int64_t mod_bstride, const void* kc, const void* vc, int B, int N, int L,
+                            bool ctx_out_needed, const BlockBufs& bb, cudaStream_t s) {
+  const dit_config& c = m->cfg;
+  const int D = c.hidden, F = c.mlp;
+  const float eps = c.ln_eps;
+  const bool bf = m->bf16;
+  if (c.cond_mode == DIT_COND_CROSS) {
+    const int64_t R = (int64_t)B * N;
+    // self-attention half
+    K_TRY(ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, bf, s));
+    DIT_TRY(do_gemm(m, bb.h, R, D, D, m->W(m->blk(blk, "attn.qkv.weight")), 3 * D,
+                    epi_heads(m, m->V(m->blk(blk, "attn.qkv.bias")), bb.q, bb.k, bb.v, N, N, 0, 0x3), s));
+    DIT_TRY(do_attn(m, bb.q, bb.k, bb.v, B, N, N, bb.a, nullptr, N, s));
+    DIT_TRY(do_gemm(m, bb.a, R, D, D, m->W(m->blk(blk, "attn.out.weight")), D,
+                    epi_resid(m->V(m->blk(blk, "attn.out.bias")), x, mod + 2 * D, mod_bstride, N), s));
+    // cross-attention half: plain LN, no rotation, ungated residual
+    K_TRY(ln_modulate(x, R, D, N, nullptr, nullptr, 0, eps, bb.h, bf, s));
+    DIT_TRY(do_gemm(m, bb.h, R, D, D, m->W(m->blk(blk, "cross.q.weight")), D,
+                    epi_heads(m, m->V(m->blk(blk, "cross.q.bias")), bb.q, nullptr, nullptr, N, N, 0, 0), s));
+    DIT_TRY(do_attn(m, bb.q, kc, vc, B, N, L, bb.a, nullptr, N, s));
+    DIT_TRY(do_gemm(m, bb.a, R, D, D, m->W(m->blk(blk, "cross.out.weight")), D,
+                    epi_resid(m->V(m->blk(blk, "cross.out.bias")), x, nullptr, 0, N), s));
+    // MLP half
+    K_TRY(ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, s));
+    DIT_TRY(do_gemm(m, bb.h, R, D, D, m->W(m->blk(blk, "mlp.fc1.weight")), F,
+                    epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F), s));
+    DIT_TRY(do_gemm(m, bb.g, R, F, F, m->W(m->blk(blk, "mlp.fc2.weight")), D,
+                    epi_resid(m->V(m->blk(blk, "mlp.fc2.bias")), x, mod + 5 * D, mod_bstride, N), s));
+    return DIT_OK;
+  }
+  // joint (dual-stream) block: sequence [condition; image]
+  const int S = L + N;
+  const int64_t R = (int64_t)B * N, Rc = (int64_t)B * L;
+  K_TRY(ln_modulate(xc, Rc, D, L, modc + 0 * D, modc + 1 * D, mod_bstride, eps, bb.h, bf, s));
+  DIT_TRY(do_gemm(m, bb.h, Rc, D, D, m->W(m->blk(blk, "ctx.attn.qkv.weight")), 3 * D,
+                  epi_heads(m, m->V(m->blk(blk, "ctx.attn.qkv.bias")), bb.q, bb.k, bb.v, L, S, 0, 0), s));
+  K_TRY(ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, bf, s));
+  DIT_TRY(do_gemm(m, bb.h, R, D, D, m->W(m->blk(blk, "attn.qkv.weight")), 3 * D,
+                  epi_heads(m, m->V(m->blk(blk, "attn.qkv.bias")), bb.q, bb.k, bb.v, N, S, L, 0x3), s));
+  DIT_TRY(do_attn(m, bb.q, bb.k, bb.v, B, S, S, bb.ac, bb.a, L, s));
+  DIT_TRY(do_gemm(m, bb.a, R, D, D, m->W(m->blk(blk, "attn.out.weight")), D,
+                  epi_resid(m->V(m->blk(blk, "attn.out.bias")), x, mod + 2 * D, mod_bstride, N), s));
+  K_TRY(ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, s));
+  DIT_TRY(do_gemm(m, bb.h, R, D, D, m->W(m->blk(blk, "mlp.fc1.weight")), F,
+                  epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F), s));
+  DIT_TRY(do_gemm(m, bb.g, R, F, F, m->W(m->blk(blk, "mlp.fc2.weight")), D,
+                  epi_resid(m->V(m->blk(blk, "mlp.fc2.bias")), x, mod + 5 * D, mod_bstride, N), s));
+  if (!ctx_out_needed) return DIT_OK;
+  DIT_TRY(do_gemm(m, bb.ac, Rc, D, D, m->W(m->blk(blk, "ctx.attn.out.weight")), D,
+                  epi_resid(m->V(m->blk(blk, "ctx.attn.out.bias")), xc, modc + 2 * D, mod_bstride, L), s));
+  K_TRY(ln_modulate(xc, Rc, D, L, modc + 3 * D, modc + 4 * D, mod_bstride, eps, bb.h, bf, s));
+  DIT_TRY(do_gemm(m, bb.h, Rc, D, D, m->W(m->blk(blk, "ctx.mlp.fc1.weight")), F,
+                  epi_store(EPI_GELU, m->V(m->blk(blk, "ctx.mlp.fc1.bias")), bb.g, F), s));
+  DIT_TRY(do_gemm(m, bb.g, Rc, F, F, m->W(m->blk(blk, "ctx.mlp.fc2.weight")), D,
+                  epi_resid(m->V(m->blk(blk, "ctx.mlp.fc2.bias")), xc, modc + 5 * D, mod_bstride, L), s));
+  return DIT_OK;
+}
+
+static dit_status check_latent(const dit_model* m, int batch, const int32_t thw[3]) {
+  if (batch <= 0) return fail(DIT_ERR_INVALID_ARG, "batch must be positive");
+  if (!thw) return fail(DIT_ERR_INVALID_ARG, "latent shape is NULL");
+  for (int i = 0; i < 3; ++i) {
+    if (thw[i] <= 0) return fail(DIT_ERR_SHAPE, "latent dims must be positive");
+    if (thw[i] % m->cfg.patch[i])
+      return fail(DIT_ERR_SHAPE, "latent dim %d (%d) not divisible by patch %d", i, thw[i], m->cfg.patch[i]);
+  }
+  return DIT_OK;
+}
+
+// ============================================================== ABI: pieces
+extern "C" dit_status dit_timestep_modulation(dit_model* m, const float* t_host, int batch, float* mod,
+                                              void* stream) {
+  g_last_error[0] = 0;
+  DIT_TRY(require_loaded(m));
+  if (!t_host || !mod || batch <= 0) return fail(DIT_ERR_INVALID_ARG, "bad timestep arguments");
+  for (int b = 0; b < batch; ++b)
+    if (!isfinite(t_host[b])) return fail(DIT_ERR_INVALID_ARG, "timestep %d is not finite", b);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CU_TRY(cudaSetDevice(m->device));
+  if (m->d_t_cap < batch) {
+    CU_TRY(cudaDeviceSynchronize());
+    cudaFree(m->d_t);
+    m->d_t = nullptr;
+    m->d_t_cap = 0;
+    DIT_TRY(dev_alloc(reinterpret_cast<void**>(&m->d_t), batch * sizeof(float)));
+    m->d_t_cap = batch;
+  }
+  const size_t need = (size_t)batch * m->cfg.hidden * sizeof(float) + 256;
+  DIT_TRY(ensure_ws(m, need));
+  CU_TRY(cudaMemcpyAsync(m->d_t, t_host, batch * sizeof(float), cudaMemcpyHostToDevice, s));
+  K_TRY(timestep_mlp(m->d_t, 0.0, batch, m->cfg.freq_dim, m->cfg.hidden, m->W("time_mlp.fc1.weight"),
+                     m->V("time_mlp.fc1.bias"), m->W("time_mlp.fc2.weight"), m->V("time_mlp.fc2.bias"), m->bf16,
+                     static_cast<float*>(m->ws), mod, s));
+  return DIT_OK;
+}
+
+extern "C" dit_status dit_patch_embed(dit_model* m, const float* lat, int batch, const int32_t thw[3], float* x,
+                                      void* stream) {
+  g_last_error[0] = 0;
+  DIT_TRY(require_loaded(m));
+  DIT_TRY(check_latent(m, batch, thw));
+  if (!lat || !x) return fail(DIT_ERR_INVALID_ARG, "NULL tensor");
+  const dit_config& c = m->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CU_TRY(cudaSetDevice(m->device));
+  const int64_t N = (int64_t)(thw[0] / c.patch[0]) * (thw[1] / c.patch[1]) * (thw[2] / c.patch[2]);
+  const int P = c.in_channels * c.patch[0] * c.patch[1] * c.patch[2];
+  DIT_TRY(ensure_ws(m, (size_t)batch * N * P * m->act + 256));
+  K_TRY(patchify(lat, batch, 1, c.in_channels, thw[0], thw[1], thw[2], c.patch[0], c.patch[1], c.patch[2], m->ws,
+                 m->bf16, s));
+  return do_gemm(m, m->ws, (int64_t)batch * N, P, P, m->W("patch_embed.weight"), c.hidden,
+                 epi_store(EPI_F32, m->V("patch_embed.bias"), x, c.hidden), s);
+}
+
+extern "C" dit_status dit_block_forward(dit_model* m, int block, float* x, float* xc, const float* mod,
+                                        const float* cond, int batch, const int32_t grid[3], int cond_len,
+                                        void* stream) {
+  g_last_error[0] = 0;
+  DIT_TRY(require_loaded(m));
+  const dit_config& c = m->cfg;
+  if (block < 0 || block >= c.depth) return fail(DIT_ERR_INVALID_ARG, "block %d out of range", block);
+  if (!x || !mod || batch <= 0 || !grid) return fail(DIT_ERR_INVALID_ARG, "NULL tensor or bad batch");
+  if (grid[0] <= 0 || grid[1] <= 0 || grid[2] <= 0) return fail(DIT_ERR_SHAPE, "grid dims must be positive");
+  if (cond_len <= 0) return fail(DIT_ERR_SHAPE, "cond_len must be positive");
+  if (c.cond_mode == DIT_COND_CROSS && (!cond || xc))
+    return fail(DIT_ERR_INVALID_ARG, "cross mode takes cond and no xc");
+  if (c.cond_mode == DIT_COND_JOINT && (cond || !xc))
+    return fail(DIT_ERR_INVALID_ARG, "joint mode takes xc and no cond");
+  const int64_t N64 = (int64_t)grid[0] * grid[1] * grid[2];
+  if (N64 > (1 << 24)) return fail(DIT_ERR_SHAPE, "too many tokens");
+  const int N = (int)N64, L = cond_len, D = c.hidden;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CU_TRY(cudaSetDevice(m->device));
+  const size_t modtab_bytes = (size_t)2 * batch * 6 * D * sizeof(float);
+  DIT_TRY(ensure_rope(m, grid));
+  DIT_TRY(ensure_ws(m, block_ws_bytes(m, batch, N, L) + modtab_bytes + 4096));
+  Workspace w{m->ws, m->ws_bytes, 0};
+  BlockBufs bb = carve_block(m, w, batch, N, L);
+  float* modtab = static_cast<float*>(w.take((size_t)batch * 6 * D * sizeof(float)));
+  float* modtab_c = static_cast<float*>(w.take((size_t)batch * 6 * D * sizeof(float)));
+  K_TRY(add_tables(mod, batch, D, 6, m->V(m->blk(block, "mod_table")), 1, modtab, s));
+  if (c.cond_mode == DIT_COND_JOINT)
+    K_TRY(add_tables(mod, batch, D, 6, m->V(m->blk(block, "ctx.mod_table")), 1, modtab_c, s));
+  const void* kc = nullptr;
+  const void* vc = nullptr;
+  if (c.cond_mode == DIT_COND_CROSS) {
+    const void* ca = cond;
+    if (m->bf16) {
+      K_TRY(f32_to_bf16(cond, bb.cond_act, (int64_t)batch * L * c.cond_dim, s));
+      ca = bb.cond_act;
+    }
+    DIT_TRY(cross_kv(m, block, ca, batch, L, bb.kc, bb.vc, s));
+    kc = bb.kc;
+    vc = bb.vc;
+  }
+  return run_block(m, block, x, xc, modtab, modtab_c, 6 * D, kc, vc, batch, N, L, true, bb, s);
+}
+
+extern "C" dit_status dit_final_layer(dit_model* m, const float* x, const float* mod, int batch,
+                                      const int32_t thw[3], float* v, void* stream) {
+  g_last_error[0] = 0;
+  DIT_TRY(require_loaded(m));
+  DIT_TRY(check_latent(m, batch, thw));
+  if (!x || !mod || !v) return fail(DIT_ERR_INVALID_ARG, "NULL tensor");
+  const dit_config& c = m->cfg;
+  const int D = c.hidden;
+  const int64_t N = (int64_t)(thw[0] / c.patch[0]) * (thw[1] / c.patch[1]) * (thw[2] / c.patch[2]);
+  const int P = c.in_channels * c.patch[0] * c.patch[1] * c.patch[2];
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CU_TRY(cudaSetDevice(m->device));
+  Workspace w{nullptr, 0, 0};
+  const size_t need = (size_t)batch * 2 * D * 4 + (size_t)batch * N * D * m->act + (size_t)batch * N * P * 4 + 1024;
+  DIT_TRY(ensure_ws(m, need));
+  w.base = m->ws;
+  w.bytes = m->ws_bytes;
+  float* headtab = static_cast<float*>(w.take((size_t)batch * 2 * D * 4));
+  void* h = w.take((size_t)batch * N * D * m->act);
+  float* vt = static_cast<float*>(w.take((size_t)batch * N * P * 4));
+  K_TRY(add_tables(mod, batch, D, 2, m->V("head.mod_table"), 1, headtab, s));
+  K_TRY(ln_modulate(x, batch * N, D, (int)N, headtab, headtab + D, 2 * D, c.ln_eps, h, m->bf16, s));
+  DIT_TRY(do_gemm(m, h, batch * N, D, D, m->W("head.weight"), P, epi_store(EPI_F32, m->V("head.bias"), vt, P), s));
+  K_TRY(unpatchify(vt, batch, c.in_channels, thw[0], thw[1], thw[2], c.patch[0], c.patch[1], c.patch[2], v, s));
+  return DIT_OK;
+}
+
+extern "C" dit_status cfg_combine(const float* vc, const float* vu, float g, float* v, int64_t n, void* stream) {
+  g_last_error[0] = 0;
+  if (n < 0 || (n > 0 && (!vc || !vu || !v))) return fail(DIT_ERR_INVALID_ARG, "bad cfg_combine arguments");
+  if (!isfinite(g)) return fail(DIT_ERR_INVALID_ARG, "guidance scale is not finite");
+  K_TRY(cfg_combine_kernel(vc, vu, g, v, n, static_cast<cudaStream_t>(stream)));
+  return DIT_OK;
+}
+
+extern "C" dit_status flow_euler_step(float* x, const float* v, float sigma, float sigma_next, int64_t n,
+                                      void* stream) {
+  g_last_error[0] = 0;
+  if (n < 0 || (n > 0 && (!x || !v))) return fail(DIT_ERR_INVALID_ARG, "bad flow_euler_step arguments");
+  if (!isfinite(sigma) || !isfinite(sigma_next)) return fail(DIT_ERR_INVALID_ARG, "sigma is not finite");
+  const float dsig = (float)((double)sigma_next - (double)sigma);
+  K_TRY(euler_kernel(x, v, dsig, n, static_cast<cudaStream_t>(stream)));
+  return DIT_OK;
+}
+
+// ============================================================== ABI: loop
+extern "C" dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, const int32_t thw[3],
+                                       const float* cond, const float* uncond, int cond_len, const float* sigmas,
+                                       int n_steps, float guidance, uint32_t flags, void* stream) {
+  g_last_error[0] = 0;
+  DIT_TRY(require_loaded(m));
+  DIT_TRY(check_latent(m, batch, thw));
+  const dit_config& c = m->cfg;
+  if (!latents || !cond) return fail(DIT_ERR_INVALID_ARG, "NULL latents or cond");
+  if (cond_len <= 0) return fail(DIT_ERR_SHAPE, "cond_len must be positive");
+  if (n_steps <= 0 || !sigmas) return fail(DIT_ERR_INVALID_ARG, "need n_steps > 0 and n_steps + 1 sigmas");
+  if (flags & ~(uint32_t)DIT_LOOP_PARTIAL_SCHEDULE) return fail(DIT_ERR_INVALID_ARG, "unknown flags");
+  if (!isfinite(guidance)) return fail(DIT_ERR_INVALID_ARG, "guidance is not finite");
+  if (!uncond && guidance != 1.0f)
+    return fail(DIT_ERR_INVALID_ARG, "guidance %g needs negative condition tokens (uncond is NULL)", guidance);
+  for (int i = 0; i <= n_steps; ++i)
+    if (!isfinite(sigmas[i])) return fail(DIT_ERR_INVALID_ARG, "sigma %d is not finite", i);
+  for (int i = 0; i < n_steps; ++i)
+    if (!(sigmas[i + 1] < sigmas[i]))
+      return fail(DIT_ERR_INVALID_ARG, "sigmas must be strictly decreasing (reversed schedule?) at step %d", i);
+  if (!(flags & DIT_LOOP_PARTIAL_SCHEDULE) && (sigmas[0] != 1.0f || sigmas[n_steps] != 0.0f))
+    return fail(DIT_ERR_INVALID_ARG, "schedule must run from sigma 1 to 0 (set DIT_LOOP_PARTIAL_SCHEDULE to resume)");
+  const bool cfg = uncond != nullptr;
+  const int Bq = batch, B = cfg ? 2 * batch : batch;
+  const int32_t grid[3] = {thw[0] / c.patch[0], thw[1] / c.patch[1], thw[2] / c.patch[2]};
+  const int64_t N64 = (int64_t)grid[0] * grid[1] * grid[2];
+  if (N64 > (1 << 24)) return fail(DIT_ERR_SHAPE, "too many tokens");
+  const int N = (int)N64, L = cond_len, D = c.hidden, P = c.in_channels * c.patch[0] * c.patch[1] * c.patch[2];
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CU_TRY(cudaSetDevice(m->device));
+  DIT_TRY(ensure_rope(m, grid));
+
+  // workspace: block scratch + loop state
+  const size_t a = m->act;
+  const int nst = c.cond_mode == DIT_COND_JOINT ? 2 : 1;
+  size_t need = block_ws_bytes(m, B, N, L);
+  need += (size_t)c.depth * nst * 6 * D * 4 + 2 * D * 4 + 6 * D * 4 + D * 4;  // tables, m, temb hidden
+  need += (size_t)B * N * D * 4;                                                // x
+  need += (size_t)B * L * D * 4;                                                // xc
+  need += (size_t)B * N * P * a + (size_t)B * N * P * 4;                        // tokens, vt
+  if (c.cond_mode == DIT_COND_CROSS) need += (size_t)c.depth * 2 * B * L * D * a;  // K/V cache
+  need += 64 * 256;
+  DIT_TRY(ensure_ws(m, need));
+  Workspace w{m->ws, m->ws_bytes, 0};
+  BlockBufs bb = carve_block(m, w, B, N, L);
+  float* tabs = static_cast<float*>(w.take((size_t)c.depth * 6 * D * 4));
+  float* tabs_c = nst == 2 ? static_cast<float*>(w.take((size_t)c.depth * 6 * D * 4)) : nullptr;
+  float* headtab = static_cast<float*>(w.take((size_t)2 * D * 4));
+  float* mvec = static_cast<float*>(w.take((size_t)6 * D * 4));
+  float* thid = static_cast<float*>(w.take((size_t)D * 4));
+  float* x = static_cast<float*>(w.take((size_t)B * N * D * 4));
+  float* xc = static_cast<float*>(w.take((size_t)B * L * D * 4));
+  void* tokens = w.take((size_t)B * N * P * a);
+  float* vt = static_cast<float*>(w.take((size_t)B * N * P * 4));
+  void* kvcache = c.cond_mode == DIT_COND_CROSS ? w.take((size_t)c.depth * 2 * B * L * D * a) : nullptr;
+
+  // condition rows: [cond (Bq); uncond (Bq)]
+  const size_t cond_bytes = (size_t)Bq * L * c.cond_dim * 4;
+  if (c.cond_mode == DIT_COND_CROSS) {
+    // keys/values of the condition tokens do not depend on the step: once per call
+    float* cf = xc;  // xc is unused in cross mode; borrow it to stage fp32 rows
+    if ((size_t)B * L * c.cond_dim > (size_t)B * L * D) {
+      // cond_dim > hidden: stage through the MLP scratch instead
+      cf = static_cast<float*>(bb.g);
+    }
+    CU_TRY(cudaMemcpyAsync(cf, cond, cond_bytes, cudaMemcpyDeviceToDevice, s));
+    if (cfg) CU_TRY(cudaMemcpyAsync(cf + (size_t)Bq * L * c.cond_dim, uncond, cond_bytes, cudaMemcpyDeviceToDevice, s));
+    const void* ca = cf;
+    if (m->bf16) {
+      K_TRY(f32_to_bf16(cf, bb.cond_act, (int64_t)B * L * c.cond_dim, s));
+      ca = bb.cond_act;
+    }
+    const size_t per = (size_t)B * L * D * a;
+    for (int blk = 0; blk < c.depth; ++blk) {
+      char* kb = static_cast<char*>(kvcache) + (size_t)blk * 2 * per;
+      DIT_TRY(cross_kv(m, blk, ca, B, L, kb, kb + per, s));
+    }
+  }
+  for (int i = 0; i < n_steps; ++i) {
+    const double t = (double)c.timestep_scale * (double)sigmas[i];
+    K_TRY(timestep_mlp(nullptr, t, 1, c.freq_dim, D, m->W("time_mlp.fc1.weight"), m->V("time_mlp.fc1.bias"),
+                       m->W("time_mlp.fc2.weight"), m->V("time_mlp.fc2.bias"), m->bf16, thid, mvec, s));
+    K_TRY(add_tables(mvec, 1, D, 6, m->V("blocks.0.mod_table"), c.depth, tabs, s));
+    if (tabs_c) K_TRY(add_tables(mvec, 1, D, 6, m->V("blocks.0.ctx.mod_table"), c.depth, tabs_c, s));
+    K_TRY(add_tables(mvec, 1, D, 2, m->V("head.mod_table"), 1, headtab, s));
+    K_TRY(patchify(latents, Bq, cfg ? 2 : 1, c.in_channels, thw[0], thw[1], thw[2], c.patch[0], c.patch[1],
+                   c.patch[2], tokens, m->bf16, s));
+    DIT_TRY(do_gemm(m, tokens, (int64_t)B * N, P, P, m->W("patch_embed.weight"), D,
+                    epi_store(EPI_F32, m->V("patch_embed.bias"), x, D), s));
+    if (c.cond_mode == DIT_COND_JOINT) {
+      CU_TRY(cudaMemcpyAsync(xc, cond, cond_bytes, cudaMemcpyDeviceToDevice, s));
+      if (cfg) CU_TRY(cudaMemcpyAsync(xc + (size_t)Bq * L * D, uncond, cond_bytes, cudaMemcpyDeviceToDevice, s));
+    }
+    const size_t per = (size_t)B * L * D * a;
+    for (int blk = 0; blk < c.depth; ++blk) {
+      const void* kc = nullptr;
+      const void* vc = nullptr;
+      if (kvcache) {
+        kc = static_cast<char*>(kvcache) + (size_t)blk * 2 * per;
+        vc = static_cast<const char*>(kc) + per;
+      }
+      DIT_TRY(run_block(m, blk, x, c.cond_mode == DIT_COND_JOINT ? xc : nullptr, tabs + (size_t)blk * 6 * D,
+                        tabs_c ? tabs_c + (size_t)blk * 6 * D : nullptr, 0, kc, vc, B, N, L, blk + 1 < c.depth, bb,
+                        s));
+    }
+    K_TRY(ln_modulate(x, (int64_t)B * N, D, N, headtab, headtab + D, 0, c.ln_eps, bb.h, m->bf16, s));
+    DIT_TRY(do_gemm(m, bb.h, (int64_t)B * N, D, D, m->W("head.weight"), P,
+                    epi_store(EPI_F32, m->V("head.bias"), vt, P), s));
+    const float dsig = (float)((double)sigmas[i + 1] - (double)sigmas[i]);
+    K_TRY(cfg_euler_tokens(vt, Bq, cfg, guidance, dsig, c.in_channels, thw[0], thw[1], thw[2], c.patch[0],
+                           c.patch[1], c.patch[2], latents, s));
+  }
+  return DIT_OK;
+}
+
+extern "C" dit_status dit_synchronize(dit_model* m, void* stream) {
+  g_last_error[0] = 0;
+  if (!m) return fail(DIT_ERR_INVALID_ARG, "model is NULL");
+  CU_TRY(cudaSetDevice(m->device));
+  CU_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  int h = 0;
+  CU_TRY(cudaMemcpy(&h, m->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (h) {
+    CU_TRY(cudaMemset(m->d_err, 0, sizeof(int)));
+    return fail(DIT_ERR_TIMEOUT, "a kernel abandoned a bounded wait (site %d); outputs are invalid", h);
+  }
+  return DIT_OK;
+}

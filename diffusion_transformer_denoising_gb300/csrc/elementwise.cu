@@ -1,0 +1,382 @@
+// Memory-bound kernels of the denoiser step: modulated LayerNorm, timestep
+// embedding MLP, modulation tables, latent packing, guidance + Euler.
+// All use coalesced 128-bit accesses where the layout allows and one warp
+// per row for row reductions.
+#include <math.h>
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dit {
+
+DIT_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+static inline unsigned blocks_for(int64_t n, int per_block, int cap = 152 * 32) {
+  int64_t b = (n + per_block - 1) / per_block;
+  if (b < 1) b = 1;
+  return (unsigned)(b > cap ? cap : b);
+}
+
+// ---------------------------------------------------------------- LayerNorm + adaLN
+// One warp per row; the row stays in registers (NCH float4 per lane) so x is
+// read once.  Statistics in fp32: mean, then the centred second moment.
+template <int NCH, bool kBf16>
+__global__ void __launch_bounds__(256) ln_mod_kernel(const float* __restrict__ x, int64_t rows, int D, int rpb,
+                                                     const float* __restrict__ shift,
+                                                     const float* __restrict__ scale, int64_t mbs, float eps,
+                                                     void* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int n4 = D >> 2;
+  const float4* xr = reinterpret_cast<const float4*>(x + row * D);
+  float4 v[NCH];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    const int c = lane + 32 * i;
+    if (c < n4) {
+      v[i] = __ldg(xr + c);
+      s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    } else {
+      v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  const float mean = warp_sum(s) / (float)D;
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    const int c = lane + 32 * i;
+    if (c < n4) {
+      const float a = v[i].x - mean, b = v[i].y - mean, cc = v[i].z - mean, d = v[i].w - mean;
+      q += (a * a + b * b) + (cc * cc + d * d);
+    }
+  }
+  const float rstd = 1.0f / sqrtf(warp_sum(q) / (float)D + eps);
+  const int64_t bi = row / rpb;
+  const float4* sh4 = shift ? reinterpret_cast<const float4*>(shift + bi * mbs) : nullptr;
+  const float4* sc4 = scale ? reinterpret_cast<const float4*>(scale + bi * mbs) : nullptr;
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    const int c = lane + 32 * i;
+    if (c >= n4) continue;
+    float4 y = make_float4((v[i].x - mean) * rstd, (v[i].y - mean) * rstd, (v[i].z - mean) * rstd,
+                           (v[i].w - mean) * rstd);
+    if (sc4) {
+      const float4 a = __ldg(sc4 + c), b = __ldg(sh4 + c);
+      y.x = fmaf(y.x, 1.f + a.x, b.x);
+      y.y = fmaf(y.y, 1.f + a.y, b.y);
+      y.z = fmaf(y.z, 1.f + a.z, b.z);
+      y.w = fmaf(y.w, 1.f + a.w, b.w);
+    }
+    if constexpr (kBf16) {
+      uint2 u;
+      u.x = pack_bf16x2(y.x, y.y);
+      u.y = pack_bf16x2(y.z, y.w);
+      reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + row * D)[c] = u;
+    } else {
+      reinterpret_cast<float4*>(static_cast<float*>(out) + row * D)[c] = y;
+    }
+  }
+}
+
+template <int NCH>
+static cudaError_t ln_launch(const float* x, int64_t rows, int D, int rpb, const float* sh, const float* sc,
+                             int64_t mbs, float eps, void* out, bool bf16, cudaStream_t s) {
+  const unsigned grid = (unsigned)((rows + 7) / 8);
+  if (bf16)
+    ln_mod_kernel<NCH, true><<<grid, 256, 0, s>>>(x, rows, D, rpb, sh, sc, mbs, eps, out);
+  else
+    ln_mod_kernel<NCH, false><<<grid, 256, 0, s>>>(x, rows, D, rpb, sh, sc, mbs, eps, out);
+  return cudaGetLastError();
+}
+
+cudaError_t ln_modulate(const float* x, int64_t rows, int D, int rpb, const float* shift, const float* scale,
+                        int64_t mbs, float eps, void* out, bool out_bf16, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  if (D % 4) return cudaErrorInvalidValue;
+  const int nch = (D / 4 + 31) / 32;
+  if (nch <= 1) return ln_launch<1>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
+  if (nch <= 2) return ln_launch<2>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
+  if (nch <= 4) return ln_launch<4>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
+  if (nch <= 8) return ln_launch<8>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
+  if (nch <= 12) return ln_launch<12>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
+  if (nch <= 16) return ln_launch<16>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
+  if (nch <= 24) return ln_launch<24>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
+  if (nch <= 32) return ln_launch<32>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
+  return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------- timestep MLP
+template <typename WT>
+DIT_DEV float wload(const WT* w, int64_t i);
+template <>
+DIT_DEV float wload<float>(const float* w, int64_t i) { return __ldg(w + i); }
+template <>
+DIT_DEV float wload<__nv_bfloat16>(const __nv_bfloat16* w, int64_t i) { return __bfloat162float(w[i]); }
+
+// hidden[b, j] = SiLU(W1[j, :] . e(t_b) + b1[j]); one warp per output.
+// The sinusoid's arguments reach 1000 rad, so they are formed in double.
+template <typename WT>
+__global__ void __launch_bounds__(256) temb_fc1_kernel(const float* t_dev, double t0, int fq, int D,
+                                                       const WT* __restrict__ w1, const float* __restrict__ b1,
+                                                       float* hidden) {
+  extern __shared__ float e[];
+  const int b = blockIdx.y;
+  const double t = t_dev ? (double)t_dev[b] : t0;
+  const int half = fq / 2;
+  for (int k = threadIdx.x; k < half; k += blockDim.x) {
+    const double a = t * pow(10000.0, -(double)k / (double)half);
+    double sv, cv;
+    sincos(a, &sv, &cv);
+    e[k] = (float)cv;
+    e[half + k] = (float)sv;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (j >= D) return;
+  float acc = 0.f;
+  for (int k = lane; k < fq; k += 32) acc = fmaf(wload(w1, (int64_t)j * fq + k), e[k], acc);
+  acc = warp_sum(acc) + b1[j];
+  if (lane == 0) hidden[(int64_t)b * D + j] = acc / (1.f + expf(-acc));
+}
+
+// mod[b, i] = W2[i, :] . hidden[b] + b2[i]; one warp per output.
+template <typename WT>
+__global__ void __launch_bounds__(256) temb_fc2_kernel(int D, const WT* __restrict__ w2,
+                                                       const float* __restrict__ b2, const float* hidden,
+                                                       float* mod) {
+  extern __shared__ float h[];
+  const int b = blockIdx.y;
+  for (int k = threadIdx.x; k < D; k += blockDim.x) h[k] = hidden[(int64_t)b * D + k];
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (i >= 6 * D) return;
+  float acc = 0.f;
+  for (int k = lane; k < D; k += 32) acc = fmaf(wload(w2, (int64_t)i * D + k), h[k], acc);
+  acc = warp_sum(acc);
+  if (lane == 0) mod[(int64_t)b * 6 * D + i] = acc + b2[i];
+}
+
+cudaError_t timestep_mlp(const float* t_dev, double t0, int batch, int fq, int D, const void* w1, const float* b1,
+                         const void* w2, const float* b2, bool w_bf16, float* hidden, float* mod, cudaStream_t s) {
+  dim3 g1((D + 7) / 8, batch), g2((6 * D + 7) / 8, batch);
+  if (w_bf16) {
+    temb_fc1_kernel<__nv_bfloat16><<<g1, 256, fq * sizeof(float), s>>>(
+        t_dev, t0, fq, D, static_cast<const __nv_bfloat16*>(w1), b1, hidden);
+    temb_fc2_kernel<__nv_bfloat16><<<g2, 256, D * sizeof(float), s>>>(
+        D, static_cast<const __nv_bfloat16*>(w2), b2, hidden, mod);
+  } else {
+    temb_fc1_kernel<float><<<g1, 256, fq * sizeof(float), s>>>(t_dev, t0, fq, D, static_cast<const float*>(w1),
+                                                               b1, hidden);
+    temb_fc2_kernel<float><<<g2, 256, D * sizeof(float), s>>>(D, static_cast<const float*>(w2), b2, hidden,
+                                                              mod);
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- modulation tables
+__global__ void add_tables_kernel(const float* __restrict__ mod, int batch, int D, int rows,
+                                  const float* __restrict__ tab, int ntab, float* __restrict__ out) {
+  const int64_t per = (int64_t)rows * D;
+  const int64_t n = (int64_t)ntab * batch * per;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t k = i / (batch * per);
+    const int64_t r = i - k * batch * per;
+    const int64_t b = r / per;
+    const int64_t jc = r - b * per;
+    out[i] = mod[b * 6 * D + jc] + tab[k * per + jc];
+  }
+}
+
+cudaError_t add_tables(const float* mod, int batch, int D, int rows, const float* tables, int ntab, float* out,
+                       cudaStream_t s) {
+  const int64_t n = (int64_t)ntab * batch * rows * D;
+  if (n == 0) return cudaSuccess;
+  add_tables_kernel<<<blocks_for(n, 256), 256, 0, s>>>(mod, batch, D, rows, tables, ntab, out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- latent packing
+struct PatchGeom {
+  int C, T, H, W, pt, ph, pw, gt, gh, gw, P;
+  int64_t N;
+};
+static PatchGeom geom(int C, int T, int H, int W, int pt, int ph, int pw) {
+  PatchGeom g{C, T, H, W, pt, ph, pw, T / pt, H / ph, W / pw, C * pt * ph * pw, 0};
+  g.N = (int64_t)g.gt * g.gh * g.gw;
+  return g;
+}
+// latent element (c, t, h, w) -> (token n, patch index j)
+DIT_DEV void latent_to_token(const PatchGeom& g, int c, int t, int h, int w, int64_t& n, int& j) {
+  n = ((int64_t)(t / g.pt) * g.gh + h / g.ph) * g.gw + w / g.pw;
+  j = ((c * g.pt + t % g.pt) * g.ph + h % g.ph) * g.pw + w % g.pw;
+}
+
+template <bool kBf16>
+__global__ void patchify_kernel(const float* __restrict__ lat, int Bl, int copies, PatchGeom g, void* tokens) {
+  const int64_t per = (int64_t)g.C * g.T * g.H * g.W;
+  const int64_t n = (int64_t)Bl * per;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = i / per;
+    int64_t r = i - b * per;
+    const int w = (int)(r % g.W); r /= g.W;
+    const int h = (int)(r % g.H); r /= g.H;
+    const int t = (int)(r % g.T);
+    const int c = (int)(r / g.T);
+    int64_t tok; int j;
+    latent_to_token(g, c, t, h, w, tok, j);
+    const float v = lat[i];
+    for (int cp = 0; cp < copies; ++cp) {
+      const int64_t o = (((int64_t)cp * Bl + b) * g.N + tok) * g.P + j;
+      if constexpr (kBf16) static_cast<__nv_bfloat16*>(tokens)[o] = __float2bfloat16_rn(v);
+      else static_cast<float*>(tokens)[o] = v;
+    }
+  }
+}
+
+cudaError_t patchify(const float* lat, int Bl, int copies, int C, int T, int H, int W, int pt, int ph, int pw,
+                     void* tokens, bool out_bf16, cudaStream_t s) {
+  const PatchGeom g = geom(C, T, H, W, pt, ph, pw);
+  const int64_t n = (int64_t)Bl * C * T * H * W;
+  if (n == 0) return cudaSuccess;
+  if (out_bf16) patchify_kernel<true><<<blocks_for(n, 256), 256, 0, s>>>(lat, Bl, copies, g, tokens);
+  else patchify_kernel<false><<<blocks_for(n, 256), 256, 0, s>>>(lat, Bl, copies, g, tokens);
+  return cudaGetLastError();
+}
+
+__global__ void unpatchify_kernel(const float* __restrict__ tok, int B, PatchGeom g, float* __restrict__ lat) {
+  const int64_t per = (int64_t)g.C * g.T * g.H * g.W;
+  const int64_t n = (int64_t)B * per;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = i / per;
+    int64_t r = i - b * per;
+    const int w = (int)(r % g.W); r /= g.W;
+    const int h = (int)(r % g.H); r /= g.H;
+    const int t = (int)(r % g.T);
+    const int c = (int)(r / g.T);
+    int64_t tk; int j;
+    latent_to_token(g, c, t, h, w, tk, j);
+    lat[i] = tok[(b * g.N + tk) * g.P + j];
+  }
+}
+
+cudaError_t unpatchify(const float* tok, int B, int C, int T, int H, int W, int pt, int ph, int pw, float* lat,
+                       cudaStream_t s) {
+  const PatchGeom g = geom(C, T, H, W, pt, ph, pw);
+  const int64_t n = (int64_t)B * C * T * H * W;
+  if (n == 0) return cudaSuccess;
+  unpatchify_kernel<<<blocks_for(n, 256), 256, 0, s>>>(tok, B, g, lat);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- guidance + Euler
+__global__ void cfg_euler_tokens_kernel(const float* __restrict__ vt, int Bl, int cfg, float gs, float dsig,
+                                        PatchGeom g, float* __restrict__ lat) {
+  const int64_t per = (int64_t)g.C * g.T * g.H * g.W;
+  const int64_t n = (int64_t)Bl * per;
+  const int64_t half = (int64_t)Bl * g.N * g.P;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = i / per;
+    int64_t r = i - b * per;
+    const int w = (int)(r % g.W); r /= g.W;
+    const int h = (int)(r % g.H); r /= g.H;
+    const int t = (int)(r % g.T);
+    const int c = (int)(r / g.T);
+    int64_t tk; int j;
+    latent_to_token(g, c, t, h, w, tk, j);
+    const int64_t o = (b * g.N + tk) * g.P + j;
+    const float vc = vt[o];
+    const float v = cfg ? fmaf(gs, vc - vt[half + o], vt[half + o]) : vc;
+    lat[i] = fmaf(dsig, v, lat[i]);
+  }
+}
+
+cudaError_t cfg_euler_tokens(const float* vt, int Bl, bool cfg, float gs, float dsig, int C, int T, int H, int W,
+                             int pt, int ph, int pw, float* lat, cudaStream_t s) {
+  const PatchGeom g = geom(C, T, H, W, pt, ph, pw);
+  const int64_t n = (int64_t)Bl * C * T * H * W;
+  if (n == 0) return cudaSuccess;
+  cfg_euler_tokens_kernel<<<blocks_for(n, 256), 256, 0, s>>>(vt, Bl, cfg ? 1 : 0, gs, dsig, g, lat);
+  return cudaGetLastError();
+}
+
+__global__ void cfg_kernel(const float* __restrict__ vc, const float* __restrict__ vu, float gs, float* v,
+                           int64_t n) {
+  const int64_t n4 = n / 4;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  const bool vec = ((reinterpret_cast<uintptr_t>(vc) | reinterpret_cast<uintptr_t>(vu) |
+                     reinterpret_cast<uintptr_t>(v)) & 15) == 0;
+  int64_t done = 0;
+  if (vec) {
+    for (int64_t i = i0; i < n4; i += stride) {
+      const float4 a = reinterpret_cast<const float4*>(vc)[i], b = reinterpret_cast<const float4*>(vu)[i];
+      reinterpret_cast<float4*>(v)[i] =
+          make_float4(fmaf(gs, a.x - b.x, b.x), fmaf(gs, a.y - b.y, b.y), fmaf(gs, a.z - b.z, b.z),
+                      fmaf(gs, a.w - b.w, b.w));
+    }
+    done = n4 * 4;
+  }
+  for (int64_t i = done + i0; i < n; i += stride) v[i] = fmaf(gs, vc[i] - vu[i], vu[i]);
+}
+
+__global__ void euler_kernel_(float* x, const float* __restrict__ v, float dsig, int64_t n) {
+  const int64_t n4 = n / 4;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(v)) & 15) == 0;
+  int64_t done = 0;
+  if (vec) {
+    for (int64_t i = i0; i < n4; i += stride) {
+      float4 a = reinterpret_cast<float4*>(x)[i];
+      const float4 b = reinterpret_cast<const float4*>(v)[i];
+      a.x = fmaf(dsig, b.x, a.x); a.y = fmaf(dsig, b.y, a.y);
+      a.z = fmaf(dsig, b.z, a.z); a.w = fmaf(dsig, b.w, a.w);
+      reinterpret_cast<float4*>(x)[i] = a;
+    }
+    done = n4 * 4;
+  }
+  for (int64_t i = done + i0; i < n; i += stride) x[i] = fmaf(dsig, v[i], x[i]);
+}
+
+cudaError_t cfg_combine_kernel(const float* vc, const float* vu, float g, float* v, int64_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  cfg_kernel<<<blocks_for(n / 4 + 1, 256), 256, 0, s>>>(vc, vu, g, v, n);
+  return cudaGetLastError();
+}
+
+cudaError_t euler_kernel(float* x, const float* v, float dsig, int64_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  euler_kernel_<<<blocks_for(n / 4 + 1, 256), 256, 0, s>>>(x, v, dsig, n);
+  return cudaGetLastError();
+}
+
+__global__ void f32_to_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* __restrict__ out, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = __float2bfloat16_rn(in[i]);
+}
+
+cudaError_t f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  f32_to_bf16_kernel<<<blocks_for(n, 256), 256, 0, s>>>(in, static_cast<__nv_bfloat16*>(out), n);
+  return cudaGetLastError();
+}
+
+__global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ in, float* __restrict__ out, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = __bfloat162float(in[i]);
+}
+
+cudaError_t bf16_to_f32(const void* in, float* out, int64_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  bf16_to_f32_kernel<<<blocks_for(n, 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in), out, n);
+  return cudaGetLastError();
+}
+
+}  // namespace dit

@@ -1,0 +1,147 @@
+// GEMM epilogues applied to a chunk of NV consecutive columns of one output
+// row while the accumulators are still in registers: bias, GELU (tanh form),
+// gated residual update of the fp32 stream, or the head-major Q/K/V scatter
+// with rotary embedding of interleaved channel pairs.
+#pragma once
+#include <type_traits>
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dit {
+
+template <typename T>
+DIT_DEV T to_act(float v);
+template <>
+DIT_DEV float to_act<float>(float v) { return v; }
+template <>
+DIT_DEV __nv_bfloat16 to_act<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// Store NV values to dst (16-byte aligned when NV * sizeof(T) >= 16 and the
+// caller passes an aligned address).
+template <typename T, int NV>
+DIT_DEV void store_chunk(T* dst, const float (&v)[NV]) {
+  if constexpr (std::is_same<T, float>::value) {
+    if constexpr (NV % 4 == 0) {
+#pragma unroll
+      for (int j = 0; j < NV; j += 4)
+        *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < NV; ++j) dst[j] = v[j];
+    }
+  } else {
+    if constexpr (NV % 8 == 0) {
+#pragma unroll
+      for (int j = 0; j < NV; j += 8) {
+        uint4 u;
+        u.x = pack_bf16x2(v[j + 0], v[j + 1]);
+        u.y = pack_bf16x2(v[j + 2], v[j + 3]);
+        u.z = pack_bf16x2(v[j + 4], v[j + 5]);
+        u.w = pack_bf16x2(v[j + 6], v[j + 7]);
+        *reinterpret_cast<uint4*>(dst + j) = u;
+      }
+    } else if constexpr (NV % 2 == 0) {
+#pragma unroll
+      for (int j = 0; j < NV; j += 2) *reinterpret_cast<uint32_t*>(dst + j) = pack_bf16x2(v[j], v[j + 1]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < NV; ++j) dst[j] = __float2bfloat16_rn(v[j]);
+    }
+  }
+}
+
+template <bool kFast>
+DIT_DEV float gelu_tanh(float x) {
+  const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+  const float u = k0 * (x + 0.044715f * x * x * x);
+  const float t = kFast ? tanh_approx(u) : tanhf(u);
+  return 0.5f * x * (1.0f + t);
+}
+
+// Apply the epilogue to columns [col0, col0 + NV) of row `row` (row < M).
+// col0 is a multiple of NV; for EPI_HEADS NV divides hd and D.
+template <typename ActT, int NV>
+DIT_DEV void epilogue_chunk(const EpiParams& p, int64_t row, int col0, float (&v)[NV]) {
+  constexpr bool kFast = std::is_same<ActT, __nv_bfloat16>::value;
+  const bool full = col0 + NV <= p.N;
+  if (p.bias) {
+    if (full) {
+#pragma unroll
+      for (int j = 0; j < NV; ++j) v[j] += __ldg(p.bias + col0 + j);
+    } else {
+#pragma unroll
+      for (int j = 0; j < NV; ++j)
+        if (col0 + j < p.N) v[j] += __ldg(p.bias + col0 + j);
+    }
+  }
+  switch (p.kind) {
+    case EPI_F32: {
+      float* o = static_cast<float*>(p.out) + row * p.ldo + col0;
+      if (full && (p.ldo % 4 == 0)) {
+        store_chunk<float, NV>(o, v);
+      } else {
+        for (int j = 0; j < NV; ++j)
+          if (col0 + j < p.N) o[j] = v[j];
+      }
+      break;
+    }
+    case EPI_GELU:
+#pragma unroll
+      for (int j = 0; j < NV; ++j) v[j] = gelu_tanh<kFast>(v[j]);
+      [[fallthrough]];
+    case EPI_ACT: {
+      ActT* o = static_cast<ActT*>(p.out) + row * p.ldo + col0;
+      if (full && (p.ldo % 8 == 0)) {
+        store_chunk<ActT, NV>(o, v);
+      } else {
+        for (int j = 0; j < NV; ++j)
+          if (col0 + j < p.N) o[j] = to_act<ActT>(v[j]);
+      }
+      break;
+    }
+    case EPI_RESID: {
+      float* xr = p.x + row * (int64_t)p.N + col0;
+      const float* g = p.gate ? p.gate + (row / p.rows_per_batch) * p.gate_bstride + col0 : nullptr;
+      if (full && (p.N % 4 == 0) && (NV % 4 == 0)) {
+#pragma unroll
+        for (int j = 0; j < NV; j += 4) {
+          float4 xv = *reinterpret_cast<float4*>(xr + j);
+          float4 gv = g ? __ldg(reinterpret_cast<const float4*>(g + j)) : make_float4(1.f, 1.f, 1.f, 1.f);
+          xv.x += gv.x * v[j + 0];
+          xv.y += gv.y * v[j + 1];
+          xv.z += gv.z * v[j + 2];
+          xv.w += gv.w * v[j + 3];
+          *reinterpret_cast<float4*>(xr + j) = xv;
+        }
+      } else {
+        for (int j = 0; j < NV; ++j)
+          if (col0 + j < p.N) xr[j] += (g ? g[j] : 1.0f) * v[j];
+      }
+      break;
+    }
+    case EPI_HEADS: {
+      const int sec = col0 / p.D;
+      const int cc = col0 - sec * p.D;
+      const int h = cc / p.hd;
+      const int c = cc - h * p.hd;
+      const int64_t b = row / p.rows_per_batch;
+      const int t = (int)(row - b * p.rows_per_batch);
+      if (p.rope && ((p.rope_mask >> sec) & 1)) {
+        const float2* cs = p.rope + (int64_t)t * (p.hd / 2) + c / 2;
+#pragma unroll
+        for (int j = 0; j < NV; j += 2) {
+          const float2 r = __ldg(cs + j / 2);
+          const float a = v[j], bb = v[j + 1];
+          v[j] = a * r.x - bb * r.y;
+          v[j + 1] = a * r.y + bb * r.x;
+        }
+      }
+      ActT* o = static_cast<ActT*>(p.dst[sec]) +
+                ((b * p.H + h) * (int64_t)p.seq_total + p.tok_off + t) * p.hd + c;
+      store_chunk<ActT, NV>(o, v);
+      break;
+    }
+  }
+}
+
+}  // namespace dit

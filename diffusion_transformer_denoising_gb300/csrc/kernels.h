@@ -1,0 +1,99 @@
+// Internal launch interface between the C ABI layer (dit_api.cu) and the
+// kernel translation units.  Nothing here is exported from libdit.so.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dit {
+
+// ------------------------------------------------------------------ GEMM
+// C[M, N] = A[M, K] . W[N, K]^T (+ bias), followed by one fused epilogue.
+enum EpiKind : int {
+  EPI_F32 = 0,    // out_f32[row * ldo + col] = acc + bias
+  EPI_ACT = 1,    // out_act[row * ldo + col] = acc + bias       (activation dtype)
+  EPI_GELU = 2,   // out_act[row * ldo + col] = gelu_tanh(acc + bias)
+  EPI_RESID = 3,  // x[row * N + col] += gate[b, col] * (acc + bias)   (gate NULL = 1)
+  EPI_HEADS = 4   // scatter sections of D columns into head-major [B, H, S, hd] (+ RoPE)
+};
+
+struct EpiParams {
+  int kind = EPI_F32;
+  int M = 0, N = 0;
+  const float* bias = nullptr;
+  void* out = nullptr;
+  int64_t ldo = 0;
+  // residual update
+  float* x = nullptr;
+  const float* gate = nullptr;
+  int64_t gate_bstride = 0;
+  int rows_per_batch = 1;  // also used by EPI_HEADS
+  // head-major scatter: column n -> section n / D, head (n % D) / hd, channel n % hd;
+  // row r -> batch r / rows_per_batch, token tok_off + r % rows_per_batch of seq_total
+  void* dst[3] = {nullptr, nullptr, nullptr};
+  int D = 0, hd = 0, H = 0, seq_total = 0, tok_off = 0, rope_mask = 0;
+  const float2* rope = nullptr;  // [rows_per_batch][hd / 2] (cos, sin)
+};
+
+struct GemmArgs {
+  const void* A = nullptr;  // [M, K] row-major, row stride lda elements
+  int64_t M = 0;
+  int K = 0;
+  int64_t lda = 0;
+  const void* W = nullptr;  // [N, K] row-major (row stride K)
+  int N = 0;
+  EpiParams epi;
+};
+
+// fp32 CUDA-core GEMM (test precision).
+cudaError_t gemm_f32(const GemmArgs& g, cudaStream_t s);
+// bf16 tcgen05 GEMM (production precision); err = device error word for
+// bounded waits; num_sms = persistent grid size.
+cudaError_t gemm_bf16_tc(const GemmArgs& g, int* err, int num_sms, cudaStream_t s);
+
+// ------------------------------------------------------------------ attention
+// Q [B, H, Lq, hd], K/V [B, H, Lk, hd] head-major; output token-major rows of
+// width D = H * hd: token t < split goes to o1[b, t], else o2[b, t - split].
+struct AttnArgs {
+  const void* q = nullptr;
+  const void* k = nullptr;
+  const void* v = nullptr;
+  int B = 0, H = 0, Lq = 0, Lk = 0, hd = 0;
+  void* o1 = nullptr;
+  void* o2 = nullptr;
+  int split = 0;
+};
+cudaError_t attention_f32(const AttnArgs& a, cudaStream_t s);
+cudaError_t attention_bf16_tc(const AttnArgs& a, int* err, cudaStream_t s);
+
+// ------------------------------------------------------------------ elementwise
+// h[r, :] = LN(x[r, :]) * (1 + scale[b]) + shift[b], b = r / rows_per_batch;
+// shift/scale NULL = plain LN.  Output bf16 (out_bf16) or fp32.
+cudaError_t ln_modulate(const float* x, int64_t rows, int D, int rows_per_batch, const float* shift,
+                        const float* scale, int64_t mod_bstride, float eps, void* out, bool out_bf16,
+                        cudaStream_t s);
+// Sinusoidal timestep embedding + 2-layer MLP: mod[b, 6D] for each t[b].
+// hidden_scratch: float[batch * D].
+// t_dev NULL: every batch element uses t0.
+cudaError_t timestep_mlp(const float* t_dev, double t0, int batch, int freq_dim, int D, const void* w1, const float* b1,
+                         const void* w2, const float* b2, bool w_bf16, float* hidden_scratch, float* mod,
+                         cudaStream_t s);
+// out[k, b, j, c] = mod[b, j*D + c] + tables[k, j, c] for k < ntab, j < rows
+// (tables contiguous [ntab, rows, D]).
+cudaError_t add_tables(const float* mod, int batch, int D, int rows, const float* tables, int ntab, float* out,
+                       cudaStream_t s);
+// latents [Bl, C, T, H, W] -> tokens [copies * Bl, N, C*pt*ph*pw] (copies of the batch back to back)
+cudaError_t patchify(const float* lat, int Bl, int copies, int C, int T, int H, int W, int pt, int ph, int pw,
+                     void* tokens, bool out_bf16, cudaStream_t s);
+// tokens [B, N, P] -> latents [B, C, T, H, W]
+cudaError_t unpatchify(const float* tok, int B, int C, int T, int H, int W, int pt, int ph, int pw, float* lat,
+                       cudaStream_t s);
+// Fused guidance + Euler + unpatchify over velocity tokens vt [2*Bl or Bl, N, P]:
+// lat += dsig * (vu + g (vc - vu)) (or vc alone when !cfg).
+cudaError_t cfg_euler_tokens(const float* vt, int Bl, bool cfg, float g, float dsig, int C, int T, int H, int W,
+                             int pt, int ph, int pw, float* lat, cudaStream_t s);
+cudaError_t cfg_combine_kernel(const float* vc, const float* vu, float g, float* v, int64_t n, cudaStream_t s);
+cudaError_t euler_kernel(float* x, const float* v, float dsig, int64_t n, cudaStream_t s);
+cudaError_t f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t s);
+cudaError_t bf16_to_f32(const void* in, float* out, int64_t n, cudaStream_t s);
+
+}  // namespace dit

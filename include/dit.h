@@ -1,0 +1,215 @@
+/*
+ * dit.h -- C ABI of the GB300 denoiser stage (libdit.so).
+ *
+ * The denoiser stage is the DiT forward loop together with the scheduler
+ * stepping it drives (SGLang-Diffusion "Disaggregated Diffusion Pipeline",
+ * Quick Start, role table: "denoiser").  Its inputs are the latents, the
+ * timestep / sigma schedule in the exact order used, the positive prompt
+ * embeddings and, when classifier-free guidance is on, the negative ones
+ * (SGLang-Diffusion "Support New Diffusion Models", section 4, table of the
+ * fields DenoisingStage requires).  The network is called with
+ * hidden_states / encoder_hidden_states / timestep, once with the positive
+ * and once with the negative condition (same page, section 2 "Pipeline
+ * Config").  Velocities are flow predictions integrated with a flow-matching
+ * Euler step on a shifted sigma schedule (stable-diffusion.cpp "Model
+ * Configuration Conventions", "Sampling And Geometry").
+ *
+ * Conventions for every call:
+ *   - Every pointer documented "device" is a CUDA device pointer owned by the
+ *     caller; the library never frees it.  Host pointers are read before the
+ *     call returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously on it; results are ready once
+ *     the stream is synchronised (dit_synchronize does that and also reports
+ *     a device-side timeout).
+ *   - Argument errors are detected on the host before anything is launched;
+ *     outputs are then left untouched.  Nothing aborts the process: every
+ *     failure is a status code, with a message from dit_last_error().
+ *   - There is no CPU fallback and no silent precision change: a call the
+ *     GPU path cannot serve returns an error.
+ *   - Floating-point tensors crossing the ABI are float32, row-major, densely
+ *     packed, in the layouts given per call.  B is the batch of network
+ *     passes; in the loop B = 2 x requests with CFG (conditional passes
+ *     first, then unconditional ones).
+ */
+#ifndef DIT_H
+#define DIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DIT_OK = 0,
+  DIT_ERR_INVALID_ARG = 1, /* bad pointer, value, schedule or flag          */
+  DIT_ERR_SHAPE = 2,       /* inconsistent or unsupported tensor shape      */
+  DIT_ERR_NOT_LOADED = 3,  /* forward called before a complete weight load  */
+  DIT_ERR_OOM = 4,         /* device allocation failed                      */
+  DIT_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed             */
+  DIT_ERR_TIMEOUT = 6      /* a kernel gave up a bounded wait (see dit_synchronize) */
+} dit_status;
+
+enum { DIT_PREC_BF16 = 0, DIT_PREC_F32 = 1 };
+enum { DIT_COND_CROSS = 0, DIT_COND_JOINT = 1 };
+enum { DIT_DTYPE_F32 = 0, DIT_DTYPE_BF16 = 1 };
+/* dit_denoise_loop flags */
+enum { DIT_LOOP_PARTIAL_SCHEDULE = 1 /* allow sigmas[0] != 1 or sigmas[n] != 0 */ };
+
+/*
+ * Model configuration, copied by dit_create.  Mirrors the C++ "*Config"
+ * convention of stable-diffusion.cpp "Model Configuration Conventions"
+ * (Config Types / Runner And Model Responsibilities): derived once, passed to
+ * the model, never re-scanned.
+ *   in_channels   latent channels C (stable-diffusion.cpp ModelGeometry latent_channels)
+ *   patch[3]      patch size (pt, ph, pw) over (T, H, W) of the latent
+ *   hidden        D = heads * head_dim
+ *   mlp           F, width of the GELU MLP
+ *   cond_dim      Dc, width of a condition token (must equal hidden in joint mode)
+ *   freq_dim      width of the sinusoidal timestep embedding (even)
+ *   rope_axes[3]  rotary channels per axis (t, h, w), each even, summing to
+ *                 head_dim, or all zero for no rotation
+ *   cond_mode     DIT_COND_CROSS: cross-attention to condition tokens;
+ *                 DIT_COND_JOINT: dual-stream joint attention with them
+ *   precision     DIT_PREC_BF16: bf16 weights/activations, fp32 accumulate
+ *                 (tcgen05 tensor cores; requires head_dim == 128);
+ *                 DIT_PREC_F32: fp32 everywhere (test mode, CUDA cores)
+ *   ln_eps, rope_theta, timestep_scale (t = timestep_scale * sigma)
+ */
+typedef struct {
+  int32_t in_channels;
+  int32_t patch[3];
+  int32_t hidden;
+  int32_t heads;
+  int32_t head_dim;
+  int32_t mlp;
+  int32_t depth;
+  int32_t cond_dim;
+  int32_t freq_dim;
+  int32_t rope_axes[3];
+  int32_t cond_mode;
+  int32_t precision;
+  float ln_eps;
+  float rope_theta;
+  float timestep_scale;
+} dit_config;
+
+/* One named parameter for dit_load_weights.  `data` may be a host or a
+ * device pointer (unified addressing decides); dtype is DIT_DTYPE_F32 or
+ * DIT_DTYPE_BF16; shape[0..ndim) must equal the expected shape. */
+typedef struct {
+  const char* name;
+  int32_t ndim;
+  int64_t shape[4];
+  int32_t dtype;
+  const void* data;
+} dit_tensor;
+
+typedef struct dit_model dit_model;
+
+/* Create a model on CUDA device `device`.  Validates the configuration
+ * (DIT_ERR_INVALID_ARG / DIT_ERR_SHAPE) before touching the GPU. */
+dit_status dit_create(const dit_config* cfg, int device, dit_model** out);
+
+/* Copy parameters into the model's own device arena (converted to the
+ * model's storage precision).  Strict: every name must be a known parameter,
+ * appear once across all calls, and have the expected shape; otherwise
+ * DIT_ERR_SHAPE and nothing of this call is kept (SGLang-Diffusion "Support
+ * New Diffusion Models", "Reuse component loaders": strict key and shape
+ * checks, fail instead of falling back).  The forward calls return
+ * DIT_ERR_NOT_LOADED until every parameter has been loaded.  Synchronous. */
+dit_status dit_load_weights(dit_model* m, const dit_tensor* tensors, int n);
+
+/* Host-only queries on a configuration (no GPU needed): the number of
+ * parameters a model of this configuration expects, and the name (copied into
+ * name_buf, NUL-terminated) and shape of the i-th, in load order.  Linear
+ * weights are [out_features, in_features]; each block carries a learned
+ * [6, hidden] modulation table (shift1, scale1, gate1, shift2, scale2,
+ * gate2) added to the shared timestep modulation. */
+int dit_num_params(const dit_config* cfg);
+dit_status dit_param_info(const dit_config* cfg, int i, char* name_buf, int buf_len, int32_t* ndim,
+                          int64_t shape[4]);
+
+/* a1: timestep embedding -> MLP -> shared modulation.
+ *   t_host  host float[batch], the network timestep per batch element
+ *   mod     device float[batch, 6*hidden] output */
+dit_status dit_timestep_modulation(dit_model* m, const float* t_host, int batch, float* mod, void* stream);
+
+/* a2: patchify + patch embedding.
+ *   latents device float[batch, C, T, H, W]; latent_thw = {T, H, W}, each
+ *           divisible by the patch size (else DIT_ERR_SHAPE)
+ *   x       device float[batch, N, hidden] output, N = (T/pt)(H/ph)(W/pw),
+ *           tokens in row-major (t, h, w) grid order */
+dit_status dit_patch_embed(dit_model* m, const float* latents, int batch, const int32_t latent_thw[3],
+                           float* x, void* stream);
+
+/* a3-a9: one DiT block, in place on the residual stream(s).
+ *   block   0 .. depth-1
+ *   x       device float[batch, N, hidden], image/video token stream, in/out
+ *   xc      joint mode: device float[batch, cond_len, hidden], condition-token
+ *           stream, in/out; cross mode: must be NULL
+ *   mod     device float[batch, 6*hidden], the shared timestep modulation from
+ *           dit_timestep_modulation (the block adds its own table)
+ *   cond    cross mode: device float[batch, cond_len, cond_dim] condition
+ *           tokens; joint mode: must be NULL
+ *   grid    token grid {T/pt, H/ph, W/pw} (N = product), sets RoPE positions */
+dit_status dit_block_forward(dit_model* m, int block, float* x, float* xc, const float* mod,
+                             const float* cond, int batch, const int32_t grid[3], int cond_len,
+                             void* stream);
+
+/* a10: final layer (LN + head modulation + linear) and unpatchify.
+ *   x  device float[batch, N, hidden];  mod as above
+ *   v  device float[batch, C, T, H, W] output velocity */
+dit_status dit_final_layer(dit_model* m, const float* x, const float* mod, int batch,
+                           const int32_t latent_thw[3], float* v, void* stream);
+
+/* a11 (first half): classifier-free guidance v = vu + g (vc - vu) over n
+ * floats (device pointers; v may alias vc or vu). */
+dit_status cfg_combine(const float* vc, const float* vu, float g, float* v, int64_t n, void* stream);
+
+/* a11 (second half): flow-matching Euler update x += (sigma_next - sigma) v
+ * over n floats, in place on device x. */
+dit_status flow_euler_step(float* x, const float* v, float sigma, float sigma_next, int64_t n,
+                           void* stream);
+
+/* The whole denoiser stage for `batch` requests.
+ *   latents  device float[batch, C, T, H, W], initial noise in, denoised out
+ *   cond     device float[batch, cond_len, cond_dim] positive condition
+ *   uncond   device float[batch, cond_len, cond_dim] negative condition, or
+ *            NULL for no guidance (then `guidance` must be 1)
+ *   sigmas   host float[n_steps + 1], already shifted, strictly decreasing,
+ *            sigmas[0] == 1 and sigmas[n_steps] == 0 unless
+ *            DIT_LOOP_PARTIAL_SCHEDULE is set (resuming part of a schedule)
+ *   Per step i: t = timestep_scale * sigmas[i]; v from the network on the
+ *   2*batch conditional+unconditional passes; v = vu + g (vc - vu);
+ *   latents += (sigmas[i+1] - sigmas[i]) v.  Condition-token keys/values of
+ *   cross-attention are computed once per call (they do not depend on the
+ *   step). */
+dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, const int32_t latent_thw[3],
+                            const float* cond, const float* uncond, int cond_len,
+                            const float* sigmas, int n_steps, float guidance, uint32_t flags,
+                            void* stream);
+
+/* Synchronise `stream` and report DIT_ERR_TIMEOUT if a kernel of this model
+ * abandoned a bounded wait since the last check (its outputs are then
+ * invalid; the flag is cleared). */
+dit_status dit_synchronize(dit_model* m, void* stream);
+
+/* Bytes of device memory held by the model (weights + workspace). */
+int64_t dit_device_bytes(const dit_model* m);
+
+void dit_destroy(dit_model* m);
+const char* dit_status_string(dit_status s);
+/* Message of the last failing call on this thread ("" if none). */
+const char* dit_last_error(void);
+
+/* Test hook: make the next `n`-th device allocation of any model fail with
+ * DIT_ERR_OOM (0 disables).  Host-side only; used to test failure paths. */
+void dit_debug_fail_alloc_after(int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DIT_H */

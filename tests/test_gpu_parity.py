@@ -1,0 +1,277 @@
+"""Parity of the CUDA path (called through the C ABI) with the CPU oracle on
+the same seeded inputs."""
+import numpy as np
+import pytest
+
+from diffusion_transformer_denoising_gb300 import dit, synth
+from oracle import dit_oracle as O
+from tests.gpu_util import (COS_BF16_LOOP, TOL_BF16_BLOCK, TOL_F32, cosine, dev, empty, host, make_model,
+                            rel_max_err, small_bf16_cfg)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    cfg = synth.config("tiny")
+    W = synth.make_weights(cfg, seed=0)
+    m = make_model(cfg, W)
+    yield cfg, W, m
+    m.close()
+
+
+# ------------------------------------------------------------------ tiny, fp32
+def test_tiny_timestep_modulation(tiny):
+    cfg, W, m = tiny
+    ts = np.array([0.0, 250.0, 700.0, 1000.0], np.float32)
+    out = empty(4, 6 * cfg["hidden"])
+    m.dit_timestep_modulation(ts, out)
+    got = host(out)
+    for i, t in enumerate(ts):
+        ref = O.timestep_modulation(float(t), W, cfg)
+        assert rel_max_err(got[i], ref) < TOL_F32
+
+
+def test_tiny_patch_embed_and_final_layer(tiny):
+    cfg, W, m = tiny
+    lat = synth.make_latent(cfg, batch=2, seed=5)
+    thw = cfg["latent"]
+    x = empty(2, 64, cfg["hidden"])
+    m.dit_patch_embed(dev(lat), 2, thw, x)
+    gx = host(x)
+    for b in range(2):
+        assert rel_max_err(gx[b], O.patch_embed(lat[b], W, cfg)) < TOL_F32
+    mod = dev(np.stack([O.timestep_modulation(t, W, cfg) for t in (300.0, 900.0)]))
+    v = empty(2, *lat.shape[1:])
+    m.dit_final_layer(x, mod, 2, thw, v)
+    gv = host(v)
+    for b, t in enumerate((300.0, 900.0)):
+        mm = O.timestep_modulation(t, W, cfg)
+        ref = O.unpatchify(O.final_layer(gx[b], mm, W, cfg), cfg["patch"], lat.shape[1:])
+        assert rel_max_err(gv[b], ref) < TOL_F32
+
+
+@pytest.mark.parametrize("block", [0, 1])
+def test_tiny_block(tiny, block):
+    cfg, W, m = tiny
+    rng = np.random.default_rng(40 + block)
+    x0 = rng.standard_normal((2, 64, cfg["hidden"])).astype(np.float32)
+    ctx = synth.make_cond(cfg, batch=2, seed=7)
+    mods = np.stack([O.timestep_modulation(t, W, cfg) for t in (123.0, 876.0)])
+    x = dev(x0)
+    m.dit_block_forward(block, x, None, dev(mods), dev(ctx), 2, (1, 8, 8), 16)
+    got = host(x)
+    for b in range(2):
+        ref = O.block_cross(x0[b], mods[b], ctx[b], W, block, cfg, (1, 8, 8))
+        assert rel_max_err(got[b], ref) < TOL_F32
+        # the block's own update, not just the carried residual
+        assert rel_max_err(got[b] - x0[b], ref - x0[b]) < 10 * TOL_F32
+
+
+def test_tiny_denoise_loop(tiny):
+    cfg, W, m = tiny
+    lat = synth.make_latent(cfg, batch=1, seed=1)
+    cond = synth.make_cond(cfg, batch=1, seed=2)
+    unc = np.zeros_like(cond)
+    sig = O.shift_sigma(O.sigma_schedule(cfg["steps"]), cfg["shift"]).astype(np.float32)
+    x = dev(lat)
+    m.dit_denoise_loop(x, 1, cfg["latent"], dev(cond), dev(unc), 16, sig, cfg["guidance"])
+    m.dit_synchronize()
+    got = host(x)[0]
+    ref = O.denoise_loop(lat[0], cond[0], unc[0], W, cfg, sig.astype(np.float64), cfg["guidance"])
+    assert rel_max_err(got, ref) < TOL_F32
+    # the denoised latent moved away from the noise: compare the displacement too
+    assert rel_max_err(got - lat[0], ref - lat[0]) < 10 * TOL_F32
+
+
+def test_tiny_loop_twice_is_bitwise_identical(tiny):
+    cfg, W, m = tiny
+    lat = synth.make_latent(cfg, batch=1, seed=3)
+    cond = dev(synth.make_cond(cfg, batch=1, seed=4))
+    unc = dev(np.zeros((1, 16, 128), np.float32))
+    sig = O.shift_sigma(O.sigma_schedule(4), 3.0).astype(np.float32)
+    outs = []
+    for _ in range(2):
+        x = dev(lat)
+        m.dit_denoise_loop(x, 1, cfg["latent"], cond, unc, 16, sig, 5.0)
+        outs.append(host(x))
+    assert np.array_equal(outs[0], outs[1])
+
+
+# ------------------------------------------------------------------ guidance / Euler
+@pytest.mark.parametrize("n", [1, 7, 4096, 100003])
+def test_cfg_combine_and_euler(n):
+    rng = np.random.default_rng(n)
+    vc, vu, x = (rng.standard_normal(n).astype(np.float32) for _ in range(3))
+    v = empty(n)
+    dit.cfg_combine(dev(vc), dev(vu), 4.0, v, n)
+    np.testing.assert_allclose(host(v), O.cfg_combine(vc, vu, 4.0), rtol=0, atol=1e-5)
+    xd = dev(x)
+    dit.flow_euler_step(xd, v, 0.75, 0.5, n)
+    np.testing.assert_allclose(host(xd), O.euler_step(x, O.cfg_combine(vc, vu, 4.0), 0.75, 0.5), rtol=0, atol=1e-5)
+
+
+def test_cfg_scale_one_gives_conditional():
+    rng = np.random.default_rng(3)
+    vc, vu = (rng.standard_normal(1000).astype(np.float32) for _ in range(2))
+    v = empty(1000)
+    dit.cfg_combine(dev(vc), dev(vu), 1.0, v, 1000)
+    np.testing.assert_allclose(host(v), vc, rtol=0, atol=2e-7 * 8)
+
+
+# ------------------------------------------------------------------ bf16, tensor cores
+@pytest.fixture(scope="module")
+def small_cross():
+    cfg = small_bf16_cfg(synth.COND_CROSS)
+    W = synth.make_weights(cfg, seed=11)
+    m = make_model(cfg, W)
+    yield cfg, W, m
+    m.close()
+
+
+@pytest.fixture(scope="module")
+def small_joint():
+    cfg = small_bf16_cfg(synth.COND_JOINT)
+    W = synth.make_weights(cfg, seed=12)
+    m = make_model(cfg, W)
+    yield cfg, W, m
+    m.close()
+
+
+def test_bf16_patch_embed(small_cross):
+    cfg, W, m = small_cross
+    thw = (3, 20, 26)      # grid 3 x 10 x 13 = 390 tokens: ragged GEMM tail
+    lat = synth.make_latent(cfg, batch=2, seed=8, latent=thw)
+    x = empty(2, 390, cfg["hidden"])
+    m.dit_patch_embed(dev(lat), 2, thw, x)
+    m.dit_synchronize()
+    gx = host(x)
+    for b in range(2):
+        lat_b = synth.round_bf16(lat[b]).astype(np.float64)   # the tensor-core path reads bf16 tokens
+        assert rel_max_err(gx[b], O.patch_embed(lat_b, W, cfg)) < 1e-3
+
+
+def test_bf16_final_layer(small_cross):
+    cfg, W, m = small_cross
+    thw = (3, 20, 26)
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((2, 390, cfg["hidden"])).astype(np.float32)
+    mods = np.stack([O.timestep_modulation(t, W, cfg) for t in (100.0, 600.0)])
+    v = empty(2, cfg["in_channels"], *thw)
+    m.dit_final_layer(dev(x), dev(mods), 2, thw, v)
+    m.dit_synchronize()
+    gv = host(v)
+    for b in range(2):
+        ref = O.unpatchify(O.final_layer(x[b], mods[b], W, cfg), cfg["patch"], (cfg["in_channels"],) + thw)
+        assert rel_max_err(gv[b], ref) < TOL_BF16_BLOCK
+
+
+@pytest.mark.parametrize("grid,L", [((3, 10, 13), 77), ((1, 16, 16), 128), ((2, 9, 7), 5)])
+def test_bf16_cross_block(small_cross, grid, L):
+    cfg, W, m = small_cross
+    N = int(np.prod(grid))
+    rng = np.random.default_rng(N + L)
+    x0 = (rng.standard_normal((2, N, cfg["hidden"])) * 0.5).astype(np.float32)
+    ctx = synth.make_cond(cfg, batch=2, seed=L, length=L)
+    mods = np.stack([O.timestep_modulation(t, W, cfg) for t in (200.0, 950.0)])
+    x = dev(x0)
+    m.dit_block_forward(1, x, None, dev(mods), dev(ctx), 2, grid, L)
+    m.dit_synchronize()
+    got = host(x)
+    for b in range(2):
+        ref = O.block_cross(x0[b], mods[b], ctx[b], W, 1, cfg, grid)
+        assert rel_max_err(got[b], ref) < TOL_BF16_BLOCK
+        assert rel_max_err(got[b] - x0[b], ref - x0[b]) < 5 * TOL_BF16_BLOCK
+
+
+@pytest.mark.parametrize("grid,L", [((1, 12, 20), 64), ((1, 7, 9), 33)])
+def test_bf16_joint_block(small_joint, grid, L):
+    cfg, W, m = small_joint
+    N = int(np.prod(grid))
+    rng = np.random.default_rng(N + 3 * L)
+    x0 = (rng.standard_normal((2, N, cfg["hidden"])) * 0.5).astype(np.float32)
+    xc0 = synth.make_cond(cfg, batch=2, seed=L, length=L)
+    mods = np.stack([O.timestep_modulation(t, W, cfg) for t in (333.0, 777.0)])
+    x, xc = dev(x0), dev(xc0)
+    m.dit_block_forward(0, x, xc, dev(mods), None, 2, grid, L)
+    m.dit_synchronize()
+    gx, gc = host(x), host(xc)
+    for b in range(2):
+        rx, rc = O.block_joint(x0[b], xc0[b], mods[b], W, 0, cfg, grid)
+        assert rel_max_err(gx[b], rx) < TOL_BF16_BLOCK
+        assert rel_max_err(gc[b], rc) < TOL_BF16_BLOCK
+
+
+@pytest.mark.parametrize("mode", [synth.COND_CROSS, synth.COND_JOINT])
+def test_bf16_denoise_loop(mode, small_cross, small_joint):
+    cfg, W, m = small_cross if mode == synth.COND_CROSS else small_joint
+    thw = (2, 12, 18) if mode == synth.COND_CROSS else (1, 24, 20)
+    L = 40
+    lat = synth.make_latent(cfg, batch=1, seed=21, latent=thw)
+    cond = synth.make_cond(cfg, batch=1, seed=22, length=L)
+    unc = np.zeros_like(cond)
+    sig = O.shift_sigma(O.sigma_schedule(3), 3.0).astype(np.float32)
+    x = dev(lat)
+    m.dit_denoise_loop(x, 1, thw, dev(cond), dev(unc), L, sig, 4.0)
+    m.dit_synchronize()
+    got = host(x)[0]
+    ref = O.denoise_loop(lat[0], cond[0], unc[0], W, cfg, sig.astype(np.float64), 4.0)
+    assert cosine(got, ref) >= COS_BF16_LOOP
+    assert cosine(got - lat[0], ref - lat[0]) >= 0.99
+
+
+# ------------------------------------------------------------------ failure paths
+def test_forward_before_load_is_rejected():
+    cfg = synth.config("tiny")
+    m = dit.DiT(cfg)
+    with pytest.raises(dit.DitError) as e:
+        m.dit_timestep_modulation(np.zeros(1, np.float32), empty(1, 768))
+    assert e.value.status == dit.DIT_ERR_NOT_LOADED
+    m.close()
+
+
+def test_bad_schedule_and_missing_uncond(tiny):
+    cfg, W, m = tiny
+    x = dev(synth.make_latent(cfg))
+    cond = dev(synth.make_cond(cfg))
+    good = O.shift_sigma(O.sigma_schedule(4), 3.0).astype(np.float32)
+    for sig, unc, g in ((good[::-1].copy(), cond, 5.0),          # reversed timesteps
+                        (good, None, 5.0),                         # CFG on without negatives
+                        (good[:-1].copy(), cond, 5.0)):            # does not end at 0
+        with pytest.raises(dit.DitError) as e:
+            m.dit_denoise_loop(x, 1, cfg["latent"], cond, unc, 16, sig, g)
+        assert e.value.status == dit.DIT_ERR_INVALID_ARG
+    with pytest.raises(dit.DitError) as e:
+        m.dit_denoise_loop(x, 1, (1, 15, 16), cond, cond, 16, good, 5.0)   # not divisible by the patch
+    assert e.value.status == dit.DIT_ERR_SHAPE
+    # resuming part of a schedule is allowed with the flag
+    m.dit_denoise_loop(x, 1, cfg["latent"], cond, cond, 16, good[1:].copy(), 5.0, flags=dit.LOOP_PARTIAL_SCHEDULE)
+    m.dit_synchronize()
+
+
+def test_strict_weight_loading():
+    cfg = synth.config("tiny")
+    W = synth.make_weights(cfg)
+    m = dit.DiT(cfg)
+    bad = dict(W)
+    bad["head.bias"] = np.zeros(3, np.float32)
+    with pytest.raises(dit.DitError) as e:
+        m.load_weights(bad, chunk=10**6)
+    assert e.value.status == dit.DIT_ERR_SHAPE
+    with pytest.raises(dit.DitError) as e:
+        m.load_weights({"blocks.9.attn.qkv.weight": np.zeros((384, 128), np.float32)})
+    assert e.value.status == dit.DIT_ERR_SHAPE
+    m.load_weights(W, chunk=10**6)           # nothing of the failed calls was kept
+    with pytest.raises(dit.DitError):
+        m.load_weights({"head.bias": W["head.bias"]})   # loaded twice
+    m.close()
+
+
+def test_injected_allocation_failure():
+    cfg = synth.config("tiny")
+    dit.dit_debug_fail_alloc_after(1)
+    with pytest.raises(dit.DitError) as e:
+        dit.DiT(cfg)
+    assert e.value.status == dit.DIT_ERR_OOM
+    dit.dit_debug_fail_alloc_after(0)
+    dit.DiT(cfg).close()
