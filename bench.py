@@ -1,0 +1,422 @@
+#!/usr/bin/env python
+"""Throughput of the denoiser stage (DiT forward loop + CFG + flow-Euler) on
+GB300, printed as one JSON line.
+
+A step is one denoising step of the whole hot path: timestep MLP and
+modulation tables, patch embedding, every DiT block for the conditional and
+unconditional passes (batch 2), the final layer, guidance and the Euler
+update.  Default workload: the 30-block Wan2.1-1.3B-shaped video DiT on an
+81-frame 480x832 request (16 x 21 x 60 x 104 latent, 32760 tokens, 512 text
+tokens), random bf16 weights, synthetic inputs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload video|image]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+With N > 1 (torchrun), each rank denoises its own request on its own GPU
+(independent replicas, no collective on the data path); the timing is the
+maximum over ranks and the value counts every rank's steps.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from diffusion_transformer_denoising_gb300 import synth  # noqa: E402
+
+METRIC = "denoise steps/s per config; attention+GEMM TFLOP/s as % of GB300 BF16 peak"
+# The pages' only figure for this path: 50 denoising steps of Wan2.1-T2V-1.3B
+# (81 frames, 832x480) in 312.8 s on one H200 with layerwise offload.
+PAGES_STEPS_PER_S = {"video": 50 / 312.8}
+
+WORKLOADS = {
+    "video": dict(cfg="video", desc="30-block video DiT (hidden 1536, 12x128 heads, MLP 8960), "
+                                    "latent 16x21x60x104 -> 32760 tokens, 512 text tokens, CFG pair (batch 2)"),
+    "image": dict(cfg="image", desc="30-block dual-stream image DiT (hidden 3072, 24x128 heads, MLP 12288), "
+                                    "latent 16x128x128 -> 4096 tokens + 512 joint condition tokens, CFG pair"),
+}
+
+# ncu DRAM traffic (read + write bytes per launch) of the dominant kernel,
+# valid only for the exact kernel source it was captured on.
+TRAFFIC = {
+    # kernel source file -> (sha256 of the source, workload, bytes per launch)
+}
+
+
+def step_flops(cfg: dict, B: int, N: int, L: int) -> dict:
+    """Algorithmic FLOPs of one step: 2*MACs of every block GEMM plus QK^T and
+    PV of attention, split by kind.  Cross-attention keys/values are computed
+    once per loop call and are not part of a step."""
+    D, F, H, hd, depth = cfg["hidden"], cfg["mlp"], cfg["heads"], cfg["head_dim"], cfg["depth"]
+    if cfg["cond_mode"] == synth.COND_CROSS:
+        gemm = 2 * B * N * D * (3 * D + D + D + D + 2 * F)
+        attn_self = 4 * B * H * N * N * hd
+        attn_cross = 4 * B * H * N * L * hd
+    else:
+        S = N + L
+        gemm = 2 * B * S * D * (3 * D + D + 2 * F)
+        attn_self = 4 * B * H * S * S * hd
+        attn_cross = 0
+    return dict(gemm=depth * gemm, attn_self=depth * attn_self, attn_cross=depth * attn_cross,
+                total=depth * (gemm + attn_self + attn_cross), attn_self_per_launch=attn_self)
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sustained=d["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.p = None
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                       "-lms", "200", "-i", gpu_id], stdout=subprocess.PIPE,
+                                      stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def cpu_oracle_sample(workload: str, reps: int = 1) -> dict:
+    """Time the CPU oracle on a bounded sample of one step: one block at two
+    sampled query-row counts (keys/values over all tokens), split into a fixed
+    and a per-row cost, extrapolated to a full step (all rows, every block,
+    both CFG passes).  Returns seconds per step and the description."""
+    from oracle import dit_oracle as O
+    cfg = synth.config(WORKLOADS[workload]["cfg"])
+    W = synth.make_weights(cfg, seed=0, blocks=[0])
+    grid = synth.grid(cfg)
+    N, L, D = int(np.prod(grid)), cfg["cond_len"], cfg["hidden"]
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((N, D)).astype(np.float32) * 0.5
+    ctx = synth.make_cond(cfg, seed=2)[0]
+    m = O.timestep_modulation(700.0, W, cfg)
+    angles = O.rope_angles(O.token_positions(grid), cfg["rope_axes"], cfg["rope_theta"])
+    r1, r2 = 128, 384
+    times = {r1: [], r2: []}
+    for _ in range(reps):
+        for r in (r1, r2):
+            rows = np.linspace(0, N - 1, r).astype(np.int64)
+            t0 = time.perf_counter()
+            if cfg["cond_mode"] == synth.COND_CROSS:
+                O.block_cross(x, m, ctx, W, 0, cfg, grid, rows=rows, angles=angles)
+            else:
+                O.block_joint(x, ctx, m, W, 0, cfg, grid, rows=rows + L, angles=angles)
+            times[r].append(time.perf_counter() - t0)
+    t1, t2 = min(times[r1]), min(times[r2])
+    per_row = max((t2 - t1) / (r2 - r1), 0.0)
+    fixed = max(t1 - r1 * per_row, 0.0)
+    rows_all = N if cfg["cond_mode"] == synth.COND_CROSS else N + L
+    t_block = fixed + rows_all * per_row
+    t_step = 2 * cfg["depth"] * t_block
+    sample = (f"oracle (numpy float64) on one {workload} block at {r1} and {r2} sampled query rows "
+              f"(keys/values over all {rows_all} tokens), split into fixed + per-row cost and extrapolated "
+              f"x{rows_all} rows x{cfg['depth']} blocks x2 CFG passes")
+    return dict(t_step=t_step, sample_s=sum(times[r1]) + sum(times[r2]), sample=sample,
+                cores=os.cpu_count())
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        cpu_oracle_sample(args.workload)
+    ts, total = [], 0.0
+    for _ in range(args.steps):
+        r = cpu_oracle_sample(args.workload)
+        ts.append(r["t_step"])
+        total += r["sample_s"]
+    t_step = statistics.median(ts)
+    v = 1.0 / t_step
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOADS[args.workload]["desc"], "sample": r["sample"]},
+            "cpu_baseline": {"value": v, "unit": "steps/s", "cores": r["cores"], "kind": "oracle",
+                             "sample": r["sample"]},
+            "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU run
+def aggregate(elapsed_s: float, steps: int, world: int, dist=None) -> tuple:
+    """Maximum time over ranks and the whole-job step rate."""
+    t = elapsed_s
+    if dist is not None and world > 1:
+        import torch
+        tt = torch.tensor([t], dtype=torch.float64)
+        if dist.get_backend() == "nccl":
+            tt = tt.cuda()
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    return t, steps * world / t
+
+
+def file_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def run_gpu(args):
+    import torch
+    from diffusion_transformer_denoising_gb300 import dit
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev_idx = torch.cuda.current_device()
+    stream = torch.cuda.current_stream()
+
+    wl = WORKLOADS[args.workload]
+    cfg = synth.config(wl["cfg"])
+    T, H, Wd = cfg["latent"]
+    N = int(np.prod(synth.grid(cfg)))
+    L = cfg["cond_len"]
+    C = cfg["in_channels"]
+    m = dit.DiT(cfg, device=dev_idx)
+    W = synth.make_weights_torch(cfg, seed=0, device=f"cuda:{dev_idx}")
+    m.load_weights(W)
+    del W
+    torch.cuda.empty_cache()
+    g = torch.Generator(device=f"cuda:{dev_idx}")
+    g.manual_seed(1000 + rank)
+    lat0 = torch.randn((1, C, T, H, Wd), generator=g, device="cuda", dtype=torch.float32)
+    cond = torch.randn((1, L, cfg["cond_dim"]), generator=g, device="cuda", dtype=torch.float32)
+    cond = cond.to(torch.bfloat16).float()
+    unc = torch.zeros_like(cond)
+    full = np.array([1.0 - i / cfg["steps"] for i in range(cfg["steps"] + 1)])
+    full = (cfg["shift"] * full / (1 + (cfg["shift"] - 1) * full)).astype(np.float32)
+
+    def schedule(k):
+        # the first k steps of the workload's schedule (a longer linear one if k exceeds it)
+        if k <= cfg["steps"]:
+            return full[:k + 1].copy()
+        return np.linspace(1.0, 1e-3, k + 1).astype(np.float32)
+
+    flags = dit.LOOP_PARTIAL_SCHEDULE
+    # warm-up
+    lat = lat0.clone()
+    sw = schedule(args.warmup)
+    m.dit_denoise_loop(lat, 1, cfg["latent"], cond, unc, L, sw, cfg["guidance"], flags)
+    m.dit_synchronize()
+
+    # timed region: exactly K steps in one loop call, per-kernel events on the stream
+    st = schedule(args.steps)
+    lat = lat0.clone()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    uuid = str(torch.cuda.get_device_properties(dev_idx).uuid)
+    clocks = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    m.dit_profile_start(timing=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    m.dit_denoise_loop(lat, 1, cfg["latent"], cond, unc, L, st, cfg["guidance"], flags)
+    e1.record(stream)
+    prof = m.dit_profile_stop()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    m.dit_synchronize()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    if dist is not None:
+        dist.barrier()
+    t_max, value = aggregate(elapsed, args.steps, world, dist)
+    ok = bool(torch.isfinite(lat).all().item())
+
+    # end to end through the public API with host buffers: every step copies
+    # its inputs host->device and reads the latent back
+    pin_lat = lat0.cpu().pin_memory()
+    pin_cond = cond.cpu().pin_memory()
+    pin_unc = unc.cpu().pin_memory()
+    out_host = torch.empty_like(pin_lat).pin_memory()
+    d_lat, d_cond, d_unc = torch.empty_like(lat0), torch.empty_like(cond), torch.empty_like(unc)
+    k_e2e = max(1, min(args.steps, 3))
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for i in range(k_e2e):
+        d_lat.copy_(pin_lat if i == 0 else out_host, non_blocking=True)
+        d_cond.copy_(pin_cond, non_blocking=True)
+        d_unc.copy_(pin_unc, non_blocking=True)
+        m.dit_denoise_loop(d_lat, 1, cfg["latent"], d_cond, d_unc, L, full[i:i + 2].copy(), cfg["guidance"], flags)
+        out_host.copy_(d_lat, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_t, e2e_value = aggregate(f0.elapsed_time(f1) / 1e3, k_e2e, world, dist)
+    h2d = (pin_lat.numel() + pin_cond.numel() + pin_unc.numel()) * 4
+    d2h = out_host.numel() * 4
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    fl = step_flops(cfg, 2, N, L)
+    peaks = measured_peaks()
+    ms_step = t_max / args.steps * 1e3
+    tflops = fl["total"] / (t_max / args.steps) / 1e12
+    n_self, ms_self = prof["attn_self"]
+    attn_ms = ms_self / max(n_self, 1)
+    attn_achieved = fl["attn_self_per_launch"] / (attn_ms / 1e3) / 1e12
+    src = os.path.join(ROOT, "diffusion_transformer_denoising_gb300", "csrc", "attn_tc.cu")
+    tr = TRAFFIC.get("attn_tc.cu")
+    traffic = tr[2] if tr and tr[0] == file_sha(src) and tr[1] == args.workload else None
+    gemm_ms = sum(prof[k][1] for k in prof if k.startswith("gemm"))
+    kern_ms = sum(v[1] for v in prof.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / world / PAGES_STEPS_PER_S[args.workload]) if args.workload in PAGES_STEPS_PER_S
+        else None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) latents/condition, N(0,0.02) bf16 weights)",
+        "config": {"workload": wl["desc"], "tokens": N, "cond_tokens": L, "cfg_batch": 2,
+                   "schedule": f"first {args.steps} of {cfg['steps']} flow steps, shift {cfg['shift']}",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (activations >= 400 MB per step)"},
+        "attn_gemm_tflops": tflops,
+        "pct_bf16_peak": 100 * tflops / peaks["bf16"],
+        "pct_bf16_peak_sustained": 100 * tflops / peaks["bf16_sustained"],
+        "roofline": {"kernel": "attn_tc_kernel (self-attention)", "bound": "tensor",
+                     "achieved": attn_achieved, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                     "frac": attn_achieved / peaks["bf16_sustained"], "traffic": traffic,
+                     "peak_kind": f"bf16 sustained ({peaks['source']}), kernel timed inside a long step",
+                     "per_launch_flops": fl["attn_self_per_launch"], "avg_launch_ms": attn_ms},
+        "kernel_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
+        "kernel_share": {k: v[1] / kern_ms for k, v in prof.items()} if kern_ms > 0 else None,
+        "gemm_tflops": fl["gemm"] / (gemm_ms / args.steps / 1e3) / 1e12 if gemm_ms > 0 else None,
+        "gpu_launches": int(sum(v[0] for v in prof.values())),
+        "clocks": clk,
+        "finite": ok,
+        "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": k_e2e, "note": "one dit_denoise_loop call per step from pinned host buffers; "
+                                        "includes the per-call condition key/value projection"},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        r = cpu_oracle_sample(args.workload)
+        line["cpu_baseline"] = {"value": 1.0 / r["t_step"], "unit": "steps/s", "cores": r["cores"],
+                                "kind": "oracle", "sample": r["sample"], "sample_seconds": r["sample_s"]}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_block_case(args):
+    """One DiT block of the workload (depth-1 model, CFG batch 2, full token
+    count, batch --batch) run warmup + steps times: the small case for kernel
+    profiling."""
+    import torch
+    from diffusion_transformer_denoising_gb300 import dit
+    from oracle import dit_oracle as O  # noqa: F401
+    torch.cuda.set_device(0)
+    cfg = synth.config(WORKLOADS[args.workload]["cfg"], depth=1)
+    grid = synth.grid(cfg)
+    N, L, D = int(np.prod(grid)), cfg["cond_len"], cfg["hidden"]
+    m = dit.DiT(cfg)
+    W = synth.make_weights_torch(cfg, seed=0, device="cuda")
+    m.load_weights(W)
+    del W
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    B = args.batch
+    x0 = torch.randn((B, N, D), generator=g, device="cuda") * 0.5
+    cond = torch.randn((B, L, cfg["cond_dim"]), generator=g, device="cuda").to(torch.bfloat16).float()
+    mod = torch.randn((B, 6 * D), generator=g, device="cuda") * 0.1
+    joint = cfg["cond_mode"] == synth.COND_JOINT
+    x = x0.clone()
+    xc = cond.clone() if joint else None
+    for _ in range(args.warmup):
+        m.dit_block_forward(0, x, xc, mod, None if joint else cond, B, grid, L)
+    m.dit_synchronize()
+    m.dit_profile_start(timing=True)
+    for _ in range(args.steps):
+        m.dit_block_forward(0, x, xc, mod, None if joint else cond, B, grid, L)
+    prof = m.dit_profile_stop()
+    m.dit_synchronize()
+    fl = step_flops(cfg, B, N, L)
+    n, ms = prof["attn_self"]
+    out = {"case": f"one {args.workload} block, batch {B}", "per_kernel_ms": {k: v[1] / args.steps for k, v in prof.items()},
+           "attn_self_tflops": fl["attn_self_per_launch"] / (ms / max(n, 1) / 1e3) / 1e12,
+           "block_tflops": fl["total"] / (sum(v[1] for v in prof.values()) / args.steps / 1e3) / 1e12}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="video", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=2, help="batch of the block case")
+    ap.add_argument("--case", default="step", choices=["step", "block"],
+                    help="block: one DiT block repeatedly (small case for kernel profiling)")
+    args = ap.parse_args()
+    if args.case == "block":
+        run_block_case(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,16 +1,31 @@
 // Bidirectional multi-head attention (no mask), head_dim 128, bf16 in/out,
 // fp32 softmax and accumulation, on the 5th-generation tensor cores.
 //
-// One CTA = 128 query rows of one (batch, head).  Warps 0-3 run the online
-// softmax (thread = query row = TMEM lane), warp 4 streams K/V tiles of 128
-// keys with TMA through a 3-stage ring, warp 5 issues the MMAs:
-//     S_j = Q K_j^T          (SS: both operands in shared memory, K-major)
-//     O  += P_j V_j          (TS: P from tensor memory, V N-major in smem)
-// Tensor memory (512 columns): S double buffer [0,128) [128,256), O [256,384),
-// P double buffer [384,448) [448,512) as packed bf16 pairs.  S_{j+1} is
-// computed while the softmax works on S_j.  The running max is updated
-// lazily: O is rescaled only when a row's max grows by more than 2^8, so most
-// steps never touch O from the CUDA cores.
+// One CTA = 128 query rows of one (batch, head).  Each row's 128 key columns
+// per step are split into two halves, each with its own online-softmax state
+// (running max m_h, sum l_h) and its own output accumulator O_h; the halves
+// are merged once at the end:
+//     O = (2^(m_0-M) O_0 + 2^(m_1-M) O_1) / (2^(m_0-M) l_0 + 2^(m_1-M) l_1).
+// Warps 0-3 run the softmax of key half 0 and warps 4-7 that of half 1 (warp
+// w reads TMEM lane quadrant w%4, i.e. 32 query rows), so no warp ever waits
+// for another inside the loop.  Warp 8 streams K and V tiles of 128 keys
+// with TMA through two 3-stage rings; warp 9 issues the MMAs from one thread:
+//     S_j = Q K_j^T                 (SS, K-major operands in shared memory)
+//     O_h += P_j[:, half h] V_j[half h]   (TS: P from tensor memory, V N-major)
+// Tensor memory (512 columns): S double buffer [0,128) [128,256); O_0 at
+// [256,384); O_1 at [384,512).  P_j (packed bf16 pairs) overwrites the first
+// 64 columns of its S slot once the softmax has read them.  tcgen05.mma
+// operations of a CTA execute in issue order, so PV_j has read P_j before
+// S_{j+2} overwrites the slot.
+// Every tcgen05.commit costs the tensor pipe a few hundred cycles, so there
+// is exactly one per key tile: after "PV_j, S_{j+2}" the MMA thread commits
+// to done[(j+2) % 3].  Completion i of that ring (i = 0, 1 for S_0, S_1;
+// i = j+2 for PV_j together with S_{j+2}) tells the softmax that S_i is in
+// TMEM, the producer that K_{i} and V_{i-2} stages are free, and a lazy O
+// rescale that PV_{i-2} has landed.  Each waiter takes the completions of a
+// barrier in order, and completion i+3 cannot happen before K_{i+3} is
+// loaded, so a parity wait never aliases.  O is rescaled lazily (only when a
+// max grows by more than 2^8).
 //
 // All waits are bounded (common.cuh); on a timeout the CTA flags *err, waits
 // for its own copies and MMAs, frees TMEM and exits.
@@ -20,157 +35,180 @@
 namespace dit {
 
 namespace fa {
-constexpr int BQ = 128, BKV = 128, HD = 128, STAGES = 3;
-constexpr int TILE_BYTES = BKV * HD * 2;   // 32 KB: two 16 KB swizzle blocks of 64 channels
+constexpr int BQ = 128, BKV = 128, HD = 128, KST = 3, VST = 3;
+constexpr int TILE_BYTES = 128 * HD * 2;   // 32 KB: two 16 KB swizzle blocks of 64 channels
 constexpr int Q_OFF = 0;
-constexpr int KV_OFF = TILE_BYTES;
-constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K then V
-constexpr int BAR_OFF = KV_OFF + STAGES * STAGE_BYTES;
-constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
-constexpr uint32_t TM_S = 0, TM_O = 256, TM_P = 384;
+constexpr int K_OFF = Q_OFF + TILE_BYTES;
+constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
+constexpr int BAR_OFF = V_OFF + VST * TILE_BYTES;
+constexpr int XCH_OFF = BAR_OFF + 256;     // float[4][128]: m_0, m_1, l_0, l_1 per row
+// The tiles need 1024-byte alignment.  The dynamic shared window of a kernel
+// without static shared memory starts 1024-aligned (checked at entry), so no
+// alignment slack is reserved and the total stays under 227 KB.
+constexpr int SMEM_BYTES = XCH_OFF + 4 * BQ * 4;
+constexpr int NUM_THREADS = 320;           // 8 softmax warps, TMA warp, MMA warp
+constexpr int TMA_WARP = 8, MMA_WARP = 9;
+constexpr uint32_t TM_S = 0, TM_O = 256;
 constexpr uint32_t IDESC_S = umma_idesc_bf16(128, 128, false);
 constexpr uint32_t IDESC_O = umma_idesc_bf16(128, 128, true);
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 }  // namespace fa
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, AttnArgs a, float scale_log2, int* err) {
   using namespace fa;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023) {  // uniform across the CTA: nothing has started yet
+    if (threadIdx.x == 0) atomicCAS(err, 0, 20);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;        // [3]
-  uint64_t* v_full = bars + 4;        // [3]
-  uint64_t* kv_empty = bars + 7;      // [3]
-  uint64_t* s_full = bars + 10;       // [2]
-  uint64_t* p_ready = bars + 12;      // [2]
-  uint64_t* o_done = bars + 14;
-  uint64_t* drain = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* k_full = bars + 1;    // [3]
+  uint64_t* v_full = bars + 4;    // [3]
+  uint64_t* done = bars + 7;      // [3] MMA completion ring (see above)
+  uint64_t* p_ready = bars + 10;  // [2] per S slot
+  uint64_t* drain = bars + 12;
+  uint64_t* fin = bars + 13;      // [4] per lane quadrant
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* xch = reinterpret_cast<float*>(smem + XCH_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.z * a.H + blockIdx.y;
   const int q0 = blockIdx.x * BQ;
   const int nkv = (a.Lk + BKV - 1) / BKV;
+  // Each CTA walks the key tiles in a rotated order (the result does not
+  // depend on the order), so CTAs running together read different K/V tiles.
+  const int kv_rot = (int)(blockIdx.x % (unsigned)nkv);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&done[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_ready[b], 4);
-    }
-    mbar_init(o_done, 1);
+    for (int b = 0; b < 2; ++b) mbar_init(&p_ready[b], 8);
     mbar_init(drain, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&fin[i], 2);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == TMA_WARP && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (warp == 5) tmem_alloc(tmem_slot, 512);
+  if (warp == MMA_WARP) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == TMA_WARP) {
     // ------------------------------------------------ TMA producer
-    int issued[STAGES] = {0, 0, 0};
-    bool q_issued = false, ok = true;
+    int k_issued[KST] = {0, 0, 0}, v_issued[VST] = {0, 0, 0};
+    bool ok = true;
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, TILE_BYTES);
       tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, q0, bh);
       tma_load_3d(smem + Q_OFF + TILE_BYTES / 2, &tmQ, q_full, 64, q0, bh);
-      q_issued = true;
     }
     for (int j = 0; j < nkv; ++j) {
-      const int st = j % STAGES;
-      const uint32_t ph = (uint32_t)((j / STAGES) & 1);
-      if (lane == 0) ok = mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, err, 21);
+      const int jt = (j + kv_rot) % nkv;
+      const int ks = j % KST, vs = j % VST;
+      // K_j's stage held K_{j-3}: free once S_{j-3} completed (completion j-3)
+      if (j >= KST && lane == 0) ok = mbar_wait(&done[(j - 3) % 3], (uint32_t)(((j - 3) / 3) & 1), abort_flag, err, 21);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       if (lane == 0) {
-        uint8_t* kb = smem + KV_OFF + st * STAGE_BYTES;
-        mbar_arrive_expect_tx(&k_full[st], TILE_BYTES);
-        tma_load_3d(kb, &tmK, &k_full[st], 0, j * BKV, bh);
-        tma_load_3d(kb + TILE_BYTES / 2, &tmK, &k_full[st], 64, j * BKV, bh);
-        mbar_arrive_expect_tx(&v_full[st], TILE_BYTES);
-        tma_load_3d(kb + TILE_BYTES, &tmV, &v_full[st], 0, j * BKV, bh);
-        tma_load_3d(kb + TILE_BYTES + TILE_BYTES / 2, &tmV, &v_full[st], 64, j * BKV, bh);
+        uint8_t* kb = smem + K_OFF + ks * TILE_BYTES;
+        mbar_arrive_expect_tx(&k_full[ks], TILE_BYTES);
+        tma_load_3d(kb, &tmK, &k_full[ks], 0, jt * BKV, bh);
+        tma_load_3d(kb + TILE_BYTES / 2, &tmK, &k_full[ks], 64, jt * BKV, bh);
       }
-      ++issued[st];
+      ++k_issued[ks];
+      // V_j's stage held V_{j-3}: free once PV_{j-3} completed (completion j-1)
+      if (j >= VST && lane == 0) ok = mbar_wait(&done[(j - 1) % 3], (uint32_t)(((j - 1) / 3) & 1), abort_flag, err, 22);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (lane == 0) {
+        uint8_t* vb = smem + V_OFF + vs * TILE_BYTES;
+        mbar_arrive_expect_tx(&v_full[vs], TILE_BYTES);
+        tma_load_3d(vb, &tmV, &v_full[vs], 0, jt * BKV, bh);
+        tma_load_3d(vb + TILE_BYTES / 2, &tmV, &v_full[vs], 64, jt * BKV, bh);
+      }
+      ++v_issued[vs];
     }
     if (!ok && lane == 0) {
+      // wind down: every copy this thread started lands before the CTA exits
       volatile int no_abort = 0;
-      if (q_issued) mbar_wait(q_full, 0, &no_abort, nullptr, 0);
-      for (int s = 0; s < STAGES; ++s)
-        if (issued[s] > 0) {
-          mbar_wait(&k_full[s], (uint32_t)((issued[s] - 1) & 1), &no_abort, nullptr, 0);
-          mbar_wait(&v_full[s], (uint32_t)((issued[s] - 1) & 1), &no_abort, nullptr, 0);
-        }
+      mbar_wait(q_full, 0, &no_abort, nullptr, 0);
+      for (int s = 0; s < KST; ++s)
+        if (k_issued[s] > 0) mbar_wait(&k_full[s], (uint32_t)((k_issued[s] - 1) & 1), &no_abort, nullptr, 0);
+      for (int s = 0; s < VST; ++s)
+        if (v_issued[s] > 0) mbar_wait(&v_full[s], (uint32_t)((v_issued[s] - 1) & 1), &no_abort, nullptr, 0);
     }
-  } else if (warp == 5) {
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------ MMA issuer
-    const uint32_t qa = smem_u32(smem + Q_OFF);
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait(q_full, 0, abort_flag, err, 22);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    auto issue_s = [&](int j) -> bool {
-      const int st = j % STAGES;
+    auto wait1 = [&](uint64_t* bar, uint32_t parity, int site) -> bool {
       bool r = true;
-      if (lane == 0) r = mbar_wait(&k_full[st], (uint32_t)((j / STAGES) & 1), abort_flag, err, 23);
-      r = __shfl_sync(0xffffffffu, r, 0);
-      if (!r) return false;
+      if (lane == 0) r = mbar_wait(bar, parity, abort_flag, err, site);
+      return __shfl_sync(0xffffffffu, r, 0);
+    };
+    // base descriptors, built once; per MMA only a constant is added
+    const uint64_t q_desc = umma_desc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
+    const uint64_t k_desc = umma_desc_sw128(smem_u32(smem + K_OFF), 16, 1024);
+    const uint64_t v_desc = umma_desc_sw128(smem_u32(smem + V_OFF), 16384, 1024);
+    // S_j = Q K_j^T into S slot j % 2 (no commit here)
+    auto issue_s = [&](int j) -> bool {
+      const int ks = j % KST;
+      if (!wait1(&k_full[ks], (uint32_t)((j / KST) & 1), 23)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t ka = smem_u32(smem + KV_OFF + st * STAGE_BYTES);
+        const uint64_t kd = umma_desc_add(k_desc, ks * TILE_BYTES);
+        const uint32_t d_tmem = tmem + TM_S + (j & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (TILE_BYTES / 2) + (kk & 3) * 32;
-          umma_ss(tmem + TM_S + (j & 1) * 128, umma_desc_sw128(qa + off, 16, 1024),
-                  umma_desc_sw128(ka + off, 16, 1024), IDESC_S, kk != 0);
+          umma_ss(d_tmem, umma_desc_add(q_desc, off), umma_desc_add(kd, off), IDESC_S, kk != 0);
         }
-        umma_commit(&s_full[j & 1]);
       }
       __syncwarp();
       return true;
     };
+    bool ok = wait1(q_full, 0, 24);
     if (ok) ok = issue_s(0);
+    if (ok && lane == 0) umma_commit(&done[0]);  // completion 0: S_0
+    if (ok && nkv > 1) {
+      ok = issue_s(1);
+      if (ok && lane == 0) umma_commit(&done[1]);  // completion 1: S_1
+    }
+    __syncwarp();
     for (int j = 0; ok && j < nkv; ++j) {
-      if (j + 1 < nkv) {
-        ok = issue_s(j + 1);
-        if (!ok) break;
-      }
-      const int st = j % STAGES;
-      if (lane == 0) {
-        ok = mbar_wait(&p_ready[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, err, 24) &&
-             mbar_wait(&v_full[st], (uint32_t)((j / STAGES) & 1), abort_flag, err, 25);
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      const int vs = j % VST;
+      ok = wait1(&p_ready[j & 1], (uint32_t)((j >> 1) & 1), 25) &&
+           wait1(&v_full[vs], (uint32_t)((j / VST) & 1), 26);
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t va = smem_u32(smem + KV_OFF + st * STAGE_BYTES + TILE_BYTES);
+        const uint64_t vd = umma_desc_add(v_desc, vs * TILE_BYTES);
+        const uint32_t p_tmem = tmem + TM_S + (j & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk) {
-          // V tile [128 keys][128 ch]: keys are the K dimension (8-row groups
-          // 1 KB apart), channels the N dimension (64-wide halves 16 KB apart).
-          umma_ts(tmem + TM_O, tmem + TM_P + (j & 1) * 64 + kk * 8, umma_desc_sw128(va + kk * 2048, 16384, 1024),
-                  IDESC_O, (j | kk) != 0);
-        }
-        umma_commit(&kv_empty[st]);
-        umma_commit(o_done);
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // keys 64h+16kk.. of V (8-row groups 1 KB apart; channel halves 16 KB apart)
+            umma_ts(tmem + TM_O + h * 128, p_tmem + h * 32 + kk * 8, umma_desc_add(vd, (4 * h + kk) * 2048),
+                    IDESC_O, (j | kk) != 0);
+          }
       }
+      __syncwarp();
+      if (j + 2 < nkv) ok = issue_s(j + 2);
+      if (lane == 0) umma_commit(&done[(j + 2) % 3]);  // completion j+2: PV_j (+ S_{j+2})
       __syncwarp();
     }
     if (lane == 0) {
@@ -180,113 +218,135 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------ softmax warps 0-3
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // ------------------------------------------------ softmax warps 0-7
+    const int q = warp & 3, h = warp >> 2;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const uint32_t o_col = tmem + TM_O + h * 128 + lane_off;
+    const int row = q * 32 + lane;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      if (lane == 0) ok = mbar_wait(&s_full[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, err, 26);
+      if (lane == 0) ok = mbar_wait(&done[j % 3], (uint32_t)((j / 3) & 1), abort_flag, err, 31);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      float s[BKV];
-#pragma unroll
-      for (int c = 0; c < BKV / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + TM_S + (j & 1) * 128 + c * 32 + lane_off, r);
+      const uint32_t s_col = tmem + TM_S + (j & 1) * 128 + lane_off;
+      float s[64];
+      {
+        uint32_t r[64];
+        tmem_ld32(s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
       }
-      const int valid = a.Lk - j * BKV;
-      if (valid < BKV) {
+      const int valid = a.Lk - ((j + kv_rot) % nkv) * BKV - h * 64;
+      if (valid < 64) {
 #pragma unroll
-        for (int i = 0; i < BKV; ++i)
+        for (int i = 0; i < 64; ++i)
           if (i >= valid) s[i] = -INFINITY;
       }
-      float mx = s[0];
+      // row max: four independent chains of three-input max over s[4..59], then s[60..63]
+      float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int i = 1; i < BKV; ++i) mx = fmaxf(mx, s[i]);
+      for (int i = 4; i + 8 <= 60; i += 8)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], s[i + 2 * k], s[i + 2 * k + 1]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m4[k] = fmaxf(m4[k], s[60 + k]);
+      const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
       const float m_new = fmaxf(m_used, mx * scale_log2);
-      bool need;
-      float alpha;
+      float alpha = 1.f;
       if (j == 0) {
-        need = false;
-        alpha = 0.f;
         m_used = m_new;
       } else {
-        need = m_new - m_used > RESCALE_THRESHOLD;
-        alpha = need ? ex2_approx(m_used - m_new) : 1.f;
-        if (need) m_used = m_new;
-      }
-      float rs = 0.f;
-      uint32_t pk[BKV / 2];
-#pragma unroll
-      for (int i = 0; i < BKV; i += 2) {
-        const float p0 = ex2_approx(fmaf(s[i], scale_log2, -m_used));
-        const float p1 = ex2_approx(fmaf(s[i + 1], scale_log2, -m_used));
-        rs += p0 + p1;
-        pk[i / 2] = pack_bf16x2(p0, p1);
-      }
-      l = l * alpha + rs;
-      {
-        uint32_t r[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = pk[i];
-        tmem_st32(tmem + TM_P + (j & 1) * 64 + lane_off, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = pk[32 + i];
-        tmem_st32(tmem + TM_P + (j & 1) * 64 + 32 + lane_off, r);
-      }
-      tmem_st_wait();
-      if (j > 0) {
-        // P_j may only be consumed after O holds P_{j-1} V_{j-1}; rescale then
-        if (lane == 0) ok = mbar_wait(o_done, (uint32_t)((j - 1) & 1), abort_flag, err, 27);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        tc_fence_after();
+        const bool need = m_new - m_used > RESCALE_THRESHOLD;
         if (__any_sync(0xffffffffu, need)) {
+          // O_h must hold PV_{j-1} (completion j+1) before it is rescaled
+          if (lane == 0) ok = mbar_wait(&done[(j + 1) % 3], (uint32_t)(((j + 1) / 3) & 1), abort_flag, err, 32);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          tc_fence_after();
+          if (need) {
+            alpha = ex2_approx(m_used - m_new);
+            m_used = m_new;
+          }
 #pragma unroll 1
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t r[32];
-            tmem_ld32(tmem + TM_O + c * 32 + lane_off, r);
+            tmem_ld32(o_col + c * 32, r);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(tmem + TM_O + c * 32 + lane_off, r);
+            tmem_st32(o_col + c * 32, r);
           }
-          tmem_st_wait();
         }
       }
+      // a half that has seen no valid key yet keeps m = -inf and p = 0
+      const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+      const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-mref, -mref);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        const float2 x = ffma2(make_float2(s[i], s[i + 1]), sc2, nm2);
+        const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        acc[(i >> 1) & 3] = fadd2(acc[(i >> 1) & 3], p);
+        pk[i / 2] = pack_bf16x2(p.x, p.y);
+      }
+      const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+      l = l * alpha + ((a01.x + a01.y) + (a23.x + a23.y));
+      tmem_st32(s_col + h * 32, pk);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_ready[j & 1]);
     }
     if (ok) {
-      if (lane == 0) ok = mbar_wait(o_done, (uint32_t)((nkv - 1) & 1), abort_flag, err, 28);
+      // PV_{nkv-1} is completion nkv+1
+      if (lane == 0) ok = mbar_wait(&done[(nkv + 1) % 3], (uint32_t)(((nkv + 1) / 3) & 1), abort_flag, err, 33);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    if (ok) {
+      // merge the two halves: swap (m, l) with the partner warp of the quadrant
+      xch[h * BQ + row] = m_used;
+      xch[(2 + h) * BQ + row] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&fin[q]);
+      if (lane == 0) ok = mbar_wait(&fin[q], 0, abort_flag, err, 34);
       ok = __shfl_sync(0xffffffffu, ok, 0);
     }
     if (ok) {
       tc_fence_after();
-      const int t = q0 + warp * 32 + lane;
+      const float m_o = xch[(1 - h) * BQ + row], l_o = xch[(3 - h) * BQ + row];
+      const float M = fmaxf(m_used, m_o);
+      const float a_s = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - M);
+      const float a_o = (m_o == -INFINITY) ? 0.f : ex2_approx(m_o - M);
+      const float inv = 1.f / (l * a_s + l_o * a_o);
+      const int tok = q0 + row;
       const int D = a.H * HD;
       __nv_bfloat16* out = nullptr;
-      if (t < a.Lq) {
-        out = (t < a.split)
-                  ? static_cast<__nv_bfloat16*>(a.o1) + ((int64_t)blockIdx.z * a.split + t) * D
-                  : static_cast<__nv_bfloat16*>(a.o2) + ((int64_t)blockIdx.z * (a.Lq - a.split) + (t - a.split)) * D;
-        out += blockIdx.y * HD;
+      if (tok < a.Lq) {
+        out = (tok < a.split)
+                  ? static_cast<__nv_bfloat16*>(a.o1) + ((int64_t)blockIdx.z * a.split + tok) * D
+                  : static_cast<__nv_bfloat16*>(a.o2) +
+                        ((int64_t)blockIdx.z * (a.Lq - a.split) + (tok - a.split)) * D;
+        out += blockIdx.y * HD + h * 64;
       }
-      const float inv = 1.f / l;
+      // this warp writes channels [64h, 64h+64) from both accumulators
+      const uint32_t self_col = tmem + TM_O + h * 128 + h * 64 + lane_off;
+      const uint32_t oth_col = tmem + TM_O + (1 - h) * 128 + h * 64 + lane_off;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + TM_O + c * 32 + lane_off, r);
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r1[32], r2[32];
+        tmem_ld32(self_col + c * 32, r1);
+        tmem_ld32(oth_col + c * 32, r2);
         tmem_ld_wait();
         if (out) {
           float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * inv;
+          for (int i = 0; i < 32; ++i)
+            v[i] = (__uint_as_float(r1[i]) * a_s + __uint_as_float(r2[i]) * a_o) * inv;
           store_chunk<__nv_bfloat16, 32>(out + c * 32, v);
         }
       }
@@ -294,7 +354,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -321,8 +381,10 @@ cudaError_t attention_bf16_tc(const AttnArgs& a, int* err, cudaStream_t s) {
   }
   dim3 grid((a.Lq + BQ - 1) / BQ, a.H, a.B);
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
-  attn_tc_kernel<<<grid, 192, SMEM_BYTES, s>>>(tq, tk, tv, a, scale_log2, err);
+  attn_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tq, tk, tv, a, scale_log2, err);
   return cudaGetLastError();
 }
 
 }  // namespace dit
+
+static_assert(dit::fa::SMEM_BYTES <= 232448, "attention tile set exceeds 227 KB of shared memory");

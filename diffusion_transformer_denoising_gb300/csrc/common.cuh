@@ -15,15 +15,43 @@ DIT_DEV uint32_t pack_bf16x2(float lo, float hi) {
 DIT_DEV float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 DIT_DEV float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
+// Pure functions: no volatile, so the compiler may schedule them freely.
 DIT_DEV float ex2_approx(float x) {
   float y;
-  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 DIT_DEV float tanh_approx(float x) {
   float y;
-  asm volatile("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Packed fp32 pairs (sm_100+ f32x2 instructions) and three-input max.
+DIT_DEV uint64_t f2_bits(float2 v) {
+  uint64_t u;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(u) : "f"(v.x), "f"(v.y));
+  return u;
+}
+DIT_DEV float2 f2_from(uint64_t u) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(u));
+  return v;
+}
+DIT_DEV float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return f2_from(d);
+}
+DIT_DEV float2 fadd2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return f2_from(d);
+}
+DIT_DEV float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // ---------------------------------------------------------------- smem / mbarrier
@@ -120,6 +148,13 @@ DIT_DEV uint64_t umma_desc_sw128(uint32_t smem_addr, uint32_t lbo_bytes, uint32_
   d |= (uint64_t)2 << 61;
   return d;
 }
+
+// Advance a descriptor's start address by `bytes` (a multiple of 16).  The
+// start field holds address >> 4 in its low 14 bits; shared addresses stay
+// below 256 KB, so the add never carries out of the field.  Building a base
+// descriptor once and advancing it keeps the single MMA-issuing thread from
+// spending tens of cycles per instruction on descriptor arithmetic.
+DIT_DEV uint64_t umma_desc_add(uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
 // b_mn_major: B stored N-contiguous (transpose bit).

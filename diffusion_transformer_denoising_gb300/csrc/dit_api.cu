@@ -175,6 +175,16 @@ struct dit_model {
   float2* rope = nullptr;
   int rope_grid[3] = {0, 0, 0};
   size_t rope_bytes = 0;
+  // launch accounting (dit_profile_start / dit_profile_stop)
+  bool prof_timing = false;
+  int64_t prof_counts[DIT_KERNEL_KINDS] = {};
+  struct Rec {
+    int kind;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> prof_rec;
+  std::vector<cudaEvent_t> prof_pool;
+  size_t prof_next = 0;
 
   const void* W(const std::string& n) const { return arena + params[index.at(n)].offset; }
   const float* V(const std::string& n) const {
@@ -231,6 +241,7 @@ extern "C" void dit_destroy(dit_model* m) {
   cudaFree(m->d_t);
   cudaFree(m->ws);
   cudaFree(m->rope);
+  for (auto e : m->prof_pool) cudaEventDestroy(e);
   cudaSetDevice(prev);
   delete m;
 }
@@ -388,6 +399,42 @@ static dit_status require_loaded(const dit_model* m) {
   return DIT_OK;
 }
 
+// Counts the kernels a launcher enqueues and, while timing is on, brackets
+// them with an event pair on the launching stream.
+struct Launch {
+  dit_model* m;
+  int kind, n;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  static cudaEvent_t event(dit_model* m) {
+    if (m->prof_next == m->prof_pool.size()) {
+      cudaEvent_t e = nullptr;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      m->prof_pool.push_back(e);
+    }
+    return m->prof_pool[m->prof_next++];
+  }
+  Launch(dit_model* m_, int kind_, int n_, cudaStream_t s_) : m(m_), kind(kind_), n(n_), s(s_) {
+    if (m->prof_timing && (a = event(m))) cudaEventRecord(a, s);
+  }
+  ~Launch() {
+    m->prof_counts[kind] += n;
+    if (a) {
+      cudaEvent_t b = event(m);
+      if (b) {
+        cudaEventRecord(b, s);
+        m->prof_rec.push_back({kind, a, b});
+      }
+    }
+  }
+};
+#define LAUNCH(kind, n, expr)             \
+  do {                                    \
+    Launch l_(m, kind, n, s);             \
+    cudaError_t e_ = (expr);              \
+    if (e_ != cudaSuccess) return fail(DIT_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
 static dit_status ensure_ws(dit_model* m, size_t bytes) {
   if (bytes <= m->ws_bytes) return DIT_OK;
   if (m->ws) {
@@ -435,7 +482,7 @@ static dit_status ensure_rope(dit_model* m, const int32_t g[3]) {
   return DIT_OK;
 }
 
-static dit_status do_gemm(dit_model* m, const void* A, int64_t M, int K, int64_t lda, const void* W, int N,
+static dit_status do_gemm(dit_model* m, int kind, const void* A, int64_t M, int K, int64_t lda, const void* W, int N,
                           const EpiParams& ep, cudaStream_t s) {
   GemmArgs g;
   g.A = A;
@@ -447,13 +494,14 @@ static dit_status do_gemm(dit_model* m, const void* A, int64_t M, int K, int64_t
   g.epi = ep;
   g.epi.M = (int)M;
   g.epi.N = N;
+  Launch l_(m, kind, 1, s);
   cudaError_t e = m->bf16 ? gemm_bf16_tc(g, m->d_err, m->num_sms, s) : gemm_f32(g, s);
   if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "GEMM launch (M=%lld N=%d K=%d) failed: %s", (long long)M, N, K,
                                     cudaGetErrorString(e));
   return DIT_OK;
 }
 
-static dit_status do_attn(dit_model* m, const void* q, const void* k, const void* v, int B, int Lq, int Lk,
+static dit_status do_attn(dit_model* m, int kind, const void* q, const void* k, const void* v, int B, int Lq, int Lk,
                           void* o1, void* o2, int split, cudaStream_t s) {
   AttnArgs a;
   a.q = q;
@@ -467,6 +515,7 @@ static dit_status do_attn(dit_model* m, const void* q, const void* k, const void
   a.o1 = o1;
   a.o2 = o2;
   a.split = split;
+  Launch l_(m, kind, 1, s);
   cudaError_t e = m->bf16 ? attention_bf16_tc(a, m->d_err, s) : attention_f32(a, s);
   if (e != cudaSuccess)
     return fail(DIT_ERR_CUDA, "attention launch (Lq=%d Lk=%d) failed: %s", Lq, Lk, cudaGetErrorString(e));
@@ -573,7 +622,7 @@ static dit_status cross_kv(dit_model* m, int blk, const void* cond_act, int B, i
                            cudaStream_t s) {
   const dit_config& c = m->cfg;
   EpiParams ep = epi_heads(m, m->V(m->blk(blk, "cross.kv.bias")), kc, vc, nullptr, L, L, 0, 0);
-  return do_gemm(m, cond_act, (int64_t)B * L, c.cond_dim, c.cond_dim, m->W(m->blk(blk, "cross.kv.weight")),
+  return do_gemm(m, DIT_KERNEL_GEMM_CROSS_KV, cond_act, (int64_t)B * L, c.cond_dim, c.cond_dim, m->W(m->blk(blk, "cross.kv.weight")),
                  2 * c.hidden, ep, s);
 }
 
@@ -589,51 +638,51 @@ static dit_status run_block(dit_model* m, int blk, float* x, float* xc, const fl
   if (c.cond_mode == DIT_COND_CROSS) {
     const int64_t R = (int64_t)B * N;
     // self-attention half
-    K_TRY(ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, bf, s));
-    DIT_TRY(do_gemm(m, bb.h, R, D, D, m->W(m->blk(blk, "attn.qkv.weight")), 3 * D,
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, bf, s));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_QKV, bb.h, R, D, D, m->W(m->blk(blk, "attn.qkv.weight")), 3 * D,
                     epi_heads(m, m->V(m->blk(blk, "attn.qkv.bias")), bb.q, bb.k, bb.v, N, N, 0, 0x3), s));
-    DIT_TRY(do_attn(m, bb.q, bb.k, bb.v, B, N, N, bb.a, nullptr, N, s));
-    DIT_TRY(do_gemm(m, bb.a, R, D, D, m->W(m->blk(blk, "attn.out.weight")), D,
+    DIT_TRY(do_attn(m, DIT_KERNEL_ATTN_SELF, bb.q, bb.k, bb.v, B, N, N, bb.a, nullptr, N, s));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, m->W(m->blk(blk, "attn.out.weight")), D,
                     epi_resid(m->V(m->blk(blk, "attn.out.bias")), x, mod + 2 * D, mod_bstride, N), s));
     // cross-attention half: plain LN, no rotation, ungated residual
-    K_TRY(ln_modulate(x, R, D, N, nullptr, nullptr, 0, eps, bb.h, bf, s));
-    DIT_TRY(do_gemm(m, bb.h, R, D, D, m->W(m->blk(blk, "cross.q.weight")), D,
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, nullptr, nullptr, 0, eps, bb.h, bf, s));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_CROSS_Q, bb.h, R, D, D, m->W(m->blk(blk, "cross.q.weight")), D,
                     epi_heads(m, m->V(m->blk(blk, "cross.q.bias")), bb.q, nullptr, nullptr, N, N, 0, 0), s));
-    DIT_TRY(do_attn(m, bb.q, kc, vc, B, N, L, bb.a, nullptr, N, s));
-    DIT_TRY(do_gemm(m, bb.a, R, D, D, m->W(m->blk(blk, "cross.out.weight")), D,
+    DIT_TRY(do_attn(m, DIT_KERNEL_ATTN_CROSS, bb.q, kc, vc, B, N, L, bb.a, nullptr, N, s));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, m->W(m->blk(blk, "cross.out.weight")), D,
                     epi_resid(m->V(m->blk(blk, "cross.out.bias")), x, nullptr, 0, N), s));
     // MLP half
-    K_TRY(ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, s));
-    DIT_TRY(do_gemm(m, bb.h, R, D, D, m->W(m->blk(blk, "mlp.fc1.weight")), F,
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, s));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN1, bb.h, R, D, D, m->W(m->blk(blk, "mlp.fc1.weight")), F,
                     epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F), s));
-    DIT_TRY(do_gemm(m, bb.g, R, F, F, m->W(m->blk(blk, "mlp.fc2.weight")), D,
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN2, bb.g, R, F, F, m->W(m->blk(blk, "mlp.fc2.weight")), D,
                     epi_resid(m->V(m->blk(blk, "mlp.fc2.bias")), x, mod + 5 * D, mod_bstride, N), s));
     return DIT_OK;
   }
   // joint (dual-stream) block: sequence [condition; image]
   const int S = L + N;
   const int64_t R = (int64_t)B * N, Rc = (int64_t)B * L;
-  K_TRY(ln_modulate(xc, Rc, D, L, modc + 0 * D, modc + 1 * D, mod_bstride, eps, bb.h, bf, s));
-  DIT_TRY(do_gemm(m, bb.h, Rc, D, D, m->W(m->blk(blk, "ctx.attn.qkv.weight")), 3 * D,
+  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(xc, Rc, D, L, modc + 0 * D, modc + 1 * D, mod_bstride, eps, bb.h, bf, s));
+  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_QKV, bb.h, Rc, D, D, m->W(m->blk(blk, "ctx.attn.qkv.weight")), 3 * D,
                   epi_heads(m, m->V(m->blk(blk, "ctx.attn.qkv.bias")), bb.q, bb.k, bb.v, L, S, 0, 0), s));
-  K_TRY(ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, bf, s));
-  DIT_TRY(do_gemm(m, bb.h, R, D, D, m->W(m->blk(blk, "attn.qkv.weight")), 3 * D,
+  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, bf, s));
+  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_QKV, bb.h, R, D, D, m->W(m->blk(blk, "attn.qkv.weight")), 3 * D,
                   epi_heads(m, m->V(m->blk(blk, "attn.qkv.bias")), bb.q, bb.k, bb.v, N, S, L, 0x3), s));
-  DIT_TRY(do_attn(m, bb.q, bb.k, bb.v, B, S, S, bb.ac, bb.a, L, s));
-  DIT_TRY(do_gemm(m, bb.a, R, D, D, m->W(m->blk(blk, "attn.out.weight")), D,
+  DIT_TRY(do_attn(m, DIT_KERNEL_ATTN_SELF, bb.q, bb.k, bb.v, B, S, S, bb.ac, bb.a, L, s));
+  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, m->W(m->blk(blk, "attn.out.weight")), D,
                   epi_resid(m->V(m->blk(blk, "attn.out.bias")), x, mod + 2 * D, mod_bstride, N), s));
-  K_TRY(ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, s));
-  DIT_TRY(do_gemm(m, bb.h, R, D, D, m->W(m->blk(blk, "mlp.fc1.weight")), F,
+  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, s));
+  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN1, bb.h, R, D, D, m->W(m->blk(blk, "mlp.fc1.weight")), F,
                   epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F), s));
-  DIT_TRY(do_gemm(m, bb.g, R, F, F, m->W(m->blk(blk, "mlp.fc2.weight")), D,
+  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN2, bb.g, R, F, F, m->W(m->blk(blk, "mlp.fc2.weight")), D,
                   epi_resid(m->V(m->blk(blk, "mlp.fc2.bias")), x, mod + 5 * D, mod_bstride, N), s));
   if (!ctx_out_needed) return DIT_OK;
-  DIT_TRY(do_gemm(m, bb.ac, Rc, D, D, m->W(m->blk(blk, "ctx.attn.out.weight")), D,
+  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.ac, Rc, D, D, m->W(m->blk(blk, "ctx.attn.out.weight")), D,
                   epi_resid(m->V(m->blk(blk, "ctx.attn.out.bias")), xc, modc + 2 * D, mod_bstride, L), s));
-  K_TRY(ln_modulate(xc, Rc, D, L, modc + 3 * D, modc + 4 * D, mod_bstride, eps, bb.h, bf, s));
-  DIT_TRY(do_gemm(m, bb.h, Rc, D, D, m->W(m->blk(blk, "ctx.mlp.fc1.weight")), F,
+  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(xc, Rc, D, L, modc + 3 * D, modc + 4 * D, mod_bstride, eps, bb.h, bf, s));
+  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN1, bb.h, Rc, D, D, m->W(m->blk(blk, "ctx.mlp.fc1.weight")), F,
                   epi_store(EPI_GELU, m->V(m->blk(blk, "ctx.mlp.fc1.bias")), bb.g, F), s));
-  DIT_TRY(do_gemm(m, bb.g, Rc, F, F, m->W(m->blk(blk, "ctx.mlp.fc2.weight")), D,
+  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN2, bb.g, Rc, F, F, m->W(m->blk(blk, "ctx.mlp.fc2.weight")), D,
                   epi_resid(m->V(m->blk(blk, "ctx.mlp.fc2.bias")), xc, modc + 5 * D, mod_bstride, L), s));
   return DIT_OK;
 }
@@ -670,7 +719,7 @@ extern "C" dit_status dit_timestep_modulation(dit_model* m, const float* t_host,
   const size_t need = (size_t)batch * m->cfg.hidden * sizeof(float) + 256;
   DIT_TRY(ensure_ws(m, need));
   CU_TRY(cudaMemcpyAsync(m->d_t, t_host, batch * sizeof(float), cudaMemcpyHostToDevice, s));
-  K_TRY(timestep_mlp(m->d_t, 0.0, batch, m->cfg.freq_dim, m->cfg.hidden, m->W("time_mlp.fc1.weight"),
+  LAUNCH(DIT_KERNEL_SMALL, 2, timestep_mlp(m->d_t, 0.0, batch, m->cfg.freq_dim, m->cfg.hidden, m->W("time_mlp.fc1.weight"),
                      m->V("time_mlp.fc1.bias"), m->W("time_mlp.fc2.weight"), m->V("time_mlp.fc2.bias"), m->bf16,
                      static_cast<float*>(m->ws), mod, s));
   return DIT_OK;
@@ -688,9 +737,9 @@ extern "C" dit_status dit_patch_embed(dit_model* m, const float* lat, int batch,
   const int64_t N = (int64_t)(thw[0] / c.patch[0]) * (thw[1] / c.patch[1]) * (thw[2] / c.patch[2]);
   const int P = c.in_channels * c.patch[0] * c.patch[1] * c.patch[2];
   DIT_TRY(ensure_ws(m, (size_t)batch * N * P * m->act + 256));
-  K_TRY(patchify(lat, batch, 1, c.in_channels, thw[0], thw[1], thw[2], c.patch[0], c.patch[1], c.patch[2], m->ws,
+  LAUNCH(DIT_KERNEL_SMALL, 1, patchify(lat, batch, 1, c.in_channels, thw[0], thw[1], thw[2], c.patch[0], c.patch[1], c.patch[2], m->ws,
                  m->bf16, s));
-  return do_gemm(m, m->ws, (int64_t)batch * N, P, P, m->W("patch_embed.weight"), c.hidden,
+  return do_gemm(m, DIT_KERNEL_GEMM_EMBED, m->ws, (int64_t)batch * N, P, P, m->W("patch_embed.weight"), c.hidden,
                  epi_store(EPI_F32, m->V("patch_embed.bias"), x, c.hidden), s);
 }
 
@@ -720,15 +769,15 @@ extern "C" dit_status dit_block_forward(dit_model* m, int block, float* x, float
   BlockBufs bb = carve_block(m, w, batch, N, L);
   float* modtab = static_cast<float*>(w.take((size_t)batch * 6 * D * sizeof(float)));
   float* modtab_c = static_cast<float*>(w.take((size_t)batch * 6 * D * sizeof(float)));
-  K_TRY(add_tables(mod, batch, D, 6, m->V(m->blk(block, "mod_table")), 1, modtab, s));
+  LAUNCH(DIT_KERNEL_SMALL, 1, add_tables(mod, batch, D, 6, m->V(m->blk(block, "mod_table")), 1, modtab, s));
   if (c.cond_mode == DIT_COND_JOINT)
-    K_TRY(add_tables(mod, batch, D, 6, m->V(m->blk(block, "ctx.mod_table")), 1, modtab_c, s));
+    LAUNCH(DIT_KERNEL_SMALL, 1, add_tables(mod, batch, D, 6, m->V(m->blk(block, "ctx.mod_table")), 1, modtab_c, s));
   const void* kc = nullptr;
   const void* vc = nullptr;
   if (c.cond_mode == DIT_COND_CROSS) {
     const void* ca = cond;
     if (m->bf16) {
-      K_TRY(f32_to_bf16(cond, bb.cond_act, (int64_t)batch * L * c.cond_dim, s));
+      LAUNCH(DIT_KERNEL_SMALL, 1, f32_to_bf16(cond, bb.cond_act, (int64_t)batch * L * c.cond_dim, s));
       ca = bb.cond_act;
     }
     DIT_TRY(cross_kv(m, block, ca, batch, L, bb.kc, bb.vc, s));
@@ -758,10 +807,10 @@ extern "C" dit_status dit_final_layer(dit_model* m, const float* x, const float*
   float* headtab = static_cast<float*>(w.take((size_t)batch * 2 * D * 4));
   void* h = w.take((size_t)batch * N * D * m->act);
   float* vt = static_cast<float*>(w.take((size_t)batch * N * P * 4));
-  K_TRY(add_tables(mod, batch, D, 2, m->V("head.mod_table"), 1, headtab, s));
-  K_TRY(ln_modulate(x, batch * N, D, (int)N, headtab, headtab + D, 2 * D, c.ln_eps, h, m->bf16, s));
-  DIT_TRY(do_gemm(m, h, batch * N, D, D, m->W("head.weight"), P, epi_store(EPI_F32, m->V("head.bias"), vt, P), s));
-  K_TRY(unpatchify(vt, batch, c.in_channels, thw[0], thw[1], thw[2], c.patch[0], c.patch[1], c.patch[2], v, s));
+  LAUNCH(DIT_KERNEL_SMALL, 1, add_tables(mod, batch, D, 2, m->V("head.mod_table"), 1, headtab, s));
+  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, batch * N, D, (int)N, headtab, headtab + D, 2 * D, c.ln_eps, h, m->bf16, s));
+  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_EMBED, h, batch * N, D, D, m->W("head.weight"), P, epi_store(EPI_F32, m->V("head.bias"), vt, P), s));
+  LAUNCH(DIT_KERNEL_SMALL, 1, unpatchify(vt, batch, c.in_channels, thw[0], thw[1], thw[2], c.patch[0], c.patch[1], c.patch[2], v, s));
   return DIT_OK;
 }
 
@@ -852,7 +901,7 @@ extern "C" dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, 
     if (cfg) CU_TRY(cudaMemcpyAsync(cf + (size_t)Bq * L * c.cond_dim, uncond, cond_bytes, cudaMemcpyDeviceToDevice, s));
     const void* ca = cf;
     if (m->bf16) {
-      K_TRY(f32_to_bf16(cf, bb.cond_act, (int64_t)B * L * c.cond_dim, s));
+      LAUNCH(DIT_KERNEL_SMALL, 1, f32_to_bf16(cf, bb.cond_act, (int64_t)B * L * c.cond_dim, s));
       ca = bb.cond_act;
     }
     const size_t per = (size_t)B * L * D * a;
@@ -863,14 +912,14 @@ extern "C" dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, 
   }
   for (int i = 0; i < n_steps; ++i) {
     const double t = (double)c.timestep_scale * (double)sigmas[i];
-    K_TRY(timestep_mlp(nullptr, t, 1, c.freq_dim, D, m->W("time_mlp.fc1.weight"), m->V("time_mlp.fc1.bias"),
+    LAUNCH(DIT_KERNEL_SMALL, 2, timestep_mlp(nullptr, t, 1, c.freq_dim, D, m->W("time_mlp.fc1.weight"), m->V("time_mlp.fc1.bias"),
                        m->W("time_mlp.fc2.weight"), m->V("time_mlp.fc2.bias"), m->bf16, thid, mvec, s));
-    K_TRY(add_tables(mvec, 1, D, 6, m->V("blocks.0.mod_table"), c.depth, tabs, s));
-    if (tabs_c) K_TRY(add_tables(mvec, 1, D, 6, m->V("blocks.0.ctx.mod_table"), c.depth, tabs_c, s));
-    K_TRY(add_tables(mvec, 1, D, 2, m->V("head.mod_table"), 1, headtab, s));
-    K_TRY(patchify(latents, Bq, cfg ? 2 : 1, c.in_channels, thw[0], thw[1], thw[2], c.patch[0], c.patch[1],
+    LAUNCH(DIT_KERNEL_SMALL, 1, add_tables(mvec, 1, D, 6, m->V("blocks.0.mod_table"), c.depth, tabs, s));
+    if (tabs_c) LAUNCH(DIT_KERNEL_SMALL, 1, add_tables(mvec, 1, D, 6, m->V("blocks.0.ctx.mod_table"), c.depth, tabs_c, s));
+    LAUNCH(DIT_KERNEL_SMALL, 1, add_tables(mvec, 1, D, 2, m->V("head.mod_table"), 1, headtab, s));
+    LAUNCH(DIT_KERNEL_SMALL, 1, patchify(latents, Bq, cfg ? 2 : 1, c.in_channels, thw[0], thw[1], thw[2], c.patch[0], c.patch[1],
                    c.patch[2], tokens, m->bf16, s));
-    DIT_TRY(do_gemm(m, tokens, (int64_t)B * N, P, P, m->W("patch_embed.weight"), D,
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_EMBED, tokens, (int64_t)B * N, P, P, m->W("patch_embed.weight"), D,
                     epi_store(EPI_F32, m->V("patch_embed.bias"), x, D), s));
     if (c.cond_mode == DIT_COND_JOINT) {
       CU_TRY(cudaMemcpyAsync(xc, cond, cond_bytes, cudaMemcpyDeviceToDevice, s));
@@ -888,11 +937,11 @@ extern "C" dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, 
                         tabs_c ? tabs_c + (size_t)blk * 6 * D : nullptr, 0, kc, vc, B, N, L, blk + 1 < c.depth, bb,
                         s));
     }
-    K_TRY(ln_modulate(x, (int64_t)B * N, D, N, headtab, headtab + D, 0, c.ln_eps, bb.h, m->bf16, s));
-    DIT_TRY(do_gemm(m, bb.h, (int64_t)B * N, D, D, m->W("head.weight"), P,
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, (int64_t)B * N, D, N, headtab, headtab + D, 0, c.ln_eps, bb.h, m->bf16, s));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_EMBED, bb.h, (int64_t)B * N, D, D, m->W("head.weight"), P,
                     epi_store(EPI_F32, m->V("head.bias"), vt, P), s));
     const float dsig = (float)((double)sigmas[i + 1] - (double)sigmas[i]);
-    K_TRY(cfg_euler_tokens(vt, Bq, cfg, guidance, dsig, c.in_channels, thw[0], thw[1], thw[2], c.patch[0],
+    LAUNCH(DIT_KERNEL_SMALL, 1, cfg_euler_tokens(vt, Bq, cfg, guidance, dsig, c.in_channels, thw[0], thw[1], thw[2], c.patch[0],
                            c.patch[1], c.patch[2], latents, s));
   }
   return DIT_OK;
@@ -909,5 +958,36 @@ extern "C" dit_status dit_synchronize(dit_model* m, void* stream) {
     CU_TRY(cudaMemset(m->d_err, 0, sizeof(int)));
     return fail(DIT_ERR_TIMEOUT, "a kernel abandoned a bounded wait (site %d); outputs are invalid", h);
   }
+  return DIT_OK;
+}
+
+extern "C" dit_status dit_profile_start(dit_model* m, int timing) {
+  g_last_error[0] = 0;
+  if (!m) return fail(DIT_ERR_INVALID_ARG, "model is NULL");
+  for (int k = 0; k < DIT_KERNEL_KINDS; ++k) m->prof_counts[k] = 0;
+  m->prof_rec.clear();
+  m->prof_next = 0;
+  m->prof_timing = timing != 0;
+  return DIT_OK;
+}
+
+extern "C" dit_status dit_profile_stop(dit_model* m, int64_t* counts, double* ms) {
+  g_last_error[0] = 0;
+  if (!m) return fail(DIT_ERR_INVALID_ARG, "model is NULL");
+  CU_TRY(cudaSetDevice(m->device));
+  CU_TRY(cudaDeviceSynchronize());
+  double acc[DIT_KERNEL_KINDS] = {};
+  for (const auto& r : m->prof_rec) {
+    float t = 0.f;
+    CU_TRY(cudaEventElapsedTime(&t, r.a, r.b));
+    acc[r.kind] += t;
+  }
+  for (int k = 0; k < DIT_KERNEL_KINDS; ++k) {
+    if (counts) counts[k] = m->prof_counts[k];
+    if (ms) ms[k] = acc[k];
+  }
+  m->prof_timing = false;
+  m->prof_rec.clear();
+  m->prof_next = 0;
   return DIT_OK;
 }

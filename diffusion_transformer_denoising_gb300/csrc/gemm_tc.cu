@@ -114,6 +114,8 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------ MMA issuer
     uint32_t stage = 0, phase = 0, local = 0;
     bool ok = true;
+    const uint64_t a_desc = umma_desc_sw128(smem_u32(smem), 16, 1024);
+    const uint64_t b_desc = umma_desc_sw128(smem_u32(smem) + C::A_BYTES, 16, 1024);
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
       const uint32_t acc = local & 1, aphase = (local >> 1) & 1;
       if (lane == 0) ok = mbar_wait(&tempty[acc], aphase ^ 1, abort_flag, err, 12);
@@ -127,14 +129,11 @@ __global__ void __launch_bounds__(192, 1)
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t a0 = smem_u32(smem + stage * C::STAGE_BYTES);
-          const uint32_t b0 = a0 + C::A_BYTES;
+          const uint64_t ad = umma_desc_add(a_desc, stage * C::STAGE_BYTES);
+          const uint64_t bd = umma_desc_add(b_desc, stage * C::STAGE_BYTES);
 #pragma unroll
-          for (int k = 0; k < C::BK / 16; ++k) {
-            const uint64_t ad = umma_desc_sw128(a0 + k * 32, 16, 1024);
-            const uint64_t bd = umma_desc_sw128(b0 + k * 32, 16, 1024);
-            umma_ss(d_tmem, ad, bd, C::IDESC, (kb | k) != 0);
-          }
+          for (int k = 0; k < C::BK / 16; ++k)
+            umma_ss(d_tmem, umma_desc_add(ad, k * 32), umma_desc_add(bd, k * 32), C::IDESC, (kb | k) != 0);
           umma_commit(&empty[stage]);
         }
         __syncwarp();

@@ -26,7 +26,10 @@ LOOP_PARTIAL_SCHEDULE = 1
 EXPORTS = ["dit_create", "dit_load_weights", "dit_num_params", "dit_param_info", "dit_timestep_modulation",
            "dit_patch_embed", "dit_block_forward", "dit_final_layer", "cfg_combine", "flow_euler_step",
            "dit_denoise_loop", "dit_synchronize", "dit_device_bytes", "dit_destroy", "dit_status_string",
-           "dit_last_error", "dit_debug_fail_alloc_after"]
+           "dit_last_error", "dit_debug_fail_alloc_after", "dit_profile_start", "dit_profile_stop"]
+
+KERNEL_KINDS = ["gemm_qkv", "gemm_out", "gemm_cross_q", "gemm_cross_kv", "gemm_ffn1", "gemm_ffn2", "gemm_embed",
+                "attn_self", "attn_cross", "ln", "small"]
 
 
 class DitConfig(C.Structure):
@@ -81,6 +84,8 @@ def lib():
         "dit_status_string": ([C.c_int], C.c_char_p),
         "dit_last_error": ([], C.c_char_p),
         "dit_debug_fail_alloc_after": ([C.c_int], None),
+        "dit_profile_start": ([vp, C.c_int], C.c_int),
+        "dit_profile_stop": ([vp, C.POINTER(i64), C.POINTER(C.c_double)], C.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -235,6 +240,16 @@ class DiT:
         _check(lib().dit_denoise_loop(self.h, _ptr(latents), batch, a, _ptr(cond), _ptr(uncond), cond_len,
                                       sg.ctypes.data_as(C.POINTER(C.c_float)), len(sg) - 1, guidance, flags,
                                       _stream(stream)))
+
+    def dit_profile_start(self, timing: bool = True):
+        _check(lib().dit_profile_start(self.h, 1 if timing else 0))
+
+    def dit_profile_stop(self):
+        """{kind: (launches, total device ms)} since dit_profile_start."""
+        n = len(KERNEL_KINDS)
+        counts, ms = (C.c_int64 * n)(), (C.c_double * n)()
+        _check(lib().dit_profile_stop(self.h, counts, ms))
+        return {k: (counts[i], ms[i]) for i, k in enumerate(KERNEL_KINDS)}
 
     def dit_synchronize(self, stream=None):
         _check(lib().dit_synchronize(self.h, _stream(stream)))

@@ -197,6 +197,29 @@ dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, const int32
  * invalid; the flag is cleared). */
 dit_status dit_synchronize(dit_model* m, void* stream);
 
+/* Per-kernel accounting of this model's launches, for measurement.
+ * dit_profile_start resets the counters and, when `timing` is non-zero,
+ * records a CUDA event pair on the launching stream around every launch.
+ * dit_profile_stop synchronises the device and returns, per kernel kind,
+ * the number of kernel launches and (with timing) their summed device time
+ * in milliseconds.  counts/ms: host arrays of DIT_KERNEL_KINDS entries. */
+enum {
+  DIT_KERNEL_GEMM_QKV = 0,    /* self-attention Q/K/V projection (+RoPE scatter)  */
+  DIT_KERNEL_GEMM_OUT = 1,    /* attention output projections (gated residual)   */
+  DIT_KERNEL_GEMM_CROSS_Q = 2,
+  DIT_KERNEL_GEMM_CROSS_KV = 3,
+  DIT_KERNEL_GEMM_FFN1 = 4,   /* MLP up-projection + GELU                         */
+  DIT_KERNEL_GEMM_FFN2 = 5,   /* MLP down-projection (gated residual)             */
+  DIT_KERNEL_GEMM_EMBED = 6,  /* patch embedding and final linear                 */
+  DIT_KERNEL_ATTN_SELF = 7,
+  DIT_KERNEL_ATTN_CROSS = 8,
+  DIT_KERNEL_LN = 9,          /* LayerNorm + adaLN modulation                     */
+  DIT_KERNEL_SMALL = 10,      /* timestep MLP, tables, packing, CFG + Euler, casts */
+  DIT_KERNEL_KINDS = 11
+};
+dit_status dit_profile_start(dit_model* m, int timing);
+dit_status dit_profile_stop(dit_model* m, int64_t* counts, double* ms);
+
 /* Bytes of device memory held by the model (weights + workspace). */
 int64_t dit_device_bytes(const dit_model* m);
 
