@@ -108,67 +108,61 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == TMA_WARP) {
-    // ------------------------------------------------ TMA producer
-    int k_issued[KST] = {0, 0, 0}, v_issued[VST] = {0, 0, 0};
-    bool ok = true;
+    // ------------------------------------------------ TMA producer (one thread)
     if (lane == 0) {
+      int k_issued[KST] = {0, 0, 0}, v_issued[VST] = {0, 0, 0};
+      bool ok = true;
       mbar_arrive_expect_tx(q_full, TILE_BYTES);
       tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, q0, bh);
       tma_load_3d(smem + Q_OFF + TILE_BYTES / 2, &tmQ, q_full, 64, q0, bh);
-    }
-    for (int j = 0; j < nkv; ++j) {
-      const int jt = (j + kv_rot) % nkv;
-      const int ks = j % KST, vs = j % VST;
-      // K_j's stage held K_{j-3}: free once S_{j-3} completed (completion j-3)
-      if (j >= KST && lane == 0) ok = mbar_wait(&done[(j - 3) % 3], (uint32_t)(((j - 3) / 3) & 1), abort_flag, err, 21);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (lane == 0) {
+      for (int j = 0; j < nkv; ++j) {
+        const int jt = (j + kv_rot) % nkv;
+        const int ks = j % KST, vs = j % VST;
+        // K_j's stage held K_{j-3}: free once S_{j-3} completed (completion j-3)
+        if (j >= KST) ok = mbar_wait(&done[(j - 3) % 3], (uint32_t)(((j - 3) / 3) & 1), abort_flag, err, 21);
+        if (!ok) break;
         uint8_t* kb = smem + K_OFF + ks * TILE_BYTES;
         mbar_arrive_expect_tx(&k_full[ks], TILE_BYTES);
         tma_load_3d(kb, &tmK, &k_full[ks], 0, jt * BKV, bh);
         tma_load_3d(kb + TILE_BYTES / 2, &tmK, &k_full[ks], 64, jt * BKV, bh);
-      }
-      ++k_issued[ks];
-      // V_j's stage held V_{j-3}: free once PV_{j-3} completed (completion j-1)
-      if (j >= VST && lane == 0) ok = mbar_wait(&done[(j - 1) % 3], (uint32_t)(((j - 1) / 3) & 1), abort_flag, err, 22);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (lane == 0) {
+        ++k_issued[ks];
+        // V_j's stage held V_{j-3}: free once PV_{j-3} completed (completion j-1)
+        if (j >= VST) ok = mbar_wait(&done[(j - 1) % 3], (uint32_t)(((j - 1) / 3) & 1), abort_flag, err, 22);
+        if (!ok) break;
         uint8_t* vb = smem + V_OFF + vs * TILE_BYTES;
         mbar_arrive_expect_tx(&v_full[vs], TILE_BYTES);
         tma_load_3d(vb, &tmV, &v_full[vs], 0, jt * BKV, bh);
         tma_load_3d(vb + TILE_BYTES / 2, &tmV, &v_full[vs], 64, jt * BKV, bh);
+        ++v_issued[vs];
       }
-      ++v_issued[vs];
-    }
-    if (!ok && lane == 0) {
-      // wind down: every copy this thread started lands before the CTA exits
-      volatile int no_abort = 0;
-      mbar_wait(q_full, 0, &no_abort, nullptr, 0);
-      for (int s = 0; s < KST; ++s)
-        if (k_issued[s] > 0) mbar_wait(&k_full[s], (uint32_t)((k_issued[s] - 1) & 1), &no_abort, nullptr, 0);
-      for (int s = 0; s < VST; ++s)
-        if (v_issued[s] > 0) mbar_wait(&v_full[s], (uint32_t)((v_issued[s] - 1) & 1), &no_abort, nullptr, 0);
+      if (!ok) {
+        // wind down: every copy this thread started lands before the CTA exits
+        volatile int no_abort = 0;
+        mbar_wait(q_full, 0, &no_abort, nullptr, 0);
+        for (int s = 0; s < KST; ++s)
+          if (k_issued[s] > 0) mbar_wait(&k_full[s], (uint32_t)((k_issued[s] - 1) & 1), &no_abort, nullptr, 0);
+        for (int s = 0; s < VST; ++s)
+          if (v_issued[s] > 0) mbar_wait(&v_full[s], (uint32_t)((v_issued[s] - 1) & 1), &no_abort, nullptr, 0);
+      }
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
-    // ------------------------------------------------ MMA issuer
-    auto wait1 = [&](uint64_t* bar, uint32_t parity, int site) -> bool {
-      bool r = true;
-      if (lane == 0) r = mbar_wait(bar, parity, abort_flag, err, site);
-      return __shfl_sync(0xffffffffu, r, 0);
-    };
-    // base descriptors, built once; per MMA only a constant is added
-    const uint64_t q_desc = umma_desc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
-    const uint64_t k_desc = umma_desc_sw128(smem_u32(smem + K_OFF), 16, 1024);
-    const uint64_t v_desc = umma_desc_sw128(smem_u32(smem + V_OFF), 16384, 1024);
-    // S_j = Q K_j^T into S slot j % 2 (no commit here)
-    auto issue_s = [&](int j) -> bool {
-      const int ks = j % KST;
-      if (!wait1(&k_full[ks], (uint32_t)((j / KST) & 1), 23)) return false;
-      tc_fence_after();
-      if (lane == 0) {
+    // ------------------------------------------------ MMA issuer (one thread)
+    // The whole role runs on lane 0: a warp that diverges and reconverges
+    // around every MMA burst costs the tensor pipe a large share of its rate.
+    if (lane == 0) {
+      auto wait1 = [&](uint64_t* bar, uint32_t parity, int site) -> bool {
+        return mbar_wait(bar, parity, abort_flag, err, site);
+      };
+      // base descriptors, built once; per MMA only a constant is added
+      const uint64_t q_desc = umma_desc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
+      const uint64_t k_desc = umma_desc_sw128(smem_u32(smem + K_OFF), 16, 1024);
+      const uint64_t v_desc = umma_desc_sw128(smem_u32(smem + V_OFF), 16384, 1024);
+      // S_j = Q K_j^T into S slot j % 2 (no commit here)
+      auto issue_s = [&](int j) -> bool {
+        const int ks = j % KST;
+        if (!wait1(&k_full[ks], (uint32_t)((j / KST) & 1), 23)) return false;
+        tc_fence_after();
         const uint64_t kd = umma_desc_add(k_desc, ks * TILE_BYTES);
         const uint32_t d_tmem = tmem + TM_S + (j & 1) * 128;
 #pragma unroll
@@ -176,25 +170,21 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
           const uint32_t off = (kk >> 2) * (TILE_BYTES / 2) + (kk & 3) * 32;
           umma_ss(d_tmem, umma_desc_add(q_desc, off), umma_desc_add(kd, off), IDESC_S, kk != 0);
         }
+        return true;
+      };
+      bool ok = wait1(q_full, 0, 24);
+      if (ok) ok = issue_s(0);
+      if (ok) umma_commit(&done[0]);  // completion 0: S_0
+      if (ok && nkv > 1) {
+        ok = issue_s(1);
+        if (ok) umma_commit(&done[1]);  // completion 1: S_1
       }
-      __syncwarp();
-      return true;
-    };
-    bool ok = wait1(q_full, 0, 24);
-    if (ok) ok = issue_s(0);
-    if (ok && lane == 0) umma_commit(&done[0]);  // completion 0: S_0
-    if (ok && nkv > 1) {
-      ok = issue_s(1);
-      if (ok && lane == 0) umma_commit(&done[1]);  // completion 1: S_1
-    }
-    __syncwarp();
-    for (int j = 0; ok && j < nkv; ++j) {
-      const int vs = j % VST;
-      ok = wait1(&p_ready[j & 1], (uint32_t)((j >> 1) & 1), 25) &&
-           wait1(&v_full[vs], (uint32_t)((j / VST) & 1), 26);
-      if (!ok) break;
-      tc_fence_after();
-      if (lane == 0) {
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int vs = j % VST;
+        ok = wait1(&p_ready[j & 1], (uint32_t)((j >> 1) & 1), 25) &&
+             wait1(&v_full[vs], (uint32_t)((j / VST) & 1), 26);
+        if (!ok) break;
+        tc_fence_after();
         const uint64_t vd = umma_desc_add(v_desc, vs * TILE_BYTES);
         const uint32_t p_tmem = tmem + TM_S + (j & 1) * 128;
 #pragma unroll
@@ -205,13 +195,9 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
             umma_ts(tmem + TM_O + h * 128, p_tmem + h * 32 + kk * 8, umma_desc_add(vd, (4 * h + kk) * 2048),
                     IDESC_O, (j | kk) != 0);
           }
+        if (j + 2 < nkv) ok = issue_s(j + 2);
+        umma_commit(&done[(j + 2) % 3]);  // completion j+2: PV_j (+ S_{j+2})
       }
-      __syncwarp();
-      if (j + 2 < nkv) ok = issue_s(j + 2);
-      if (lane == 0) umma_commit(&done[(j + 2) % 3]);  // completion j+2: PV_j (+ S_{j+2})
-      __syncwarp();
-    }
-    if (lane == 0) {
       umma_commit(drain);
       volatile int no_abort = 0;
       mbar_wait(drain, 0, &no_abort, nullptr, 0);
@@ -226,8 +212,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      if (lane == 0) ok = mbar_wait(&done[j % 3], (uint32_t)((j / 3) & 1), abort_flag, err, 31);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ok = __all_sync(0xffffffffu, mbar_wait(&done[j % 3], (uint32_t)((j / 3) & 1), abort_flag, err, 31));
       if (!ok) break;
       tc_fence_after();
       const uint32_t s_col = tmem + TM_S + (j & 1) * 128 + lane_off;
@@ -263,8 +248,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
         const bool need = m_new - m_used > RESCALE_THRESHOLD;
         if (__any_sync(0xffffffffu, need)) {
           // O_h must hold PV_{j-1} (completion j+1) before it is rescaled
-          if (lane == 0) ok = mbar_wait(&done[(j + 1) % 3], (uint32_t)(((j + 1) / 3) & 1), abort_flag, err, 32);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
+          ok = __all_sync(0xffffffffu, mbar_wait(&done[(j + 1) % 3], (uint32_t)(((j + 1) / 3) & 1), abort_flag, err, 32));
           if (!ok) break;
           tc_fence_after();
           if (need) {
@@ -304,8 +288,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     }
     if (ok) {
       // PV_{nkv-1} is completion nkv+1
-      if (lane == 0) ok = mbar_wait(&done[(nkv + 1) % 3], (uint32_t)(((nkv + 1) / 3) & 1), abort_flag, err, 33);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ok = __all_sync(0xffffffffu, mbar_wait(&done[(nkv + 1) % 3], (uint32_t)(((nkv + 1) / 3) & 1), abort_flag, err, 33));
     }
     if (ok) {
       // merge the two halves: swap (m, l) with the partner warp of the quadrant
@@ -313,8 +296,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       xch[(2 + h) * BQ + row] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(&fin[q]);
-      if (lane == 0) ok = mbar_wait(&fin[q], 0, abort_flag, err, 34);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ok = __all_sync(0xffffffffu, mbar_wait(&fin[q], 0, abort_flag, err, 34));
     }
     if (ok) {
       tc_fence_after();

@@ -79,75 +79,71 @@ __global__ void __launch_bounds__(192, 1)
   const int num_tiles = m_tiles * n_tiles;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer
-    uint32_t stage = 0, phase = 0;
-    int issued[C::STAGES];
+    // ------------------------------------------------ TMA producer (one thread)
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int issued[C::STAGES];
 #pragma unroll
-    for (int s = 0; s < C::STAGES; ++s) issued[s] = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-      const int mb = tile / n_tiles, nb = tile - mb * n_tiles;
-      for (int kb = 0; kb < k_blocks; ++kb) {
-        if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, 11);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        if (lane == 0) {
+      for (int s = 0; s < C::STAGES; ++s) issued[s] = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int mb = tile / n_tiles, nb = tile - mb * n_tiles;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, 11);
+          if (!ok) break;
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
           tma_load_2d(sa, &tmA, &full[stage], kb * C::BK, mb * C::BM);
           tma_load_2d(sa + C::A_BYTES, &tmB, &full[stage], kb * C::BK, nb * BN);
-        }
-        ++issued[stage];
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1;
+          ++issued[stage];
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
       }
+      if (!ok) {
+        // wind down: let every copy this thread started land before the CTA exits
+        volatile int no_abort = 0;
+        for (int s = 0; s < C::STAGES; ++s)
+          if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1), &no_abort, nullptr, 0);
+      }
     }
-    if (!ok && lane == 0) {
-      // wind down: let every copy this thread started land before the CTA exits
-      volatile int no_abort = 0;
-      for (int s = 0; s < C::STAGES; ++s)
-        if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1), &no_abort, nullptr, 0);
-    }
+    __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
-    uint32_t stage = 0, phase = 0, local = 0;
-    bool ok = true;
-    const uint64_t a_desc = umma_desc_sw128(smem_u32(smem), 16, 1024);
-    const uint64_t b_desc = umma_desc_sw128(smem_u32(smem) + C::A_BYTES, 16, 1024);
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
-      const uint32_t acc = local & 1, aphase = (local >> 1) & 1;
-      if (lane == 0) ok = mbar_wait(&tempty[acc], aphase ^ 1, abort_flag, err, 12);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
-      for (int kb = 0; kb < k_blocks; ++kb) {
-        if (lane == 0) ok = mbar_wait(&full[stage], phase, abort_flag, err, 13);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+    // ------------------------------------------------ MMA issuer (one thread)
+    // The whole role runs on lane 0: a warp that diverges and reconverges
+    // around every MMA burst costs the tensor pipe a large share of its rate.
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, local = 0;
+      bool ok = true;
+      const uint64_t a_desc = umma_desc_sw128(smem_u32(smem), 16, 1024);
+      const uint64_t b_desc = umma_desc_sw128(smem_u32(smem) + C::A_BYTES, 16, 1024);
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+        const uint32_t acc = local & 1, aphase = (local >> 1) & 1;
+        ok = mbar_wait(&tempty[acc], aphase ^ 1, abort_flag, err, 12);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          ok = mbar_wait(&full[stage], phase, abort_flag, err, 13);
+          if (!ok) break;
+          tc_fence_after();
           const uint64_t ad = umma_desc_add(a_desc, stage * C::STAGE_BYTES);
           const uint64_t bd = umma_desc_add(b_desc, stage * C::STAGE_BYTES);
 #pragma unroll
           for (int k = 0; k < C::BK / 16; ++k)
             umma_ss(d_tmem, umma_desc_add(ad, k * 32), umma_desc_add(bd, k * 32), C::IDESC, (kb | k) != 0);
           umma_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
-        __syncwarp();
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
       }
-      if (!ok) break;
-      if (lane == 0) umma_commit(&tfull[acc]);
-      __syncwarp();
-    }
-    // all MMAs issued by this thread complete before TMEM is released
-    if (lane == 0) {
+      // all MMAs issued by this thread complete before TMEM is released
       umma_commit(drain);
       volatile int no_abort = 0;
       mbar_wait(drain, 0, &no_abort, nullptr, 0);
@@ -161,8 +157,7 @@ __global__ void __launch_bounds__(192, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
       const uint32_t acc = local & 1, aphase = (local >> 1) & 1;
-      if (lane == 0) ok = mbar_wait(&tfull[acc], aphase, abort_flag, err, 14);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], aphase, abort_flag, err, 14));
       if (!ok) break;
       tc_fence_after();
       const int mb = tile / n_tiles, nb = tile - mb * n_tiles;
