@@ -1,0 +1,135 @@
+"""Parity at the full workload sizes, in the launch configuration the bench
+times (batch 2 = conditional + unconditional pass): the CUDA path runs the
+whole block; the oracle computes keys/values over every token and the block
+output for a sample of rows (first, last, ragged-tail and spread rows)."""
+import numpy as np
+import pytest
+
+from diffusion_transformer_denoising_gb300 import synth
+from oracle import dit_oracle as O
+from tests.gpu_util import COS_BF16_LOOP, TOL_BF16_BLOCK, cosine, dev, empty, host, make_model, rel_max_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows(n, extra=()):
+    r = set(np.linspace(0, n - 1, 40).astype(int).tolist()) | {0, 1, n - 1, n - 2} | set(extra)
+    return np.array(sorted(x for x in r if 0 <= x < n))
+
+
+@pytest.fixture(scope="module")
+def video_block():
+    cfg = synth.config("video", depth=1)
+    W = synth.make_weights(cfg, seed=0)
+    m = make_model(cfg, W)
+    yield cfg, W, m
+    m.close()
+
+
+def test_video_block_full_size(video_block):
+    """One video block: 32760 tokens (21 x 30 x 52 grid), 512 text tokens,
+    batch 2 (condition / zero condition), timestep 700 (sigma 0.7)."""
+    cfg, W, m = video_block
+    grid = synth.grid(cfg)
+    N, L = int(np.prod(grid)), cfg["cond_len"]
+    lat = synth.make_latent(cfg, batch=1, seed=1)
+    ctx = np.concatenate([synth.make_cond(cfg, batch=1, seed=2), np.zeros((1, L, cfg["cond_dim"]), np.float32)])
+    # block input: the patch-embedded latent (both passes see the same latent)
+    x0 = np.stack([O.patch_embed(lat[0], W, cfg)] * 2).astype(np.float32)
+    mod = O.timestep_modulation(700.0, W, cfg)
+    mods = np.stack([mod, mod]).astype(np.float32)
+    x = dev(x0)
+    m.dit_block_forward(0, x, None, dev(mods), dev(ctx), 2, grid, L)
+    m.dit_synchronize()
+    got = host(x)
+    rows = _rows(N, extra=range(N - 120, N - 110))   # rows of the last (ragged) 128-row query tile
+    angles = O.rope_angles(O.token_positions(grid), cfg["rope_axes"], cfg["rope_theta"])
+    for b in range(2):
+        ref = O.block_cross(x0[b], mods[b], ctx[b], W, 0, cfg, grid, rows=rows, angles=angles)
+        assert rel_max_err(got[b][rows], ref) < TOL_BF16_BLOCK
+        assert rel_max_err(got[b][rows] - x0[b][rows], ref - x0[b][rows]) < 5 * TOL_BF16_BLOCK
+
+
+@pytest.fixture(scope="module")
+def image_model():
+    cfg = synth.config("image", depth=2)
+    W = synth.make_weights(cfg, seed=0)
+    m = make_model(cfg, W)
+    yield cfg, W, m
+    m.close()
+
+
+def test_image_block_full_size(image_model):
+    """One dual-stream image block: 4096 image tokens (64 x 64) jointly
+    attending with 512 condition tokens, batch 2."""
+    cfg, W, m = image_model
+    grid = synth.grid(cfg)
+    N, L, D = int(np.prod(grid)), cfg["cond_len"], cfg["hidden"]
+    rng = np.random.default_rng(3)
+    x0 = (rng.standard_normal((2, N, D)) * 0.2).astype(np.float32)
+    xc0 = np.concatenate([synth.make_cond(cfg, batch=1, seed=4), np.zeros((1, L, D), np.float32)])
+    mod = O.timestep_modulation(500.0, W, cfg)
+    mods = np.stack([mod, mod]).astype(np.float32)
+    x, xc = dev(x0), dev(xc0)
+    m.dit_block_forward(1, x, xc, dev(mods), None, 2, grid, L)
+    m.dit_synchronize()
+    gx, gc = host(x), host(xc)
+    rows = _rows(L + N, extra=range(L - 3, L + 3))   # both streams and their boundary
+    angles = O.rope_angles(O.token_positions(grid), cfg["rope_axes"], cfg["rope_theta"])
+    for b in range(2):
+        ref = O.block_joint(x0[b], xc0[b], mods[b], W, 1, cfg, grid, rows=rows, angles=angles)
+        got = np.concatenate([gc[b], gx[b]])[rows]
+        assert rel_max_err(got, ref) < TOL_BF16_BLOCK
+
+
+def test_image_loop_full_tokens_reduced_depth(image_model):
+    """The whole denoise loop at the full 4096 + 512 token count, depth 2,
+    two Euler steps with CFG: final latents against the full oracle loop."""
+    cfg, W, m = image_model
+    L = cfg["cond_len"]
+    lat = synth.make_latent(cfg, batch=1, seed=5)
+    cond = synth.make_cond(cfg, batch=1, seed=6)
+    unc = np.zeros_like(cond)
+    sig = O.shift_sigma(O.sigma_schedule(2), cfg["shift"]).astype(np.float32)
+    x = dev(lat)
+    m.dit_denoise_loop(x, 1, cfg["latent"], dev(cond), dev(unc), L, sig, cfg["guidance"])
+    m.dit_synchronize()
+    got = host(x)[0]
+    ref = O.denoise_loop(lat[0], cond[0], unc[0], W, cfg, sig.astype(np.float64), cfg["guidance"])
+    assert cosine(got, ref) >= COS_BF16_LOOP
+    assert cosine(got - lat[0], ref - lat[0]) >= 0.99
+
+
+def test_video_embed_head_and_cfg_euler_full_size(video_block):
+    """Patch embedding, final layer and guidance + Euler at the full video
+    latent size (16 x 21 x 60 x 104)."""
+    cfg, W, m = video_block
+    thw = cfg["latent"]
+    grid = synth.grid(cfg)
+    N, D = int(np.prod(grid)), cfg["hidden"]
+    lat = synth.make_latent(cfg, batch=2, seed=7)
+    x = empty(2, N, D)
+    m.dit_patch_embed(dev(lat), 2, thw, x)
+    m.dit_synchronize()
+    gx = host(x)
+    rows = _rows(N)
+    for b in range(2):
+        lat_b = synth.round_bf16(lat[b]).astype(np.float64)
+        assert rel_max_err(gx[b][rows], O.patch_embed(lat_b, W, cfg)[rows]) < 1e-3
+    mods = np.stack([O.timestep_modulation(t, W, cfg) for t in (900.0, 100.0)]).astype(np.float32)
+    v = empty(2, cfg["in_channels"], *thw)
+    xs = (gx * 0.5).astype(np.float32)
+    m.dit_final_layer(dev(xs), dev(mods), 2, thw, v)
+    m.dit_synchronize()
+    gv = host(v)
+    for b in range(2):
+        ref = O.unpatchify(O.final_layer(xs[b], mods[b], W, cfg), cfg["patch"], (cfg["in_channels"],) + thw)
+        assert rel_max_err(gv[b], ref) < TOL_BF16_BLOCK
+    from diffusion_transformer_denoising_gb300 import dit
+    n = gv[0].size
+    out = empty(n)
+    dit.cfg_combine(dev(gv[0]), dev(gv[1]), 5.0, out, n)
+    xl = dev(lat[0])
+    dit.flow_euler_step(xl, out, 0.7, 0.65, n)
+    ref = O.euler_step(lat[0], O.cfg_combine(gv[0], gv[1], 5.0), 0.7, 0.65)
+    np.testing.assert_allclose(host(xl).reshape(ref.shape), ref, rtol=0, atol=1e-4)
