@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 #include <string>
 #include <unordered_map>
 #include <vector>
@@ -722,6 +723,57 @@ extern "C" dit_status dit_timestep_modulation(dit_model* m, const float* t_host,
   LAUNCH(DIT_KERNEL_SMALL, 2, timestep_mlp(m->d_t, 0.0, batch, m->cfg.freq_dim, m->cfg.hidden, m->W("time_mlp.fc1.weight"),
                      m->V("time_mlp.fc1.bias"), m->W("time_mlp.fc2.weight"), m->V("time_mlp.fc2.bias"), m->bf16,
                      static_cast<float*>(m->ws), mod, s));
+  return DIT_OK;
+}
+
+// ------------------------------------------------------------ no-allocation variant
+// Scratch of dit_timestep_modulation_noalloc: DIT_NOALLOC_MAX_BATCH timesteps
+// followed by DIT_NOALLOC_MAX_HIDDEN hidden activations, in module memory
+// that is never allocated or freed by a call.  In host code the symbol is a
+// host-side stand-in, so its device address is looked up once per device.
+static __device__ __align__(256) float g_noalloc_scratch[DIT_NOALLOC_MAX_BATCH + DIT_NOALLOC_MAX_HIDDEN];
+static std::mutex g_noalloc_mutex;
+static std::unordered_map<int, float*> g_noalloc_addr;  // device -> device address of the scratch
+
+static dit_status noalloc_scratch(int device, float** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  auto it = g_noalloc_addr.find(device);
+  if (it != g_noalloc_addr.end()) {
+    *out = it->second;
+    return DIT_OK;
+  }
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // caller made `device` current
+  if (e != cudaSuccess || !p)
+    return fail(DIT_ERR_CUDA, "cudaGetSymbolAddress of the fixed scratch failed: %s", cudaGetErrorString(e));
+  g_noalloc_addr[device] = static_cast<float*>(p);
+  *out = static_cast<float*>(p);
+  return DIT_OK;
+}
+
+extern "C" dit_status dit_timestep_modulation_noalloc(dit_model* m, const float* t_host, int batch, float* mod,
+                                                      void* stream) {
+  g_last_error[0] = 0;
+  DIT_TRY(require_loaded(m));
+  if (!t_host || !mod || batch <= 0) return fail(DIT_ERR_INVALID_ARG, "bad timestep arguments");
+  if (batch > DIT_NOALLOC_MAX_BATCH)
+    return fail(DIT_ERR_INVALID_ARG, "batch %d exceeds the fixed scratch limit of %d", batch,
+                (int)DIT_NOALLOC_MAX_BATCH);
+  if ((int64_t)batch * m->cfg.hidden > DIT_NOALLOC_MAX_HIDDEN)
+    return fail(DIT_ERR_INVALID_ARG, "batch * hidden = %lld exceeds the fixed scratch limit of %d floats",
+                (long long)batch * m->cfg.hidden, (int)DIT_NOALLOC_MAX_HIDDEN);
+  for (int b = 0; b < batch; ++b)
+    if (!isfinite(t_host[b])) return fail(DIT_ERR_INVALID_ARG, "timestep %d is not finite", b);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CU_TRY(cudaSetDevice(m->device));
+  float* scratch = nullptr;
+  DIT_TRY(noalloc_scratch(m->device, &scratch));
+  float* t_dev = scratch;                          // [batch] timesteps
+  float* hidden = scratch + DIT_NOALLOC_MAX_BATCH;  // [batch, hidden], fully written by fc1 before fc2 reads it
+  CU_TRY(cudaMemcpyAsync(t_dev, t_host, batch * sizeof(float), cudaMemcpyHostToDevice, s));
+  K_TRY(timestep_mlp(t_dev, 0.0, batch, m->cfg.freq_dim, m->cfg.hidden, m->W("time_mlp.fc1.weight"),
+                     m->V("time_mlp.fc1.bias"), m->W("time_mlp.fc2.weight"), m->V("time_mlp.fc2.bias"), m->bf16,
+                     hidden, mod, s));
   return DIT_OK;
 }
 

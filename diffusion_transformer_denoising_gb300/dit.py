@@ -26,7 +26,9 @@ LOOP_PARTIAL_SCHEDULE = 1
 EXPORTS = ["dit_create", "dit_load_weights", "dit_num_params", "dit_param_info", "dit_timestep_modulation",
            "dit_patch_embed", "dit_block_forward", "dit_final_layer", "cfg_combine", "flow_euler_step",
            "dit_denoise_loop", "dit_synchronize", "dit_device_bytes", "dit_destroy", "dit_status_string",
-           "dit_last_error", "dit_debug_fail_alloc_after", "dit_profile_start", "dit_profile_stop"]
+           "dit_last_error", "dit_debug_fail_alloc_after", "dit_profile_start", "dit_profile_stop",
+           "dit_timestep_modulation_noalloc"]
+NOALLOC_MAX_BATCH, NOALLOC_MAX_HIDDEN = 64, 262144
 
 KERNEL_KINDS = ["gemm_qkv", "gemm_out", "gemm_cross_q", "gemm_cross_kv", "gemm_ffn1", "gemm_ffn2", "gemm_embed",
                 "attn_self", "attn_cross", "ln", "small"]
@@ -71,6 +73,7 @@ def lib():
         "dit_param_info": ([C.POINTER(DitConfig), C.c_int, C.c_char_p, C.c_int, C.POINTER(i32),
                             C.POINTER(i64)], C.c_int),
         "dit_timestep_modulation": ([vp, C.POINTER(f32), C.c_int, vp, vp], C.c_int),
+        "dit_timestep_modulation_noalloc": ([vp, C.POINTER(f32), C.c_int, vp, vp], C.c_int),
         "dit_patch_embed": ([vp, vp, C.c_int, C.POINTER(i32), vp, vp], C.c_int),
         "dit_block_forward": ([vp, C.c_int, vp, vp, vp, vp, C.c_int, C.POINTER(i32), C.c_int, vp], C.c_int),
         "dit_final_layer": ([vp, vp, vp, C.c_int, C.POINTER(i32), vp, vp], C.c_int),
@@ -219,6 +222,13 @@ class DiT:
         t = np.ascontiguousarray(t_host, dtype=np.float32)
         _check(lib().dit_timestep_modulation(self.h, t.ctypes.data_as(C.POINTER(C.c_float)), len(t), _ptr(mod),
                                              _stream(stream)))
+
+    def dit_timestep_modulation_noalloc(self, t_host, mod, stream=None):
+        """dit_timestep_modulation without any device allocation (fixed
+        library scratch; see include/dit.h for the limits)."""
+        t = np.ascontiguousarray(t_host, dtype=np.float32)
+        _check(lib().dit_timestep_modulation_noalloc(self.h, t.ctypes.data_as(C.POINTER(C.c_float)), len(t),
+                                                     _ptr(mod), _stream(stream)))
 
     def dit_patch_embed(self, latents, batch: int, thw, x, stream=None):
         a = (C.c_int32 * 3)(*thw)

@@ -137,6 +137,27 @@ dit_status dit_param_info(const dit_config* cfg, int i, char* name_buf, int buf_
  *   mod     device float[batch, 6*hidden] output */
 dit_status dit_timestep_modulation(dit_model* m, const float* t_host, int batch, float* mod, void* stream);
 
+/* The same computation as dit_timestep_modulation, for callers that must
+ * not allocate device memory during the call: for example a serving thread
+ * that may not trigger the implicit device synchronisation a cudaMalloc or
+ * cudaFree can cause, or a host whose device memory is entirely handed to
+ * its own pool allocator, so any allocation by this library would fail or
+ * stall.  (The pages have no counterpart; this is an interface addition.)
+ * The call allocates nothing: it never calls cudaMalloc, cudaFree or any
+ * allocating library routine.  Its scratch (the timesteps and the MLP's
+ * hidden activations) lives in one fixed array of this library's device
+ * memory (about 1 MiB), which every GPU that loads the library holds until
+ * the process exits.
+ *   batch <= DIT_NOALLOC_MAX_BATCH and batch * hidden <= DIT_NOALLOC_MAX_HIDDEN,
+ *   otherwise DIT_ERR_INVALID_ARG (nothing is launched).
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All
+ * calls share the one array: calls whose work overlaps on the GPU (for
+ * example on two streams without ordering between them) race with each
+ * other.  Every byte of scratch a call reads it has written itself first. */
+enum { DIT_NOALLOC_MAX_BATCH = 64, DIT_NOALLOC_MAX_HIDDEN = 262144 };
+dit_status dit_timestep_modulation_noalloc(dit_model* m, const float* t_host, int batch, float* mod, void* stream);
+
 /* a2: patchify + patch embedding.
  *   latents device float[batch, C, T, H, W]; latent_thw = {T, H, W}, each
  *           divisible by the patch size (else DIT_ERR_SHAPE)
