@@ -9,7 +9,8 @@
 // Warps 0-3 run the softmax of key half 0 and warps 4-7 that of half 1 (warp
 // w reads TMEM lane quadrant w%4, i.e. 32 query rows), so no warp ever waits
 // for another inside the loop.  Warp 8 streams K and V tiles of 128 keys
-// with TMA through two 3-stage rings; warp 9 issues the MMAs from one thread:
+// with TMA through two 3-stage rings; warp 9 issues the MMAs from one thread,
+// one uninterrupted burst "PV_j, S_{j+2}" per key tile after two waits:
 //     S_j = Q K_j^T                 (SS, K-major operands in shared memory)
 //     O_h += P_j[:, half h] V_j[half h]   (TS: P from tensor memory, V N-major)
 // Tensor memory (512 columns): S double buffer [0,128) [128,256); O_0 at
@@ -64,9 +65,8 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;    // [3]
-  uint64_t* v_full = bars + 4;    // [3]
+  uint64_t* q_full = bars;        // Q, K_0 and K_1
+  uint64_t* xf = bars + 1;        // [3] tile pair j: V_j and K_{j+2} (see the producer)
   uint64_t* done = bars + 7;      // [3] MMA completion ring (see above)
   uint64_t* p_ready = bars + 10;  // [2] per S slot
   uint64_t* drain = bars + 12;
@@ -86,8 +86,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < 3; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
+      mbar_init(&xf[s], 1);
       mbar_init(&done[s], 1);
     }
     for (int b = 0; b < 2; ++b) mbar_init(&p_ready[b], 8);
@@ -109,40 +108,37 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
 
   if (warp == TMA_WARP) {
     // ------------------------------------------------ TMA producer (one thread)
+    // Loads are grouped so that the MMA thread waits once per key tile: barrier
+    // xf[j % 3] covers V_j and K_{j+2}, exactly what "PV_j, S_{j+2}" reads.  Both
+    // stages are free once completion j-1 (PV_{j-3}, S_{j-1}) has landed.
     if (lane == 0) {
-      int k_issued[KST] = {0, 0, 0}, v_issued[VST] = {0, 0, 0};
+      int issued[3] = {0, 0, 0};
       bool ok = true;
-      mbar_arrive_expect_tx(q_full, TILE_BYTES);
+      auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int tile) {
+        const int jt = (tile + kv_rot) % nkv;
+        tma_load_3d(dst, tm, bar, 0, jt * BKV, bh);
+        tma_load_3d(dst + TILE_BYTES / 2, tm, bar, 64, jt * BKV, bh);
+      };
+      mbar_arrive_expect_tx(q_full, (nkv > 1 ? 3 : 2) * TILE_BYTES);
       tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, q0, bh);
       tma_load_3d(smem + Q_OFF + TILE_BYTES / 2, &tmQ, q_full, 64, q0, bh);
+      load_tile(&tmK, smem + K_OFF, q_full, 0);
+      if (nkv > 1) load_tile(&tmK, smem + K_OFF + TILE_BYTES, q_full, 1);
       for (int j = 0; j < nkv; ++j) {
-        const int jt = (j + kv_rot) % nkv;
-        const int ks = j % KST, vs = j % VST;
-        // K_j's stage held K_{j-3}: free once S_{j-3} completed (completion j-3)
-        if (j >= KST) ok = mbar_wait(&done[(j - 3) % 3], (uint32_t)(((j - 3) / 3) & 1), abort_flag, err, 21);
+        if (j >= 1) ok = mbar_wait(&done[(j - 1) % 3], (uint32_t)(((j - 1) / 3) & 1), abort_flag, err, 21);
         if (!ok) break;
-        uint8_t* kb = smem + K_OFF + ks * TILE_BYTES;
-        mbar_arrive_expect_tx(&k_full[ks], TILE_BYTES);
-        tma_load_3d(kb, &tmK, &k_full[ks], 0, jt * BKV, bh);
-        tma_load_3d(kb + TILE_BYTES / 2, &tmK, &k_full[ks], 64, jt * BKV, bh);
-        ++k_issued[ks];
-        // V_j's stage held V_{j-3}: free once PV_{j-3} completed (completion j-1)
-        if (j >= VST) ok = mbar_wait(&done[(j - 1) % 3], (uint32_t)(((j - 1) / 3) & 1), abort_flag, err, 22);
-        if (!ok) break;
-        uint8_t* vb = smem + V_OFF + vs * TILE_BYTES;
-        mbar_arrive_expect_tx(&v_full[vs], TILE_BYTES);
-        tma_load_3d(vb, &tmV, &v_full[vs], 0, jt * BKV, bh);
-        tma_load_3d(vb + TILE_BYTES / 2, &tmV, &v_full[vs], 64, jt * BKV, bh);
-        ++v_issued[vs];
+        const bool has_k = j + 2 < nkv;
+        mbar_arrive_expect_tx(&xf[j % 3], (has_k ? 2 : 1) * TILE_BYTES);
+        load_tile(&tmV, smem + V_OFF + (j % VST) * TILE_BYTES, &xf[j % 3], j);
+        if (has_k) load_tile(&tmK, smem + K_OFF + ((j + 2) % KST) * TILE_BYTES, &xf[j % 3], j + 2);
+        ++issued[j % 3];
       }
       if (!ok) {
         // wind down: every copy this thread started lands before the CTA exits
         volatile int no_abort = 0;
         mbar_wait(q_full, 0, &no_abort, nullptr, 0);
-        for (int s = 0; s < KST; ++s)
-          if (k_issued[s] > 0) mbar_wait(&k_full[s], (uint32_t)((k_issued[s] - 1) & 1), &no_abort, nullptr, 0);
-        for (int s = 0; s < VST; ++s)
-          if (v_issued[s] > 0) mbar_wait(&v_full[s], (uint32_t)((v_issued[s] - 1) & 1), &no_abort, nullptr, 0);
+        for (int s = 0; s < 3; ++s)
+          if (issued[s] > 0) mbar_wait(&xf[s], (uint32_t)((issued[s] - 1) & 1), &no_abort, nullptr, 0);
       }
     }
     __syncwarp();
@@ -158,34 +154,34 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       const uint64_t q_desc = umma_desc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
       const uint64_t k_desc = umma_desc_sw128(smem_u32(smem + K_OFF), 16, 1024);
       const uint64_t v_desc = umma_desc_sw128(smem_u32(smem + V_OFF), 16384, 1024);
-      // S_j = Q K_j^T into S slot j % 2 (no commit here)
-      auto issue_s = [&](int j) -> bool {
-        const int ks = j % KST;
-        if (!wait1(&k_full[ks], (uint32_t)((j / KST) & 1), 23)) return false;
-        tc_fence_after();
-        const uint64_t kd = umma_desc_add(k_desc, ks * TILE_BYTES);
+      // S_j = Q K_j^T into S slot j % 2 (no commit here); K_j is resident
+      auto issue_s = [&](int j) {
+        const uint64_t kd = umma_desc_add(k_desc, (j % KST) * TILE_BYTES);
         const uint32_t d_tmem = tmem + TM_S + (j & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (TILE_BYTES / 2) + (kk & 3) * 32;
           umma_ss(d_tmem, umma_desc_add(q_desc, off), umma_desc_add(kd, off), IDESC_S, kk != 0);
         }
-        return true;
       };
       bool ok = wait1(q_full, 0, 24);
-      if (ok) ok = issue_s(0);
-      if (ok) umma_commit(&done[0]);  // completion 0: S_0
-      if (ok && nkv > 1) {
-        ok = issue_s(1);
-        if (ok) umma_commit(&done[1]);  // completion 1: S_1
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        umma_commit(&done[0]);  // completion 0: S_0
+        if (nkv > 1) {
+          issue_s(1);
+          umma_commit(&done[1]);  // completion 1: S_1
+        }
       }
+      // One uninterrupted burst per key tile: the issuing thread does nothing
+      // between MMAs (any wait or detour there idles the tensor pipe).
       for (int j = 0; ok && j < nkv; ++j) {
-        const int vs = j % VST;
         ok = wait1(&p_ready[j & 1], (uint32_t)((j >> 1) & 1), 25) &&
-             wait1(&v_full[vs], (uint32_t)((j / VST) & 1), 26);
+             wait1(&xf[j % 3], (uint32_t)((j / 3) & 1), 26);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t vd = umma_desc_add(v_desc, vs * TILE_BYTES);
+        const uint64_t vd = umma_desc_add(v_desc, (j % VST) * TILE_BYTES);
         const uint32_t p_tmem = tmem + TM_S + (j & 1) * 128;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
@@ -195,7 +191,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
             umma_ts(tmem + TM_O + h * 128, p_tmem + h * 32 + kk * 8, umma_desc_add(vd, (4 * h + kk) * 2048),
                     IDESC_O, (j | kk) != 0);
           }
-        if (j + 2 < nkv) ok = issue_s(j + 2);
+        if (j + 2 < nkv) issue_s(j + 2);
         umma_commit(&done[(j + 2) % 3]);  // completion j+2: PV_j (+ S_{j+2})
       }
       umma_commit(drain);
