@@ -134,6 +134,31 @@ DIT_DEV void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int x, int 
       : "memory");
 }
 
+// Bulk tensor stores / reductions from shared memory (tracked by bulk groups
+// of the issuing thread).
+DIT_DEV void tma_store_2d(const void* tmap, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
+DIT_DEV void tma_store_3d(const void* tmap, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
+               : "memory");
+}
+// global[tile] += shared tile (element type from the tensor map), done by the TMA unit
+DIT_DEV void tma_reduce_add_2d(const void* tmap, const void* src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
+DIT_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+DIT_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+DIT_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor, K-major or MN-major, 128-byte swizzle.
 // Fields: start address >> 4 (bits 0-13), leading byte offset >> 4 (16-29),

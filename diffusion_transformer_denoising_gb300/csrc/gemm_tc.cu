@@ -4,11 +4,12 @@
 //   fused epilogue (bias, GELU, gated residual into the fp32 stream, or the
 //   head-major Q/K/V scatter with rotary embedding).
 //
-// Roles (192 threads): warp 0 issues TMA loads of 128x64 A and BNx64 W tiles
+// Roles (320 threads): warp 0 issues TMA loads of 128x64 A and BNx64 W tiles
 // (128-byte swizzle) into a STAGES-deep shared-memory ring; warp 1 issues
 // tcgen05.mma (M=128, N=BN, K=16) from one thread into one of two TMEM
-// accumulators; warps 2-5 drain the other accumulator through tcgen05.ld
-// (warp w reads TMEM lanes 32*(w%4)..+31 = its 32 rows) and run the epilogue,
+// accumulators; warps 2-9 drain the other accumulator through tcgen05.ld
+// (warp w reads TMEM lanes 32*(w%4)..+31 = its 32 rows, two warps per lane
+// quadrant splitting the column chunks) and run the epilogue,
 // so the epilogue of tile i overlaps the main loop of tile i+1.  One CTA per
 // SM walks the tile list with stride gridDim.x; tiles are ordered N-fastest so
 // CTAs running together share the same A rows through L2.
@@ -20,6 +21,11 @@
 #include "tmap.h"
 
 namespace dit {
+
+// Warps 2 .. 2+EPI_WARPS-1 drain the accumulator; two per TMEM lane quadrant,
+// each taking every other 32-column chunk of the tile.
+constexpr int EPI_WARPS = 8;
+constexpr int GEMM_THREADS = 32 * (2 + EPI_WARPS);
 
 template <int BN>
 struct TcGemmCfg {
@@ -35,7 +41,7 @@ struct TcGemmCfg {
 };
 
 template <int BN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int64_t M,
                    int N, int K, EpiParams ep, int* err) {
   using C = TcGemmCfg<BN>;
@@ -57,7 +63,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], EPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -152,6 +158,7 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ------------------------------------------------ epilogue warps
     const int q = warp & 3;
+    const int half = (warp - 2) / 4;
     const int row_in_tile = q * 32 + lane;
     uint32_t local = 0;
     bool ok = true;
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(192, 1)
       const int mb = tile / n_tiles, nb = tile - mb * n_tiles;
       const int64_t row = (int64_t)mb * C::BM + row_in_tile;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = half; c < BN / 32; c += 2) {
         uint32_t r[32];
         tmem_ld32(tmem_base + acc * BN + c * 32 + ((uint32_t)(q * 32) << 16), r);
         tmem_ld_wait();
@@ -207,7 +214,7 @@ static cudaError_t launch_gemm_tc(const GemmArgs& g, int* err, int num_sms, cuda
   }
   const int64_t tiles = ((g.M + 127) / 128) * ((g.N + BN - 1) / BN);
   const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-  gemm_tc_kernel<BN><<<grid, 192, C::SMEM_BYTES, s>>>(ta, tb, g.M, g.N, g.K, g.epi, err);
+  gemm_tc_kernel<BN><<<grid, GEMM_THREADS, C::SMEM_BYTES, s>>>(ta, tb, g.M, g.N, g.K, g.epi, err);
   return cudaGetLastError();
 }
 
