@@ -58,10 +58,13 @@ DIT_DEV float gelu_tanh(float x) {
   return 0.5f * x * (1.0f + t);
 }
 
-// Apply the epilogue to columns [col0, col0 + NV) of row `row` (row < M).
-// col0 is a multiple of NV; for EPI_HEADS NV divides hd and D.
+// Element-wise part of the epilogue for columns [col0, col0 + NV) of row
+// `row` (row < M): bias, then GELU (EPI_GELU), the gate factor (EPI_RESID:
+// v becomes gate * v, the increment of x) or the rotary embedding of
+// interleaved channel pairs (EPI_HEADS).  col0 is a multiple of NV; for
+// EPI_HEADS NV divides hd and D.
 template <typename ActT, int NV>
-DIT_DEV void epilogue_chunk(const EpiParams& p, int64_t row, int col0, float (&v)[NV]) {
+DIT_DEV void epilogue_values(const EpiParams& p, int64_t row, int col0, float (&v)[NV]) {
   constexpr bool kFast = std::is_same<ActT, __nv_bfloat16>::value;
   const bool full = col0 + NV <= p.N;
   if (p.bias) {
@@ -74,6 +77,49 @@ DIT_DEV void epilogue_chunk(const EpiParams& p, int64_t row, int col0, float (&v
         if (col0 + j < p.N) v[j] += __ldg(p.bias + col0 + j);
     }
   }
+  if (p.kind == EPI_GELU) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) v[j] = gelu_tanh<kFast>(v[j]);
+  } else if (p.kind == EPI_RESID) {
+    if (p.gate) {
+      const float* g = p.gate + (row / p.rows_per_batch) * p.gate_bstride + col0;
+      if (full && (p.gate_bstride % 4 == 0) && (NV % 4 == 0)) {
+#pragma unroll
+        for (int j = 0; j < NV; j += 4) {
+          const float4 gv = __ldg(reinterpret_cast<const float4*>(g + j));
+          v[j + 0] *= gv.x;
+          v[j + 1] *= gv.y;
+          v[j + 2] *= gv.z;
+          v[j + 3] *= gv.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+          if (col0 + j < p.N) v[j] *= __ldg(g + j);
+      }
+    }
+  } else if (p.kind == EPI_HEADS) {
+    const int sec = col0 / p.D;
+    const int c = (col0 - sec * p.D) % p.hd;
+    const int t = (int)(row % p.rows_per_batch);
+    if (p.rope && ((p.rope_mask >> sec) & 1)) {
+      const float2* cs = p.rope + (int64_t)t * (p.hd / 2) + c / 2;
+#pragma unroll
+      for (int j = 0; j < NV; j += 2) {
+        const float2 r = __ldg(cs + j / 2);
+        const float a = v[j], bb = v[j + 1];
+        v[j] = a * r.x - bb * r.y;
+        v[j + 1] = a * r.y + bb * r.x;
+      }
+    }
+  }
+}
+
+// Write the values produced by epilogue_values with plain per-thread stores
+// (EPI_RESID adds them into the fp32 stream x).
+template <typename ActT, int NV>
+DIT_DEV void epilogue_store(const EpiParams& p, int64_t row, int col0, const float (&v)[NV]) {
+  const bool full = col0 + NV <= p.N;
   switch (p.kind) {
     case EPI_F32: {
       float* o = static_cast<float*>(p.out) + row * p.ldo + col0;
@@ -86,9 +132,6 @@ DIT_DEV void epilogue_chunk(const EpiParams& p, int64_t row, int col0, float (&v
       break;
     }
     case EPI_GELU:
-#pragma unroll
-      for (int j = 0; j < NV; ++j) v[j] = gelu_tanh<kFast>(v[j]);
-      [[fallthrough]];
     case EPI_ACT: {
       ActT* o = static_cast<ActT*>(p.out) + row * p.ldo + col0;
       if (full && (p.ldo % 8 == 0)) {
@@ -101,21 +144,19 @@ DIT_DEV void epilogue_chunk(const EpiParams& p, int64_t row, int col0, float (&v
     }
     case EPI_RESID: {
       float* xr = p.x + row * (int64_t)p.N + col0;
-      const float* g = p.gate ? p.gate + (row / p.rows_per_batch) * p.gate_bstride + col0 : nullptr;
       if (full && (p.N % 4 == 0) && (NV % 4 == 0)) {
 #pragma unroll
         for (int j = 0; j < NV; j += 4) {
           float4 xv = *reinterpret_cast<float4*>(xr + j);
-          float4 gv = g ? __ldg(reinterpret_cast<const float4*>(g + j)) : make_float4(1.f, 1.f, 1.f, 1.f);
-          xv.x += gv.x * v[j + 0];
-          xv.y += gv.y * v[j + 1];
-          xv.z += gv.z * v[j + 2];
-          xv.w += gv.w * v[j + 3];
+          xv.x += v[j + 0];
+          xv.y += v[j + 1];
+          xv.z += v[j + 2];
+          xv.w += v[j + 3];
           *reinterpret_cast<float4*>(xr + j) = xv;
         }
       } else {
         for (int j = 0; j < NV; ++j)
-          if (col0 + j < p.N) xr[j] += (g ? g[j] : 1.0f) * v[j];
+          if (col0 + j < p.N) xr[j] += v[j];
       }
       break;
     }
@@ -126,22 +167,18 @@ DIT_DEV void epilogue_chunk(const EpiParams& p, int64_t row, int col0, float (&v
       const int c = cc - h * p.hd;
       const int64_t b = row / p.rows_per_batch;
       const int t = (int)(row - b * p.rows_per_batch);
-      if (p.rope && ((p.rope_mask >> sec) & 1)) {
-        const float2* cs = p.rope + (int64_t)t * (p.hd / 2) + c / 2;
-#pragma unroll
-        for (int j = 0; j < NV; j += 2) {
-          const float2 r = __ldg(cs + j / 2);
-          const float a = v[j], bb = v[j + 1];
-          v[j] = a * r.x - bb * r.y;
-          v[j + 1] = a * r.y + bb * r.x;
-        }
-      }
-      ActT* o = static_cast<ActT*>(p.dst[sec]) +
-                ((b * p.H + h) * (int64_t)p.seq_total + p.tok_off + t) * p.hd + c;
+      ActT* o = static_cast<ActT*>(p.dst[sec]) + ((b * p.H + h) * (int64_t)p.seq_total + p.tok_off + t) * p.hd + c;
       store_chunk<ActT, NV>(o, v);
       break;
     }
   }
+}
+
+// The whole epilogue of NV columns of one row (row < M).
+template <typename ActT, int NV>
+DIT_DEV void epilogue_chunk(const EpiParams& p, int64_t row, int col0, float (&v)[NV]) {
+  epilogue_values<ActT, NV>(p, row, col0, v);
+  epilogue_store<ActT, NV>(p, row, col0, v);
 }
 
 }  // namespace dit

@@ -9,8 +9,16 @@
 // tcgen05.mma (M=128, N=BN, K=16) from one thread into one of two TMEM
 // accumulators; warps 2-9 drain the other accumulator through tcgen05.ld
 // (warp w reads TMEM lanes 32*(w%4)..+31 = its 32 rows, two warps per lane
-// quadrant splitting the column chunks) and run the epilogue,
-// so the epilogue of tile i overlaps the main loop of tile i+1.  One CTA per
+// quadrant taking alternate column units) and run the epilogue, so the
+// epilogue of tile i overlaps the main loop of tile i+1.  Each epilogue warp
+// stages a finished 32-row x 128-byte unit in its own swizzled 4 KB shared
+// buffer and hands it to the TMA unit: a tiled store for bf16/fp32 outputs,
+// a reduce-add into the fp32 stream for the gated residual (the SM never
+// reads x), a 3-D store into [batch*head, token, channel] for the Q/K/V
+// scatter.  Full 128-byte lines leave the SM instead of 16-byte pieces of 32
+// rows per instruction, which keeps the L2 free for the operand stream.  (A
+// head-major unit whose 32 rows cross a batch boundary is stored directly.)
+// One CTA per
 // SM walks the tile list with stride gridDim.x; tiles are ordered N-fastest so
 // CTAs running together share the same A rows through L2.
 //
@@ -36,18 +44,111 @@ struct TcGemmCfg {
   static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static constexpr int STG_BYTES = 32 * 128;  // one epilogue warp's staging unit
+  static constexpr int STG_OFF = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = STG_OFF + EPI_WARPS * STG_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + BAR_BYTES + 1024;
   static constexpr uint32_t IDESC = umma_idesc_bf16(BM, BN, false);
 };
+
+// Output tensor maps of the TMA epilogue: m[0] = output (x for EPI_RESID);
+// EPI_HEADS: m[s] = section s as [B*H][seq_total][hd].
+struct EpiMaps {
+  CUtensorMap m[3];
+};
+
+// Drain one accumulator tile through shared memory and TMA.  UW = columns per
+// 128-byte unit (64 bf16 or 32 fp32).  The warp owns rows row0..row0+31 and
+// units u = half, half+2, ...; it releases the accumulator (tempty) as soon
+// as its last tcgen05.ld has completed.
+template <int BN, int UW>
+DIT_DEV void drain_tile_tma(const EpiParams& ep, const EpiMaps& maps, uint32_t tacc, int64_t row0, int64_t M, int N,
+                            int nb, int half, uint8_t* stg, uint64_t* tempty_bar) {
+  constexpr int NU = BN / UW;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = row0 + lane;
+  // rows past M are computed from row M-1 (never stored) so every table read stays in range
+  const int64_t vrow = row < M ? row : M - 1;
+  if (half >= NU) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tempty_bar);
+    return;
+  }
+#pragma unroll 1
+  for (int u = half; u < NU; u += 2) {
+    float v[UW];
+    {
+      uint32_t r[UW];
+      tmem_ld32(tacc + u * UW, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+      if constexpr (UW == 64) tmem_ld32(tacc + u * UW + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < UW; ++j) v[j] = __uint_as_float(r[j]);
+    }
+    if (u + 2 >= NU) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar);
+    }
+    const int col0 = nb * BN + u * UW;
+    if (col0 >= N || row0 >= M) continue;
+    epilogue_values<__nv_bfloat16, UW>(ep, vrow, col0, v);
+    int64_t b = 0;
+    int t0 = 0;
+    if (ep.kind == EPI_HEADS) {
+      b = row0 / ep.rows_per_batch;
+      t0 = (int)(row0 - b * ep.rows_per_batch);
+      if (t0 + 32 > ep.rows_per_batch || row0 + 32 > M) {
+        // the unit's rows cross a batch boundary: plain stores, one row per lane
+        if (row < M) epilogue_store<__nv_bfloat16, UW>(ep, row, col0, v);
+        continue;
+      }
+    }
+    // the previous unit's TMA read of the staging buffer must be complete
+    if (lane == 0) bulk_wait_read0();
+    __syncwarp();
+    uint8_t* rowp = stg + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint4 w;
+      if constexpr (UW == 64) {
+        w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+        w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+        w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+        w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+      } else {
+        w = make_uint4(__float_as_uint(v[4 * j + 0]), __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                       __float_as_uint(v[4 * j + 3]));
+      }
+      // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
+      *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) = w;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (ep.kind == EPI_RESID) {
+        tma_reduce_add_2d(&maps.m[0], stg, col0, (int)row0);
+      } else if (ep.kind == EPI_HEADS) {
+        const int sec = col0 / ep.D;
+        const int cc = col0 - sec * ep.D;
+        const int h = cc / ep.hd;
+        tma_store_3d(&maps.m[sec], stg, cc - h * ep.hd, ep.tok_off + t0, (int)(b * ep.H + h));
+      } else {
+        tma_store_2d(&maps.m[0], stg, col0, (int)row0);
+      }
+      bulk_commit();
+    }
+  }
+}
 
 template <int BN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int64_t M,
-                   int N, int K, EpiParams ep, int* err) {
+                   int N, int K, EpiParams ep, const __grid_constant__ EpiMaps maps, int* err) {
   using C = TcGemmCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
@@ -160,6 +261,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int q = warp & 3;
     const int half = (warp - 2) / 4;
     const int row_in_tile = q * 32 + lane;
+    uint8_t* stg = smem + C::STG_OFF + (warp - 2) * C::STG_BYTES;
+    const bool fp32_out = ep.kind == EPI_F32 || ep.kind == EPI_RESID;
     uint32_t local = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
@@ -168,11 +271,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const int mb = tile / n_tiles, nb = tile - mb * n_tiles;
+      const uint32_t tacc = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+      if (ep.tma) {
+        const int64_t row0 = (int64_t)mb * C::BM + q * 32;
+        if (fp32_out)
+          drain_tile_tma<BN, 32>(ep, maps, tacc, row0, M, N, nb, half, stg, &tempty[acc]);
+        else
+          drain_tile_tma<BN, 64>(ep, maps, tacc, row0, M, N, nb, half, stg, &tempty[acc]);
+        continue;
+      }
       const int64_t row = (int64_t)mb * C::BM + row_in_tile;
 #pragma unroll 1
       for (int c = half; c < BN / 32; c += 2) {
         uint32_t r[32];
-        tmem_ld32(tmem_base + acc * BN + c * 32 + ((uint32_t)(q * 32) << 16), r);
+        tmem_ld32(tacc + c * 32, r);
         tmem_ld_wait();
         const int col0 = nb * BN + c * 32;
         if (row < M && col0 < N) {
@@ -186,6 +298,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
     }
+    // every TMA store of this warp has read its staging buffer and landed
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -193,6 +308,48 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Tensor maps for the TMA epilogue; false leaves the epilogue on plain stores
+// (unaligned output, row stride not a multiple of 16 bytes, head_dim not a
+// multiple of 64, or the driver rejecting a map).
+static bool make_epi_maps(const EpiParams& e, int64_t M, int N, EpiMaps* maps) {
+  switch (e.kind) {
+    case EPI_F32: {
+      if (!aligned16(e.out) || e.ldo % 4 || e.ldo < N) return false;
+      const uint64_t d[2] = {(uint64_t)N, (uint64_t)M}, st[1] = {(uint64_t)e.ldo * 4};
+      const uint32_t box[2] = {32, 32};
+      return make_tmap(&maps->m[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, e.out, 2, d, st, box);
+    }
+    case EPI_ACT:
+    case EPI_GELU: {
+      if (!aligned16(e.out) || e.ldo % 8 || e.ldo < N) return false;
+      const uint64_t d[2] = {(uint64_t)N, (uint64_t)M}, st[1] = {(uint64_t)e.ldo * 2};
+      const uint32_t box[2] = {64, 32};
+      return make_tmap_bf16(&maps->m[0], e.out, 2, d, st, box);
+    }
+    case EPI_RESID: {
+      if (!aligned16(e.x) || N % 4) return false;
+      const uint64_t d[2] = {(uint64_t)N, (uint64_t)M}, st[1] = {(uint64_t)N * 4};
+      const uint32_t box[2] = {32, 32};
+      return make_tmap(&maps->m[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, e.x, 2, d, st, box);
+    }
+    case EPI_HEADS: {
+      if (e.hd % 64 || e.rows_per_batch <= 0 || M % e.rows_per_batch) return false;
+      const int64_t BH = (M / e.rows_per_batch) * e.H;
+      const uint64_t d[3] = {(uint64_t)e.hd, (uint64_t)e.seq_total, (uint64_t)BH};
+      const uint64_t st[2] = {(uint64_t)e.hd * 2, (uint64_t)e.seq_total * e.hd * 2};
+      const uint32_t box[3] = {64, 32, 1};
+      for (int sec = 0; sec < 3; ++sec) {
+        if (!e.dst[sec]) continue;
+        if (!aligned16(e.dst[sec]) || !make_tmap_bf16(&maps->m[sec], e.dst[sec], 3, d, st, box)) return false;
+      }
+      return true;
+    }
+  }
+  return false;
 }
 
 template <int BN>
@@ -205,6 +362,9 @@ static cudaError_t launch_gemm_tc(const GemmArgs& g, int* err, int num_sms, cuda
   const uint32_t bb[2] = {64, (uint32_t)BN};
   if (!make_tmap_bf16(&ta, g.A, 2, da, sa, ba) || !make_tmap_bf16(&tb, g.W, 2, db, sb, bb))
     return cudaErrorInvalidValue;
+  EpiParams ep = g.epi;
+  EpiMaps maps;
+  ep.tma = make_epi_maps(ep, g.M, g.N, &maps) ? 1 : 0;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
@@ -214,7 +374,7 @@ static cudaError_t launch_gemm_tc(const GemmArgs& g, int* err, int num_sms, cuda
   }
   const int64_t tiles = ((g.M + 127) / 128) * ((g.N + BN - 1) / BN);
   const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-  gemm_tc_kernel<BN><<<grid, GEMM_THREADS, C::SMEM_BYTES, s>>>(ta, tb, g.M, g.N, g.K, g.epi, err);
+  gemm_tc_kernel<BN><<<grid, GEMM_THREADS, C::SMEM_BYTES, s>>>(ta, tb, g.M, g.N, g.K, ep, maps, err);
   return cudaGetLastError();
 }
 

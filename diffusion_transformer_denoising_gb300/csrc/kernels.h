@@ -32,6 +32,9 @@ struct EpiParams {
   void* dst[3] = {nullptr, nullptr, nullptr};
   int D = 0, hd = 0, H = 0, seq_total = 0, tok_off = 0, rope_mask = 0;
   const float2* rope = nullptr;  // [rows_per_batch][hd / 2] (cos, sin)
+  // set by the tensor-core GEMM launcher when its output tensor maps are valid
+  // (the epilogue then stores through shared memory with TMA)
+  int tma = 0;
 };
 
 struct GemmArgs {
