@@ -1,35 +1,40 @@
 // Bidirectional multi-head attention (no mask), head_dim 128, bf16 in/out,
 // fp32 softmax and accumulation, on the 5th-generation tensor cores.
 //
-// One CTA = 128 query rows of one (batch, head).  Each row's 128 key columns
-// per step are split into two halves, each with its own online-softmax state
-// (running max m_h, sum l_h) and its own output accumulator O_h; the halves
-// are merged once at the end:
-//     O = (2^(m_0-M) O_0 + 2^(m_1-M) O_1) / (2^(m_0-M) l_0 + 2^(m_1-M) l_1).
-// Warps 0-3 run the softmax of key half 0 and warps 4-7 that of half 1 (warp
-// w reads TMEM lane quadrant w%4, i.e. 32 query rows), so no warp ever waits
-// for another inside the loop.  Warp 8 streams K and V tiles of 128 keys
-// with TMA through two 3-stage rings; warp 9 issues the MMAs from one thread,
-// one uninterrupted burst "PV_j, S_{j+2}" per key tile after two waits:
-//     S_j = Q K_j^T                 (SS, K-major operands in shared memory)
-//     O_h += P_j[:, half h] V_j[half h]   (TS: P from tensor memory, V N-major)
-// Tensor memory (512 columns): S double buffer [0,128) [128,256); O_0 at
-// [256,384); O_1 at [384,512).  P_j (packed bf16 pairs) overwrites the first
-// 64 columns of its S slot once the softmax has read them.  tcgen05.mma
-// operations of a CTA execute in issue order, so PV_j has read P_j before
-// S_{j+2} overwrites the slot.
-// Every tcgen05.commit costs the tensor pipe a few hundred cycles, so there
-// is exactly one per key tile: after "PV_j, S_{j+2}" the MMA thread commits
-// to done[(j+2) % 3].  Completion i of that ring (i = 0, 1 for S_0, S_1;
-// i = j+2 for PV_j together with S_{j+2}) tells the softmax that S_i is in
-// TMEM, the producer that K_{i} and V_{i-2} stages are free, and a lazy O
-// rescale that PV_{i-2} has landed.  Each waiter takes the completions of a
-// barrier in order, and completion i+3 cannot happen before K_{i+3} is
-// loaded, so a parity wait never aliases.  O is rescaled lazily (only when a
-// max grows by more than 2^8).
+// One CTA = 128 query rows of one (batch, head), walking the keys in tiles of
+// 128.  Per key tile j:
+//     S_j = Q K_j^T            (8 tcgen05.mma, A and B from shared memory)
+//     P_j = 2^(S_j*c - m)      (softmax warps, bf16, written to tensor memory)
+//     O  += P_j V_j            (8 tcgen05.mma, A = P_j from tensor memory)
+// with the online-softmax running row max m and row sum l (c = log2(e)/sqrt(d)).
 //
-// All waits are bounded (common.cuh); on a timeout the CTA flags *err, waits
-// for its own copies and MMAs, frees TMEM and exits.
+// The tensor pipe idles whenever its issuing thread stops issuing (a wait, a
+// fence, a commit all leave a gap), and a single chain of MMAs into one
+// accumulator does not keep it full.  So two threads issue: one warp the S
+// products, another the PV products.  Each waits only for its own inputs, and
+// while one waits the other's MMAs keep the pipe busy.  This needs S_{j+2}
+// and PV_j to be independent, so P has its own tensor-memory slots:
+//     S slots [0,128) [128,256)   P slots [256,320) [320,384)   O [384,512)
+// S_{j+2} is issued into slot j%2 as soon as the softmax has copied S_j into
+// registers; P_j goes to P slot j%2 once PV_{j-2} has consumed P_{j-2}.
+//
+// Softmax: SM_WARPS warps.  Warp w reads TMEM lane quadrant q = w%4 (query
+// rows 32q..32q+31) and key columns [h*KPW, (h+1)*KPW) of every tile,
+// h = w/4.  The NQ warps of a quadrant share one O, so they agree on each
+// row's reference max: each publishes its partial max (rounded to bf16: any
+// common reference is exact, it only has to be the same for all of them) in
+// shared memory and they meet at a named barrier.  O and l are rescaled only
+// when the max grows by more than 2^8 (the warps decide identically).
+//
+// Warp SM_WARPS streams K and V with TMA through two 3-stage rings (K_j is loaded
+// once S_{j-3} has completed, V_j once PV_{j-3} has).  Completions are
+// signalled by one tcgen05.commit per MMA group to rings s_done[3] /
+// pv_done[3]; every waiter's next completion on a barrier needs an action of
+// its own first, so a parity wait never aliases.
+//
+// All waits are bounded (common.cuh); on a timeout the CTA flags *err, keeps
+// the softmax warps' named barriers matched, waits for its own copies and
+// MMAs, frees tensor memory and exits.
 #include "epilogue.cuh"
 #include "tmap.h"
 
@@ -42,14 +47,21 @@ constexpr int Q_OFF = 0;
 constexpr int K_OFF = Q_OFF + TILE_BYTES;
 constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
 constexpr int BAR_OFF = V_OFF + VST * TILE_BYTES;
-constexpr int XCH_OFF = BAR_OFF + 256;     // float[4][128]: m_0, m_1, l_0, l_1 per row
+constexpr int XCH_OFF = BAR_OFF + 256;     // bf16[2 parities][NQ][128 rows]; float[NQ][128] at the end
 // The tiles need 1024-byte alignment.  The dynamic shared window of a kernel
 // without static shared memory starts 1024-aligned (checked at entry), so no
 // alignment slack is reserved and the total stays under 227 KB.
-constexpr int SMEM_BYTES = XCH_OFF + 4 * BQ * 4;
-constexpr int NUM_THREADS = 320;           // 8 softmax warps, TMA warp, MMA warp
-constexpr int TMA_WARP = 8, MMA_WARP = 9;
-constexpr uint32_t TM_S = 0, TM_O = 256;
+constexpr int SMEM_BYTES = XCH_OFF + 2 * 4 * BQ * 2;  // sized for NQ <= 4
+#ifndef DIT_ATTN_SOFTMAX_WARPS
+#define DIT_ATTN_SOFTMAX_WARPS 8
+#endif
+constexpr int SM_WARPS = DIT_ATTN_SOFTMAX_WARPS;  // softmax warps: 8 or 16
+constexpr int NQ = SM_WARPS / 4;                  // warps per TMEM lane quadrant
+constexpr int KPW = BKV / NQ;                     // key columns per softmax warp
+static_assert(KPW == 32 || KPW == 64, "softmax warps must be 8 or 16");
+constexpr int NUM_THREADS = 32 * (SM_WARPS + 3);  // + TMA warp, S-MMA warp, PV-MMA warp
+constexpr int TMA_WARP = SM_WARPS, S_WARP = SM_WARPS + 1, PV_WARP = SM_WARPS + 2;
+constexpr uint32_t TM_S = 0, TM_P = 256, TM_O = 384;
 constexpr uint32_t IDESC_S = umma_idesc_bf16(128, 128, false);
 constexpr uint32_t IDESC_O = umma_idesc_bf16(128, 128, true);
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
@@ -65,15 +77,18 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
-  uint64_t* q_full = bars;        // Q, K_0 and K_1
-  uint64_t* xf = bars + 1;        // [3] tile pair j: V_j and K_{j+2} (see the producer)
-  uint64_t* done = bars + 7;      // [3] MMA completion ring (see above)
-  uint64_t* p_ready = bars + 10;  // [2] per S slot
-  uint64_t* drain = bars + 12;
-  uint64_t* fin = bars + 13;      // [4] per lane quadrant
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+  uint64_t* q_full = bars;         // Q tile
+  uint64_t* kf = bars + 1;         // [3] K stage loaded
+  uint64_t* vf = bars + 4;         // [3] V stage loaded
+  uint64_t* s_done = bars + 7;     // [3] S_j complete (ring by j % 3)
+  uint64_t* pv_done = bars + 10;   // [3] PV_j complete (ring by j % 3)
+  uint64_t* s_free = bars + 13;    // [2] softmax has copied S slot j % 2 (one arrival per softmax warp)
+  uint64_t* p_ready = bars + 15;   // [2] P slot j % 2 written (one arrival per softmax warp)
+  uint64_t* drain = bars + 17;     // [2] final commit of each MMA thread
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* xch = reinterpret_cast<float*>(smem + XCH_OFF);
+  __nv_bfloat16* xmax = reinterpret_cast<__nv_bfloat16*>(smem + XCH_OFF);
+  float* xsum = reinterpret_cast<float*>(smem + XCH_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.z * a.H + blockIdx.y;
@@ -86,12 +101,16 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < 3; ++s) {
-      mbar_init(&xf[s], 1);
-      mbar_init(&done[s], 1);
+      mbar_init(&kf[s], 1);
+      mbar_init(&vf[s], 1);
+      mbar_init(&s_done[s], 1);
+      mbar_init(&pv_done[s], 1);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&p_ready[b], 8);
-    mbar_init(drain, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&fin[i], 2);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_free[b], SM_WARPS);
+      mbar_init(&p_ready[b], SM_WARPS);
+      mbar_init(&drain[b], 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -100,7 +119,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (warp == MMA_WARP) tmem_alloc(tmem_slot, 512);
+  if (warp == S_WARP) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -108,54 +127,52 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
 
   if (warp == TMA_WARP) {
     // ------------------------------------------------ TMA producer (one thread)
-    // Loads are grouped so that the MMA thread waits once per key tile: barrier
-    // xf[j % 3] covers V_j and K_{j+2}, exactly what "PV_j, S_{j+2}" reads.  Both
-    // stages are free once completion j-1 (PV_{j-3}, S_{j-1}) has landed.
     if (lane == 0) {
-      int issued[3] = {0, 0, 0};
+      int issued_k[3] = {0, 0, 0}, issued_v[3] = {0, 0, 0};
       bool ok = true;
       auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int tile) {
         const int jt = (tile + kv_rot) % nkv;
+        mbar_arrive_expect_tx(bar, TILE_BYTES);
         tma_load_3d(dst, tm, bar, 0, jt * BKV, bh);
         tma_load_3d(dst + TILE_BYTES / 2, tm, bar, 64, jt * BKV, bh);
       };
-      mbar_arrive_expect_tx(q_full, (nkv > 1 ? 3 : 2) * TILE_BYTES);
+      mbar_arrive_expect_tx(q_full, TILE_BYTES);
       tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, q0, bh);
       tma_load_3d(smem + Q_OFF + TILE_BYTES / 2, &tmQ, q_full, 64, q0, bh);
-      load_tile(&tmK, smem + K_OFF, q_full, 0);
-      if (nkv > 1) load_tile(&tmK, smem + K_OFF + TILE_BYTES, q_full, 1);
       for (int j = 0; j < nkv; ++j) {
-        if (j >= 1) ok = mbar_wait(&done[(j - 1) % 3], (uint32_t)(((j - 1) / 3) & 1), abort_flag, err, 21);
+        // K stage j%3 was last read by S_{j-3}, V stage j%3 by PV_{j-3}
+        if (j >= 3) ok = mbar_wait(&s_done[j % 3], (uint32_t)(((j - 3) / 3) & 1), abort_flag, err, 21);
         if (!ok) break;
-        const bool has_k = j + 2 < nkv;
-        mbar_arrive_expect_tx(&xf[j % 3], (has_k ? 2 : 1) * TILE_BYTES);
-        load_tile(&tmV, smem + V_OFF + (j % VST) * TILE_BYTES, &xf[j % 3], j);
-        if (has_k) load_tile(&tmK, smem + K_OFF + ((j + 2) % KST) * TILE_BYTES, &xf[j % 3], j + 2);
-        ++issued[j % 3];
+        load_tile(&tmK, smem + K_OFF + (j % KST) * TILE_BYTES, &kf[j % 3], j);
+        ++issued_k[j % 3];
+        if (j >= 3) ok = mbar_wait(&pv_done[j % 3], (uint32_t)(((j - 3) / 3) & 1), abort_flag, err, 22);
+        if (!ok) break;
+        load_tile(&tmV, smem + V_OFF + (j % VST) * TILE_BYTES, &vf[j % 3], j);
+        ++issued_v[j % 3];
       }
       if (!ok) {
         // wind down: every copy this thread started lands before the CTA exits
         volatile int no_abort = 0;
         mbar_wait(q_full, 0, &no_abort, nullptr, 0);
-        for (int s = 0; s < 3; ++s)
-          if (issued[s] > 0) mbar_wait(&xf[s], (uint32_t)((issued[s] - 1) & 1), &no_abort, nullptr, 0);
+        for (int s = 0; s < 3; ++s) {
+          if (issued_k[s] > 0) mbar_wait(&kf[s], (uint32_t)((issued_k[s] - 1) & 1), &no_abort, nullptr, 0);
+          if (issued_v[s] > 0) mbar_wait(&vf[s], (uint32_t)((issued_v[s] - 1) & 1), &no_abort, nullptr, 0);
+        }
       }
     }
     __syncwarp();
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------ MMA issuer (one thread)
-    // The whole role runs on lane 0: a warp that diverges and reconverges
-    // around every MMA burst costs the tensor pipe a large share of its rate.
+  } else if (warp == S_WARP) {
+    // ------------------------------------------------ S = Q K^T issuer (one thread)
     if (lane == 0) {
-      auto wait1 = [&](uint64_t* bar, uint32_t parity, int site) -> bool {
-        return mbar_wait(bar, parity, abort_flag, err, site);
-      };
-      // base descriptors, built once; per MMA only a constant is added
       const uint64_t q_desc = umma_desc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
       const uint64_t k_desc = umma_desc_sw128(smem_u32(smem + K_OFF), 16, 1024);
-      const uint64_t v_desc = umma_desc_sw128(smem_u32(smem + V_OFF), 16384, 1024);
-      // S_j = Q K_j^T into S slot j % 2 (no commit here); K_j is resident
-      auto issue_s = [&](int j) {
+      bool ok = mbar_wait(q_full, 0, abort_flag, err, 23);
+      for (int j = 0; ok && j < nkv; ++j) {
+        // slot j%2 is free once the softmax has copied S_{j-2}
+        if (j >= 2) ok = mbar_wait(&s_free[j & 1], (uint32_t)(((j - 2) >> 1) & 1), abort_flag, err, 24);
+        ok = ok && mbar_wait(&kf[j % 3], (uint32_t)((j / 3) & 1), abort_flag, err, 25);
+        if (!ok) break;
+        tc_fence_after();
         const uint64_t kd = umma_desc_add(k_desc, (j % KST) * TILE_BYTES);
         const uint32_t d_tmem = tmem + TM_S + (j & 1) * 128;
 #pragma unroll
@@ -163,96 +180,110 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
           const uint32_t off = (kk >> 2) * (TILE_BYTES / 2) + (kk & 3) * 32;
           umma_ss(d_tmem, umma_desc_add(q_desc, off), umma_desc_add(kd, off), IDESC_S, kk != 0);
         }
-      };
-      bool ok = wait1(q_full, 0, 24);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        umma_commit(&done[0]);  // completion 0: S_0
-        if (nkv > 1) {
-          issue_s(1);
-          umma_commit(&done[1]);  // completion 1: S_1
-        }
+        umma_commit(&s_done[j % 3]);
       }
-      // One uninterrupted burst per key tile: the issuing thread does nothing
-      // between MMAs (any wait or detour there idles the tensor pipe).
+      // all MMAs issued by this thread complete before tensor memory is released
+      umma_commit(&drain[0]);
+      volatile int no_abort = 0;
+      mbar_wait(&drain[0], 0, &no_abort, nullptr, 0);
+    }
+    __syncwarp();
+  } else if (warp == PV_WARP) {
+    // ------------------------------------------------ O += P V issuer (one thread)
+    if (lane == 0) {
+      const uint64_t v_desc = umma_desc_sw128(smem_u32(smem + V_OFF), 16384, 1024);
+      bool ok = true;
       for (int j = 0; ok && j < nkv; ++j) {
-        ok = wait1(&p_ready[j & 1], (uint32_t)((j >> 1) & 1), 25) &&
-             wait1(&xf[j % 3], (uint32_t)((j / 3) & 1), 26);
+        ok = mbar_wait(&p_ready[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, err, 26) &&
+             mbar_wait(&vf[j % 3], (uint32_t)((j / 3) & 1), abort_flag, err, 27);
         if (!ok) break;
         tc_fence_after();
         const uint64_t vd = umma_desc_add(v_desc, (j % VST) * TILE_BYTES);
-        const uint32_t p_tmem = tmem + TM_S + (j & 1) * 128;
+        const uint32_t p_tmem = tmem + TM_P + (j & 1) * 64;
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // keys 64h+16kk.. of V (8-row groups 1 KB apart; channel halves 16 KB apart)
-            umma_ts(tmem + TM_O + h * 128, p_tmem + h * 32 + kk * 8, umma_desc_add(vd, (4 * h + kk) * 2048),
-                    IDESC_O, (j | kk) != 0);
-          }
-        if (j + 2 < nkv) issue_s(j + 2);
-        umma_commit(&done[(j + 2) % 3]);  // completion j+2: PV_j (+ S_{j+2})
+        for (int kk = 0; kk < BKV / 16; ++kk) {
+          // keys 16kk..16kk+15: P columns 8kk.. (bf16 pairs), V rows 16kk.. (8-row groups 1 KB apart)
+          umma_ts(tmem + TM_O, p_tmem + kk * 8, umma_desc_add(vd, kk * 2048), IDESC_O, (j | kk) != 0);
+        }
+        umma_commit(&pv_done[j % 3]);
       }
-      umma_commit(drain);
+      umma_commit(&drain[1]);
       volatile int no_abort = 0;
-      mbar_wait(drain, 0, &no_abort, nullptr, 0);
+      mbar_wait(&drain[1], 0, &no_abort, nullptr, 0);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------ softmax warps 0-7
+    // ------------------------------------------------ softmax warps
     const int q = warp & 3, h = warp >> 2;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    const uint32_t o_col = tmem + TM_O + h * 128 + lane_off;
+    const uint32_t o_col = tmem + TM_O + h * KPW + lane_off;  // this warp's O (and output) channels
     const int row = q * 32 + lane;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    // The loop never breaks: after a failed wait the warp skips the work but
+    // still meets its quadrant partners at every named barrier.
     for (int j = 0; j < nkv; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&done[j % 3], (uint32_t)((j / 3) & 1), abort_flag, err, 31));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t s_col = tmem + TM_S + (j & 1) * 128 + lane_off;
-      float s[64];
-      {
-        uint32_t r[64];
-        tmem_ld32(s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-        tmem_ld32(s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-        tmem_ld_wait();
+      float s[KPW];
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&s_done[j % 3], (uint32_t)((j / 3) & 1), abort_flag, err, 31));
+      if (ok) {
+        tc_fence_after();
+        {
+          uint32_t r[KPW];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i]);
+          for (int c = 0; c < KPW / 32; ++c)
+            tmem_ld32(tmem + TM_S + (j & 1) * 128 + h * KPW + c * 32 + lane_off,
+                      *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < KPW; ++i) s[i] = __uint_as_float(r[i]);
+        }
+        // S slot j%2 may now take S_{j+2}
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[j & 1]);
+        const int valid = a.Lk - ((j + kv_rot) % nkv) * BKV - h * KPW;
+        if (valid < KPW) {
+#pragma unroll
+          for (int i = 0; i < KPW; ++i)
+            if (i >= valid) s[i] = -INFINITY;
+        }
+        // partial row max: four independent chains of three-input max
+        float m4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+        for (int i = 4; i + 8 <= KPW - 4; i += 8)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], s[i + 2 * k], s[i + 2 * k + 1]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m4[k] = fmaxf(m4[k], s[KPW - 4 + k]);
+        xmax[((j & 1) * NQ + h) * BQ + row] =
+            __float2bfloat16_rn(fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]) * scale_log2);
       }
-      const int valid = a.Lk - ((j + kv_rot) % nkv) * BKV - h * 64;
-      if (valid < 64) {
+      named_bar_sync(1 + q, 32 * NQ);
+      if (!ok) continue;
+      // the row max of the tile over the quadrant's warps (every tile has a valid key)
+      const __nv_bfloat16* xm = xmax + (j & 1) * NQ * BQ + row;
+      float m_tile = __bfloat162float(xm[0]);
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (i >= valid) s[i] = -INFINITY;
-      }
-      // row max: four independent chains of three-input max over s[4..59], then s[60..63]
-      float m4[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-      for (int i = 4; i + 8 <= 60; i += 8)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], s[i + 2 * k], s[i + 2 * k + 1]);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) m4[k] = fmaxf(m4[k], s[60 + k]);
-      const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-      const float m_new = fmaxf(m_used, mx * scale_log2);
-      float alpha = 1.f;
+      for (int w = 1; w < NQ; ++w) m_tile = fmaxf(m_tile, __bfloat162float(xm[w * BQ]));
+      const float m_new = fmaxf(m_used, m_tile);
       if (j == 0) {
         m_used = m_new;
       } else {
         const bool need = m_new - m_used > RESCALE_THRESHOLD;
         if (__any_sync(0xffffffffu, need)) {
-          // O_h must hold PV_{j-1} (completion j+1) before it is rescaled
-          ok = __all_sync(0xffffffffu, mbar_wait(&done[(j + 1) % 3], (uint32_t)(((j + 1) / 3) & 1), abort_flag, err, 32));
-          if (!ok) break;
+          // O must hold PV_{j-1} before it is rescaled
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&pv_done[(j - 1) % 3], (uint32_t)(((j - 1) / 3) & 1), abort_flag, err, 32));
+          if (!ok) continue;
           tc_fence_after();
+          float alpha = 1.f;
           if (need) {
             alpha = ex2_approx(m_used - m_new);
             m_used = m_new;
+            l *= alpha;
           }
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
+          for (int c = 0; c < KPW / 32; ++c) {
             uint32_t r[32];
             tmem_ld32(o_col + c * 32, r);
             tmem_ld_wait();
@@ -262,45 +293,49 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
           }
         }
       }
-      // a half that has seen no valid key yet keeps m = -inf and p = 0
-      const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-mref, -mref);
+      const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m_used, -m_used);
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      uint32_t pk[32];
+      uint32_t pk[KPW / 2];
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
+      for (int i = 0; i < KPW; i += 2) {
         const float2 x = ffma2(make_float2(s[i], s[i + 1]), sc2, nm2);
         const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
         acc[(i >> 1) & 3] = fadd2(acc[(i >> 1) & 3], p);
         pk[i / 2] = pack_bf16x2(p.x, p.y);
       }
       const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
-      l = l * alpha + ((a01.x + a01.y) + (a23.x + a23.y));
-      tmem_st32(s_col + h * 32, pk);
+      l += (a01.x + a01.y) + (a23.x + a23.y);
+      // P slot j%2 held P_{j-2}: PV_{j-2} must have read it
+      if (j >= 2) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&pv_done[(j - 2) % 3], (uint32_t)(((j - 2) / 3) & 1), abort_flag, err, 33));
+        if (!ok) continue;
+        tc_fence_after();
+      }
+      const uint32_t p_col = tmem + TM_P + (j & 1) * 64 + h * (KPW / 2) + lane_off;
+      if constexpr (KPW == 64)
+        tmem_st32(p_col, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+      else
+        tmem_st16(p_col, *reinterpret_cast<const uint32_t(*)[16]>(pk));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_ready[j & 1]);
     }
-    if (ok) {
-      // PV_{nkv-1} is completion nkv+1
-      ok = __all_sync(0xffffffffu, mbar_wait(&done[(nkv + 1) % 3], (uint32_t)(((nkv + 1) / 3) & 1), abort_flag, err, 33));
-    }
-    if (ok) {
-      // merge the two halves: swap (m, l) with the partner warp of the quadrant
-      xch[h * BQ + row] = m_used;
-      xch[(2 + h) * BQ + row] = l;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&fin[q]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&fin[q], 0, abort_flag, err, 34));
-    }
+    // O is final once PV_{nkv-1} has completed
+    ok = ok && __all_sync(0xffffffffu,
+                          mbar_wait(&pv_done[(nkv - 1) % 3], (uint32_t)(((nkv - 1) / 3) & 1), abort_flag, err, 34));
+    // the quadrant's partial row sums (same reference max) go through the
+    // exchange buffer once every warp of the quadrant has read its maxima
+    named_bar_sync(1 + q, 32 * NQ);
+    xsum[h * BQ + row] = l;
+    named_bar_sync(1 + q, 32 * NQ);
     if (ok) {
       tc_fence_after();
-      const float m_o = xch[(1 - h) * BQ + row], l_o = xch[(3 - h) * BQ + row];
-      const float M = fmaxf(m_used, m_o);
-      const float a_s = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - M);
-      const float a_o = (m_o == -INFINITY) ? 0.f : ex2_approx(m_o - M);
-      const float inv = 1.f / (l * a_s + l_o * a_o);
+      float lt = 0.f;
+#pragma unroll
+      for (int w = 0; w < NQ; ++w) lt += xsum[w * BQ + row];
+      const float inv = 1.f / lt;
       const int tok = q0 + row;
       const int D = a.H * HD;
       __nv_bfloat16* out = nullptr;
@@ -309,22 +344,17 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
                   ? static_cast<__nv_bfloat16*>(a.o1) + ((int64_t)blockIdx.z * a.split + tok) * D
                   : static_cast<__nv_bfloat16*>(a.o2) +
                         ((int64_t)blockIdx.z * (a.Lq - a.split) + (tok - a.split)) * D;
-        out += blockIdx.y * HD + h * 64;
+        out += blockIdx.y * HD + h * KPW;
       }
-      // this warp writes channels [64h, 64h+64) from both accumulators
-      const uint32_t self_col = tmem + TM_O + h * 128 + h * 64 + lane_off;
-      const uint32_t oth_col = tmem + TM_O + (1 - h) * 128 + h * 64 + lane_off;
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t r1[32], r2[32];
-        tmem_ld32(self_col + c * 32, r1);
-        tmem_ld32(oth_col + c * 32, r2);
+      for (int c = 0; c < KPW / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(o_col + c * 32, r);
         tmem_ld_wait();
         if (out) {
           float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            v[i] = (__uint_as_float(r1[i]) * a_s + __uint_as_float(r2[i]) * a_o) * inv;
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * inv;
           store_chunk<__nv_bfloat16, 32>(out + c * 32, v);
         }
       }
@@ -332,7 +362,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == MMA_WARP) {
+  if (warp == S_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

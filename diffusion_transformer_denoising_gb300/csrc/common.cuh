@@ -100,8 +100,11 @@ DIT_DEV uint64_t globaltimer_ns() {
 // Bounded wait on an mbarrier phase.  `abort_flag` (shared) short-cuts every
 // later wait of the CTA once one wait has given up; `err` (global) records
 // the failure for the host.  Returns false when the wait was abandoned.
-DIT_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The polling loop lives out of line: a phase that has already completed
+// then costs one try_wait and a branch, which matters on the tensor-core
+// issue paths where every cycle between MMAs idles the pipe.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                   int* err, int site) {
   uint64_t t0 = globaltimer_ns();
   uint32_t it = 0;
   while (true) {
@@ -113,6 +116,15 @@ DIT_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
       return false;
     }
   }
+}
+DIT_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err, int site) {
+  if (__builtin_expect(mbar_try_wait(bar, parity), 1)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err, site);
+}
+
+// Barrier over `nthreads` threads (whole warps) of the CTA; id 0 is __syncthreads.
+DIT_DEV void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA
@@ -250,6 +262,15 @@ DIT_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
       "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns from registers.
+DIT_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 DIT_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }

@@ -42,10 +42,29 @@ def cosine(a, b):
     return float(a @ b / np.sqrt((a @ a) * (b @ b)))
 
 
-# tolerances (fp32-accumulate test precision / bf16 production precision)
+def rel_rms_err(got, ref):
+    """RMS(got - ref) / RMS(ref)."""
+    ref = np.asarray(ref, np.float64)
+    d = np.asarray(got, np.float64) - ref
+    return float(np.sqrt(np.mean(d ** 2)) / np.sqrt(np.mean(ref ** 2)))
+
+
+# tolerances (fp32-accumulate test precision / bf16 production precision).
+# fp32 test mode: max abs error <= 1e-4 of the output RMS.  bf16 production
+# mode: the per-block output error, taken as the RMS of the error, <= 2e-2 of
+# the output RMS; single elements are also held to TOL_BF16_MAX so that an
+# isolated wrong value still fails (bf16 rounding of the activations alone
+# puts the largest element error near 1e-2 of the RMS on 3072-wide blocks).
 TOL_F32 = 1e-4
 TOL_BF16_BLOCK = 2e-2
+TOL_BF16_MAX = 5e-2
 COS_BF16_LOOP = 0.999
+
+
+def assert_block_close(got, ref, scale=1.0):
+    """bf16 per-block criterion (RMS error and element bound), both scaled by `scale`."""
+    rms, mx = rel_rms_err(got, ref), rel_max_err(got, ref)
+    assert rms < scale * TOL_BF16_BLOCK and mx < scale * TOL_BF16_MAX, (rms, mx)
 
 
 def small_bf16_cfg(mode=synth.COND_CROSS, **kw):

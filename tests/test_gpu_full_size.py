@@ -7,7 +7,7 @@ import pytest
 
 from diffusion_transformer_denoising_gb300 import synth
 from oracle import dit_oracle as O
-from tests.gpu_util import COS_BF16_LOOP, TOL_BF16_BLOCK, cosine, dev, empty, host, make_model, rel_max_err
+from tests.gpu_util import COS_BF16_LOOP, assert_block_close, cosine, dev, empty, host, make_model, rel_max_err
 
 pytestmark = pytest.mark.gpu
 
@@ -46,8 +46,8 @@ def test_video_block_full_size(video_block):
     angles = O.rope_angles(O.token_positions(grid), cfg["rope_axes"], cfg["rope_theta"])
     for b in range(2):
         ref = O.block_cross(x0[b], mods[b], ctx[b], W, 0, cfg, grid, rows=rows, angles=angles)
-        assert rel_max_err(got[b][rows], ref) < TOL_BF16_BLOCK
-        assert rel_max_err(got[b][rows] - x0[b][rows], ref - x0[b][rows]) < 5 * TOL_BF16_BLOCK
+        assert_block_close(got[b][rows], ref)
+        assert_block_close(got[b][rows] - x0[b][rows], ref - x0[b][rows], 5)
 
 
 @pytest.fixture(scope="module")
@@ -79,7 +79,7 @@ def test_image_block_full_size(image_model):
     for b in range(2):
         ref = O.block_joint(x0[b], xc0[b], mods[b], W, 1, cfg, grid, rows=rows, angles=angles)
         got = np.concatenate([gc[b], gx[b]])[rows]
-        assert rel_max_err(got, ref) < TOL_BF16_BLOCK
+        assert_block_close(got, ref)
 
 
 def test_image_loop_full_tokens_reduced_depth(image_model):
@@ -124,7 +124,7 @@ def test_video_embed_head_and_cfg_euler_full_size(video_block):
     gv = host(v)
     for b in range(2):
         ref = O.unpatchify(O.final_layer(xs[b], mods[b], W, cfg), cfg["patch"], (cfg["in_channels"],) + thw)
-        assert rel_max_err(gv[b], ref) < TOL_BF16_BLOCK
+        assert_block_close(gv[b], ref)
     from diffusion_transformer_denoising_gb300 import dit
     n = gv[0].size
     out = empty(n)

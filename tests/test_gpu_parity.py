@@ -5,7 +5,7 @@ import pytest
 
 from diffusion_transformer_denoising_gb300 import dit, synth
 from oracle import dit_oracle as O
-from tests.gpu_util import (COS_BF16_LOOP, TOL_BF16_BLOCK, TOL_F32, cosine, dev, empty, host, make_model,
+from tests.gpu_util import (COS_BF16_LOOP, TOL_F32, assert_block_close, cosine, dev, empty, host, make_model,
                             rel_max_err, small_bf16_cfg)
 
 pytestmark = pytest.mark.gpu
@@ -163,7 +163,7 @@ def test_bf16_final_layer(small_cross):
     gv = host(v)
     for b in range(2):
         ref = O.unpatchify(O.final_layer(x[b], mods[b], W, cfg), cfg["patch"], (cfg["in_channels"],) + thw)
-        assert rel_max_err(gv[b], ref) < TOL_BF16_BLOCK
+        assert_block_close(gv[b], ref)
 
 
 @pytest.mark.parametrize("grid,L", [((3, 10, 13), 77), ((1, 16, 16), 128), ((2, 9, 7), 5)])
@@ -180,8 +180,8 @@ def test_bf16_cross_block(small_cross, grid, L):
     got = host(x)
     for b in range(2):
         ref = O.block_cross(x0[b], mods[b], ctx[b], W, 1, cfg, grid)
-        assert rel_max_err(got[b], ref) < TOL_BF16_BLOCK
-        assert rel_max_err(got[b] - x0[b], ref - x0[b]) < 5 * TOL_BF16_BLOCK
+        assert_block_close(got[b], ref)
+        assert_block_close(got[b] - x0[b], ref - x0[b], 5)
 
 
 @pytest.mark.parametrize("grid,L", [((1, 12, 20), 64), ((1, 7, 9), 33)])
@@ -198,8 +198,8 @@ def test_bf16_joint_block(small_joint, grid, L):
     gx, gc = host(x), host(xc)
     for b in range(2):
         rx, rc = O.block_joint(x0[b], xc0[b], mods[b], W, 0, cfg, grid)
-        assert rel_max_err(gx[b], rx) < TOL_BF16_BLOCK
-        assert rel_max_err(gc[b], rc) < TOL_BF16_BLOCK
+        assert_block_close(gx[b], rx)
+        assert_block_close(gc[b], rc)
 
 
 @pytest.mark.parametrize("mode", [synth.COND_CROSS, synth.COND_JOINT])
