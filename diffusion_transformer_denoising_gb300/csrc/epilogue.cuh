@@ -62,7 +62,7 @@ DIT_DEV float gelu_tanh(float x) {
 // `row` (row < M): bias, then GELU (EPI_GELU), the gate factor (EPI_RESID:
 // v becomes gate * v, the increment of x) or the rotary embedding of
 // interleaved channel pairs (EPI_HEADS).  col0 is a multiple of NV; for
-// EPI_HEADS NV divides hd and D.
+// EPI_HEADS NV divides hd and D and is a multiple of 4.
 template <typename ActT, int NV>
 DIT_DEV void epilogue_values(const EpiParams& p, int64_t row, int col0, float (&v)[NV]) {
   constexpr bool kFast = std::is_same<ActT, __nv_bfloat16>::value;
@@ -103,13 +103,16 @@ DIT_DEV void epilogue_values(const EpiParams& p, int64_t row, int col0, float (&
     const int c = (col0 - sec * p.D) % p.hd;
     const int t = (int)(row % p.rows_per_batch);
     if (p.rope && ((p.rope_mask >> sec) & 1)) {
-      const float2* cs = p.rope + (int64_t)t * (p.hd / 2) + c / 2;
+      // two (cos, sin) pairs per 16-byte load: c is a multiple of 4 channels
+      const float4* cs = reinterpret_cast<const float4*>(p.rope + (int64_t)t * (p.hd / 2) + c / 2);
 #pragma unroll
-      for (int j = 0; j < NV; j += 2) {
-        const float2 r = __ldg(cs + j / 2);
-        const float a = v[j], bb = v[j + 1];
-        v[j] = a * r.x - bb * r.y;
-        v[j + 1] = a * r.y + bb * r.x;
+      for (int j = 0; j < NV; j += 4) {
+        const float4 r = __ldg(cs + j / 4);
+        const float a0 = v[j], b0 = v[j + 1], a1 = v[j + 2], b1 = v[j + 3];
+        v[j] = a0 * r.x - b0 * r.y;
+        v[j + 1] = a0 * r.y + b0 * r.x;
+        v[j + 2] = a1 * r.z - b1 * r.w;
+        v[j + 3] = a1 * r.w + b1 * r.z;
       }
     }
   }
