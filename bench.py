@@ -403,6 +403,65 @@ def run_block_case(args):
     print(json.dumps(out), flush=True)
 
 
+SWEEP_POINTS = [(1, 4096), (2, 4096), (4, 4096), (8, 4096), (1, 1024), (1, 16384), (1, 65536)]
+
+
+def run_sweep(args):
+    """Batch/sequence sweep of the image DiT block: a depth-1 image model
+    (hidden 3072, 24x128 heads, MLP 12288) at batch 1/2/4/8 with 4096 image
+    tokens and at 1024/16384/65536 tokens with batch 1, always jointly with
+    512 condition tokens.  Each point times one denoising step (timestep MLP,
+    patch embed, the block on the CFG pair, final layer, guidance + Euler)
+    through dit_denoise_loop, device-timed over --steps calls."""
+    import torch
+    from diffusion_transformer_denoising_gb300 import dit
+    torch.cuda.set_device(0)
+    base = synth.config("image", depth=1)
+    L, C, D = base["cond_len"], base["in_channels"], base["hidden"]
+    _, ph, pw = base["patch"]
+    W = synth.make_weights_torch(base, seed=0, device="cuda")
+    sig = np.array([1.0, 1.0 - 1.0 / base["steps"]])
+    sig = (base["shift"] * sig / (1 + (base["shift"] - 1) * sig)).astype(np.float32)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
+    points = []
+    for batch, ntok in SWEEP_POINTS:
+        side = int(round(ntok ** 0.5))
+        cfg = synth.config("image", depth=1, latent=(1, side * ph, side * pw))
+        m = dit.DiT(cfg)
+        m.load_weights(W)
+        lat0 = torch.randn((batch, C) + cfg["latent"], generator=g, device="cuda")
+        cond = torch.randn((batch, L, cfg["cond_dim"]), generator=g, device="cuda").to(torch.bfloat16).float()
+        unc = torch.zeros_like(cond)
+        lat = lat0.clone()
+        for _ in range(max(1, args.warmup)):
+            m.dit_denoise_loop(lat, batch, cfg["latent"], cond, unc, L, sig, cfg["guidance"], dit.LOOP_PARTIAL_SCHEDULE)
+        m.dit_synchronize()
+        lat = lat0.clone()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            m.dit_denoise_loop(lat, batch, cfg["latent"], cond, unc, L, sig, cfg["guidance"], dit.LOOP_PARTIAL_SCHEDULE)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_step = e0.elapsed_time(e1) / 1e3 / args.steps
+        fl = step_flops(cfg, 2 * batch, side * side, L)
+        tf = fl["total"] / t_step / 1e12
+        points.append({"batch": batch, "image_tokens": side * side, "cond_tokens": L,
+                       "steps_per_s": 1.0 / t_step, "ms_per_step": t_step * 1e3, "tflops": tf,
+                       "pct_bf16_peak": 100 * tf / peaks["bf16"],
+                       "finite": bool(torch.isfinite(lat).all().item())})
+        m.close()
+        del lat, lat0, cond, unc
+        torch.cuda.empty_cache()
+    print(json.dumps({"case": "image DiT block sweep: depth 1, one CFG + Euler step per point", "dtype": "bf16",
+                      "data": "synthetic (seeded N(0,1) latents/condition, N(0,0.02) bf16 weights)",
+                      "steps": args.steps, "warmup": args.warmup, "peak_bf16_tflops": peaks["bf16"],
+                      "points": points}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -412,11 +471,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=2, help="batch of the block case")
-    ap.add_argument("--case", default="step", choices=["step", "block"],
-                    help="block: one DiT block repeatedly (small case for kernel profiling)")
+    ap.add_argument("--case", default="step", choices=["step", "block", "sweep"],
+                    help="block: one DiT block repeatedly (small case for kernel profiling); "
+                         "sweep: image block batch/sequence sweep")
     args = ap.parse_args()
     if args.case == "block":
         run_block_case(args)
+    elif args.case == "sweep":
+        run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

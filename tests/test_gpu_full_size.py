@@ -82,6 +82,40 @@ def test_image_block_full_size(image_model):
         assert_block_close(got, ref)
 
 
+def _image_block_case(cfg, W, m, latent, batch, check, seed):
+    """The dual-stream block at `latent` with `batch` rows of the CFG batch;
+    sampled rows of the batch items in `check` against the oracle."""
+    grid = synth.grid(cfg, latent)
+    N, L, D = int(np.prod(grid)), cfg["cond_len"], cfg["hidden"]
+    rng = np.random.default_rng(seed)
+    x0 = (rng.standard_normal((batch, N, D)) * 0.2).astype(np.float32)
+    xc0 = synth.round_bf16(rng.standard_normal((batch, L, D)).astype(np.float32))
+    mods = np.stack([O.timestep_modulation(t, W, cfg) for t in np.linspace(900.0, 100.0, batch)]).astype(np.float32)
+    x, xc = dev(x0), dev(xc0)
+    m.dit_block_forward(1, x, xc, dev(mods), None, batch, grid, L)
+    m.dit_synchronize()
+    gx, gc = host(x), host(xc)
+    rows = _rows(L + N, extra=range(L - 2, L + 2))
+    angles = O.rope_angles(O.token_positions(grid), cfg["rope_axes"], cfg["rope_theta"])
+    for b in check:
+        ref = O.block_joint(x0[b], xc0[b], mods[b], W, 1, cfg, grid, rows=rows, angles=angles)
+        assert_block_close(np.concatenate([gc[b], gx[b]])[rows], ref)
+
+
+def test_image_block_sweep_batch4(image_model):
+    """Sweep point: batch 4 (two requests' CFG pairs) at 4096 + 512 tokens;
+    first and last batch items checked."""
+    cfg, W, m = image_model
+    _image_block_case(cfg, W, m, cfg["latent"], 4, (0, 3), seed=21)
+
+
+def test_image_block_sweep_16384_tokens(image_model):
+    """Sweep point: 16384 image tokens (128 x 128 grid) + 512 condition
+    tokens, batch 2."""
+    cfg, W, m = image_model
+    _image_block_case(cfg, W, m, (1, 256, 256), 2, (1,), seed=22)
+
+
 def test_image_loop_full_tokens_reduced_depth(image_model):
     """The whole denoise loop at the full 4096 + 512 token count, depth 2,
     two Euler steps with CFG: final latents against the full oracle loop."""
