@@ -18,13 +18,17 @@
 // S_{j+2} is issued into slot j%2 as soon as the softmax has copied S_j into
 // registers; P_j goes to P slot j%2 once PV_{j-2} has consumed P_{j-2}.
 //
-// Softmax: SM_WARPS warps.  Warp w reads TMEM lane quadrant q = w%4 (query
-// rows 32q..32q+31) and key columns [h*KPW, (h+1)*KPW) of every tile,
-// h = w/4.  The NQ warps of a quadrant share one O, so they agree on each
-// row's reference max: each publishes its partial max (rounded to bf16: any
-// common reference is exact, it only has to be the same for all of them) in
-// shared memory and they meet at a named barrier.  O and l are rescaled only
-// when the max grows by more than 2^8 (the warps decide identically).
+// Softmax: 8 warps.  Warp w reads TMEM lane quadrant q = w%4 (query rows
+// 32q..32q+31) and key columns [64h, 64h+64) of every tile, h = w/4.  The two
+// warps of a quadrant share one O, so they share each row's reference max m.
+// Per tile each warp first evaluates 2^(s*c - m) against the current m
+// without computing a row max, and flags the rows whose tile sum exceeds
+// SUM_LIMIT (only then can a p be large).  The warps exchange the flags in
+// shared memory at a 64-thread named barrier; for flagged rows (every row of
+// the first tile) they compute the tile's row max, exchange it (rounded to
+// bf16: any common reference is exact), move O and l to the new m and redo
+// those rows.  Both warps read the same flags, so they always take the same
+// path and their barriers stay matched.
 //
 // Warp SM_WARPS streams K and V with TMA through two 3-stage rings (K_j is loaded
 // once S_{j-3} has completed, V_j once PV_{j-3} has).  Completions are
@@ -47,24 +51,43 @@ constexpr int Q_OFF = 0;
 constexpr int K_OFF = Q_OFF + TILE_BYTES;
 constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
 constexpr int BAR_OFF = V_OFF + VST * TILE_BYTES;
-constexpr int XCH_OFF = BAR_OFF + 256;     // bf16[2 parities][NQ][128 rows]; float[NQ][128] at the end
+// Exchange area: bf16 row maxima [2 parities][NQ][128], then uint8 flags
+// [2][NQ][128]; after the loop float row sums [NQ][128] over the maxima.
+constexpr int XCH_OFF = BAR_OFF + 256;
 // The tiles need 1024-byte alignment.  The dynamic shared window of a kernel
 // without static shared memory starts 1024-aligned (checked at entry), so no
 // alignment slack is reserved and the total stays under 227 KB.
-constexpr int SMEM_BYTES = XCH_OFF + 2 * 4 * BQ * 2;  // sized for NQ <= 4
-#ifndef DIT_ATTN_SOFTMAX_WARPS
-#define DIT_ATTN_SOFTMAX_WARPS 8
-#endif
-constexpr int SM_WARPS = DIT_ATTN_SOFTMAX_WARPS;  // softmax warps: 8 or 16
+constexpr int SM_WARPS = 8;                       // softmax warps
 constexpr int NQ = SM_WARPS / 4;                  // warps per TMEM lane quadrant
 constexpr int KPW = BKV / NQ;                     // key columns per softmax warp
-static_assert(KPW == 32 || KPW == 64, "softmax warps must be 8 or 16");
+constexpr int SMEM_BYTES = XCH_OFF + 2 * NQ * BQ * 2 + 2 * NQ * BQ;
+static_assert(NQ * BQ * 4 <= 2 * NQ * BQ * 2 + 2 * NQ * BQ, "row sums must fit the exchange area");
 constexpr int NUM_THREADS = 32 * (SM_WARPS + 3);  // + TMA warp, S-MMA warp, PV-MMA warp
 constexpr int TMA_WARP = SM_WARPS, S_WARP = SM_WARPS + 1, PV_WARP = SM_WARPS + 2;
 constexpr uint32_t TM_S = 0, TM_P = 256, TM_O = 384;
 constexpr uint32_t IDESC_S = umma_idesc_bf16(128, 128, false);
 constexpr uint32_t IDESC_O = umma_idesc_bf16(128, 128, true);
-constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
+// A tile's exponentials are kept against the running reference max while
+// the row's tile sum stays below this (each p <= 2^14, far from overflow:
+// bf16 and fp32 keep their relative precision at any such magnitude).
+constexpr float SUM_LIMIT = 16384.0f;
+
+// p = 2^(s*c - m) for the KPW scores of one row, packed to bf16 pairs; returns
+// the row sum of the (unrounded) p.  Masked keys (s = -inf) give exactly 0.
+template <int NV>
+DIT_DEV float exp_tile(const float (&s)[NV], uint32_t (&pk)[NV / 2], float scale_log2, float m) {
+  const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m, -m);
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int i = 0; i < NV; i += 2) {
+    const float2 x = ffma2(make_float2(s[i], s[i + 1]), sc2, nm2);
+    const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    acc[(i >> 1) & 3] = fadd2(acc[(i >> 1) & 3], p);
+    pk[i / 2] = pack_bf16x2(p.x, p.y);
+  }
+  const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+  return (a01.x + a01.y) + (a23.x + a23.y);
+}
 }  // namespace fa
 
 __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
@@ -88,6 +111,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   __nv_bfloat16* xmax = reinterpret_cast<__nv_bfloat16*>(smem + XCH_OFF);
+  uint8_t* xflag = smem + XCH_OFF + 2 * NQ * BQ * 2;  // [2 parities][NQ][128 rows]
   float* xsum = reinterpret_cast<float*>(smem + XCH_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -224,6 +248,8 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     // still meets its quadrant partners at every named barrier.
     for (int j = 0; j < nkv; ++j) {
       float s[KPW];
+      uint32_t pk[KPW / 2];
+      float tsum = 0.f;
       ok = ok && __all_sync(0xffffffffu, mbar_wait(&s_done[j % 3], (uint32_t)((j / 3) & 1), abort_flag, err, 31));
       if (ok) {
         tc_fence_after();
@@ -247,41 +273,50 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
           for (int i = 0; i < KPW; ++i)
             if (i >= valid) s[i] = -INFINITY;
         }
-        // partial row max: four independent chains of three-input max
-        float m4[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-        for (int i = 4; i + 8 <= KPW - 4; i += 8)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], s[i + 2 * k], s[i + 2 * k + 1]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) m4[k] = fmaxf(m4[k], s[KPW - 4 + k]);
-        xmax[((j & 1) * NQ + h) * BQ + row] =
-            __float2bfloat16_rn(fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]) * scale_log2);
+        // Fast path: the exponentials against the current reference max, no
+        // row max.  A row whose tile sum exceeds SUM_LIMIT (so some p may be
+        // large) is flagged and redone below against the tile's row max.
+        bool big = true;
+        if (j > 0) {
+          tsum = exp_tile(s, pk, scale_log2, m_used);
+          big = !(tsum <= SUM_LIMIT);
+        }
+        xflag[((j & 1) * NQ + h) * BQ + row] = big ? 1 : 0;
       }
       named_bar_sync(1 + q, 32 * NQ);
-      if (!ok) continue;
-      // the row max of the tile over the quadrant's warps (every tile has a valid key)
-      const __nv_bfloat16* xm = xmax + (j & 1) * NQ * BQ + row;
-      float m_tile = __bfloat162float(xm[0]);
+      // every warp of the quadrant reads the same flags (stale ones after a
+      // failed wait), so all take the same path and the barriers stay matched
+      bool row_big = false;
 #pragma unroll
-      for (int w = 1; w < NQ; ++w) m_tile = fmaxf(m_tile, __bfloat162float(xm[w * BQ]));
-      const float m_new = fmaxf(m_used, m_tile);
-      if (j == 0) {
-        m_used = m_new;
-      } else {
-        const bool need = m_new - m_used > RESCALE_THRESHOLD;
-        if (__any_sync(0xffffffffu, need)) {
-          // O must hold PV_{j-1} before it is rescaled
+      for (int w = 0; w < NQ; ++w) row_big |= xflag[((j & 1) * NQ + w) * BQ + row] != 0;
+      if (__any_sync(0xffffffffu, row_big)) {
+        // slow path: the row max of the tile over the quadrant's warps
+        if (ok) {
+          float m4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+          for (int i = 4; i + 8 <= KPW - 4; i += 8)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], s[i + 2 * k], s[i + 2 * k + 1]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) m4[k] = fmaxf(m4[k], s[KPW - 4 + k]);
+          xmax[((j & 1) * NQ + h) * BQ + row] =
+              __float2bfloat16_rn(fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]) * scale_log2);
+        }
+        named_bar_sync(1 + q, 32 * NQ);
+        if (!ok) continue;
+        const __nv_bfloat16* xm = xmax + (j & 1) * NQ * BQ + row;
+        float m_tile = __bfloat162float(xm[0]);
+#pragma unroll
+        for (int w = 1; w < NQ; ++w) m_tile = fmaxf(m_tile, __bfloat162float(xm[w * BQ]));
+        const float m_new = row_big ? fmaxf(m_used, m_tile) : m_used;
+        if (j > 0) {
+          // O (and l) move to the new reference; O must hold PV_{j-1} first
           ok = __all_sync(0xffffffffu,
                           mbar_wait(&pv_done[(j - 1) % 3], (uint32_t)(((j - 1) / 3) & 1), abort_flag, err, 32));
           if (!ok) continue;
           tc_fence_after();
-          float alpha = 1.f;
-          if (need) {
-            alpha = ex2_approx(m_used - m_new);
-            m_used = m_new;
-            l *= alpha;
-          }
+          const float alpha = ex2_approx(m_used - m_new);  // 1 for rows not flagged
+          l *= alpha;
 #pragma unroll 1
           for (int c = 0; c < KPW / 32; ++c) {
             uint32_t r[32];
@@ -292,19 +327,13 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
             tmem_st32(o_col + c * 32, r);
           }
         }
+        if (row_big) {
+          m_used = m_new;
+          tsum = exp_tile(s, pk, scale_log2, m_used);
+        }
       }
-      const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m_used, -m_used);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      uint32_t pk[KPW / 2];
-#pragma unroll
-      for (int i = 0; i < KPW; i += 2) {
-        const float2 x = ffma2(make_float2(s[i], s[i + 1]), sc2, nm2);
-        const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        acc[(i >> 1) & 3] = fadd2(acc[(i >> 1) & 3], p);
-        pk[i / 2] = pack_bf16x2(p.x, p.y);
-      }
-      const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
-      l += (a01.x + a01.y) + (a23.x + a23.y);
+      if (!ok) continue;
+      l += tsum;
       // P slot j%2 held P_{j-2}: PV_{j-2} must have read it
       if (j >= 2) {
         ok = __all_sync(0xffffffffu,
