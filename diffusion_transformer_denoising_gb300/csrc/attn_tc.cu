@@ -30,8 +30,8 @@
 // those rows.  Both warps read the same flags, so they always take the same
 // path and their barriers stay matched.
 //
-// Warp SM_WARPS streams K and V with TMA through two 3-stage rings (K_j is loaded
-// once S_{j-3} has completed, V_j once PV_{j-3} has).  Completions are
+// Two loader warps stream K and V with TMA through two 3-stage rings (K_j is
+// loaded once S_{j-3} has completed, V_j once PV_{j-3} has).  Completions are
 // signalled by one tcgen05.commit per MMA group to rings s_done[3] /
 // pv_done[3]; every waiter's next completion on a barrier needs an action of
 // its own first, so a parity wait never aliases.
@@ -62,8 +62,8 @@ constexpr int NQ = SM_WARPS / 4;                  // warps per TMEM lane quadran
 constexpr int KPW = BKV / NQ;                     // key columns per softmax warp
 constexpr int SMEM_BYTES = XCH_OFF + 2 * NQ * BQ * 2 + 2 * NQ * BQ;
 static_assert(NQ * BQ * 4 <= 2 * NQ * BQ * 2 + 2 * NQ * BQ, "row sums must fit the exchange area");
-constexpr int NUM_THREADS = 32 * (SM_WARPS + 3);  // + TMA warp, S-MMA warp, PV-MMA warp
-constexpr int TMA_WARP = SM_WARPS, S_WARP = SM_WARPS + 1, PV_WARP = SM_WARPS + 2;
+constexpr int NUM_THREADS = 32 * (SM_WARPS + 4);  // + K/Q loader, S-MMA, PV-MMA, V loader warps
+constexpr int TMA_WARP = SM_WARPS, S_WARP = SM_WARPS + 1, PV_WARP = SM_WARPS + 2, VTMA_WARP = SM_WARPS + 3;
 constexpr uint32_t TM_S = 0, TM_P = 256, TM_O = 384;
 constexpr uint32_t IDESC_S = umma_idesc_bf16(128, 128, false);
 constexpr uint32_t IDESC_O = umma_idesc_bf16(128, 128, true);
@@ -149,39 +149,40 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == TMA_WARP) {
-    // ------------------------------------------------ TMA producer (one thread)
+  auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int tile) {
+    const int jt = (tile + kv_rot) % nkv;
+    mbar_arrive_expect_tx(bar, TILE_BYTES);
+    tma_load_3d(dst, tm, bar, 0, jt * BKV, bh);
+    tma_load_3d(dst + TILE_BYTES / 2, tm, bar, 64, jt * BKV, bh);
+  };
+  if (warp == TMA_WARP || warp == VTMA_WARP) {
+    // ------------------------------------------------ TMA producers (one thread each)
+    // K and V run on separate threads: S runs about two tiles ahead of PV,
+    // so a K load must not queue behind the wait for a V stage.
     if (lane == 0) {
-      int issued_k[3] = {0, 0, 0}, issued_v[3] = {0, 0, 0};
+      const bool is_k = warp == TMA_WARP;
+      uint64_t* full = is_k ? kf : vf;
+      uint64_t* consumed = is_k ? s_done : pv_done;
+      int issued[3] = {0, 0, 0};
       bool ok = true;
-      auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int tile) {
-        const int jt = (tile + kv_rot) % nkv;
-        mbar_arrive_expect_tx(bar, TILE_BYTES);
-        tma_load_3d(dst, tm, bar, 0, jt * BKV, bh);
-        tma_load_3d(dst + TILE_BYTES / 2, tm, bar, 64, jt * BKV, bh);
-      };
-      mbar_arrive_expect_tx(q_full, TILE_BYTES);
-      tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, q0, bh);
-      tma_load_3d(smem + Q_OFF + TILE_BYTES / 2, &tmQ, q_full, 64, q0, bh);
+      if (is_k) {
+        mbar_arrive_expect_tx(q_full, TILE_BYTES);
+        tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, q0, bh);
+        tma_load_3d(smem + Q_OFF + TILE_BYTES / 2, &tmQ, q_full, 64, q0, bh);
+      }
       for (int j = 0; j < nkv; ++j) {
-        // K stage j%3 was last read by S_{j-3}, V stage j%3 by PV_{j-3}
-        if (j >= 3) ok = mbar_wait(&s_done[j % 3], (uint32_t)(((j - 3) / 3) & 1), abort_flag, err, 21);
+        // stage j%3 was last read by S_{j-3} (K) or PV_{j-3} (V)
+        if (j >= 3) ok = mbar_wait(&consumed[j % 3], (uint32_t)(((j - 3) / 3) & 1), abort_flag, err, is_k ? 21 : 22);
         if (!ok) break;
-        load_tile(&tmK, smem + K_OFF + (j % KST) * TILE_BYTES, &kf[j % 3], j);
-        ++issued_k[j % 3];
-        if (j >= 3) ok = mbar_wait(&pv_done[j % 3], (uint32_t)(((j - 3) / 3) & 1), abort_flag, err, 22);
-        if (!ok) break;
-        load_tile(&tmV, smem + V_OFF + (j % VST) * TILE_BYTES, &vf[j % 3], j);
-        ++issued_v[j % 3];
+        load_tile(is_k ? &tmK : &tmV, smem + (is_k ? K_OFF : V_OFF) + (j % 3) * TILE_BYTES, &full[j % 3], j);
+        ++issued[j % 3];
       }
       if (!ok) {
         // wind down: every copy this thread started lands before the CTA exits
         volatile int no_abort = 0;
-        mbar_wait(q_full, 0, &no_abort, nullptr, 0);
-        for (int s = 0; s < 3; ++s) {
-          if (issued_k[s] > 0) mbar_wait(&kf[s], (uint32_t)((issued_k[s] - 1) & 1), &no_abort, nullptr, 0);
-          if (issued_v[s] > 0) mbar_wait(&vf[s], (uint32_t)((issued_v[s] - 1) & 1), &no_abort, nullptr, 0);
-        }
+        if (is_k) mbar_wait(q_full, 0, &no_abort, nullptr, 0);
+        for (int s = 0; s < 3; ++s)
+          if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1), &no_abort, nullptr, 0);
       }
     }
     __syncwarp();
