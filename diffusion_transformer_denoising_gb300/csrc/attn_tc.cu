@@ -22,12 +22,13 @@
 // 32q..32q+31) and key columns [64h, 64h+64) of every tile, h = w/4.  The two
 // warps of a quadrant share one O, so they share each row's reference max m.
 // Per tile each warp first evaluates 2^(s*c - m) against the current m
-// without computing a row max, and flags the rows whose tile sum exceeds
-// SUM_LIMIT (only then can a p be large).  The warps exchange the flags in
-// shared memory at a 64-thread named barrier; for flagged rows (every row of
-// the first tile) they compute the tile's row max, exchange it (rounded to
-// bf16: any common reference is exact), move O and l to the new m and redo
-// those rows.  Both warps read the same flags, so they always take the same
+// without computing a row max, and raises a flag when a row's tile sum
+// exceeds SUM_LIMIT (only then can a p be large).  One 64-thread barrier
+// reduction (bar.red.or) tells both warps whether any flag is up; if so (and
+// on the first tile) they compute the tile's row max, exchange it in shared
+// memory (rounded to bf16: any common reference is exact), move the rows
+// whose max grew by more than 2^8 to it (O and l rescaled) and redo those
+// rows.  Both warps get the same reduction, so they always take the same
 // path and their barriers stay matched.
 //
 // Two loader warps stream K and V with TMA through two 3-stage rings (K_j is
@@ -51,8 +52,8 @@ constexpr int Q_OFF = 0;
 constexpr int K_OFF = Q_OFF + TILE_BYTES;
 constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
 constexpr int BAR_OFF = V_OFF + VST * TILE_BYTES;
-// Exchange area: bf16 row maxima [2 parities][NQ][128], then uint8 flags
-// [2][NQ][128]; after the loop float row sums [NQ][128] over the maxima.
+// Exchange area: bf16 row maxima [2 parities][NQ][128]; after the loop float
+// row sums [NQ][128] over them.
 constexpr int XCH_OFF = BAR_OFF + 256;
 // The tiles need 1024-byte alignment.  The dynamic shared window of a kernel
 // without static shared memory starts 1024-aligned (checked at entry), so no
@@ -60,13 +61,15 @@ constexpr int XCH_OFF = BAR_OFF + 256;
 constexpr int SM_WARPS = 8;                       // softmax warps
 constexpr int NQ = SM_WARPS / 4;                  // warps per TMEM lane quadrant
 constexpr int KPW = BKV / NQ;                     // key columns per softmax warp
-constexpr int SMEM_BYTES = XCH_OFF + 2 * NQ * BQ * 2 + 2 * NQ * BQ;
-static_assert(NQ * BQ * 4 <= 2 * NQ * BQ * 2 + 2 * NQ * BQ, "row sums must fit the exchange area");
+constexpr int SMEM_BYTES = XCH_OFF + 2 * NQ * BQ * 2;
+static_assert(NQ * BQ * 4 <= 2 * NQ * BQ * 2, "row sums must fit the exchange area");
 constexpr int NUM_THREADS = 32 * (SM_WARPS + 4);  // + K/Q loader, S-MMA, PV-MMA, V loader warps
 constexpr int TMA_WARP = SM_WARPS, S_WARP = SM_WARPS + 1, PV_WARP = SM_WARPS + 2, VTMA_WARP = SM_WARPS + 3;
 constexpr uint32_t TM_S = 0, TM_P = 256, TM_O = 384;
 constexpr uint32_t IDESC_S = umma_idesc_bf16(128, 128, false);
 constexpr uint32_t IDESC_O = umma_idesc_bf16(128, 128, true);
+// A row moves to a new reference max only when its max grew by more than 2^8.
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 // A tile's exponentials are kept against the running reference max while
 // the row's tile sum stays below this (each p <= 2^14, far from overflow:
 // bf16 and fp32 keep their relative precision at any such magnitude).
@@ -111,7 +114,6 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   __nv_bfloat16* xmax = reinterpret_cast<__nv_bfloat16*>(smem + XCH_OFF);
-  uint8_t* xflag = smem + XCH_OFF + 2 * NQ * BQ * 2;  // [2 parities][NQ][128 rows]
   float* xsum = reinterpret_cast<float*>(smem + XCH_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -251,6 +253,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       float s[KPW];
       uint32_t pk[KPW / 2];
       float tsum = 0.f;
+      bool big = true;  // a warp that skipped its work asks for the slow path
       ok = ok && __all_sync(0xffffffffu, mbar_wait(&s_done[j % 3], (uint32_t)((j / 3) & 1), abort_flag, err, 31));
       if (ok) {
         tc_fence_after();
@@ -277,20 +280,14 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
         // Fast path: the exponentials against the current reference max, no
         // row max.  A row whose tile sum exceeds SUM_LIMIT (so some p may be
         // large) is flagged and redone below against the tile's row max.
-        bool big = true;
         if (j > 0) {
           tsum = exp_tile(s, pk, scale_log2, m_used);
           big = !(tsum <= SUM_LIMIT);
         }
-        xflag[((j & 1) * NQ + h) * BQ + row] = big ? 1 : 0;
       }
-      named_bar_sync(1 + q, 32 * NQ);
-      // every warp of the quadrant reads the same flags (stale ones after a
-      // failed wait), so all take the same path and the barriers stay matched
-      bool row_big = false;
-#pragma unroll
-      for (int w = 0; w < NQ; ++w) row_big |= xflag[((j & 1) * NQ + w) * BQ + row] != 0;
-      if (__any_sync(0xffffffffu, row_big)) {
+      // one barrier of the quadrant's warps that ORs their flags: all of them
+      // get the same answer, take the same path and keep the barriers matched
+      if (named_bar_or(1 + q, 32 * NQ, big)) {
         // slow path: the row max of the tile over the quadrant's warps
         if (ok) {
           float m4[4] = {s[0], s[1], s[2], s[3]};
@@ -309,14 +306,17 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
         float m_tile = __bfloat162float(xm[0]);
 #pragma unroll
         for (int w = 1; w < NQ; ++w) m_tile = fmaxf(m_tile, __bfloat162float(xm[w * BQ]));
-        const float m_new = row_big ? fmaxf(m_used, m_tile) : m_used;
+        // rows whose max grew by more than 2^8 (every row of the first tile)
+        // move to the tile max; the others keep their fast-path exponentials
+        const bool row_big = m_tile - m_used > RESCALE_THRESHOLD;
+        const float m_new = row_big ? m_tile : m_used;
         if (j > 0) {
           // O (and l) move to the new reference; O must hold PV_{j-1} first
           ok = __all_sync(0xffffffffu,
                           mbar_wait(&pv_done[(j - 1) % 3], (uint32_t)(((j - 1) / 3) & 1), abort_flag, err, 32));
           if (!ok) continue;
           tc_fence_after();
-          const float alpha = ex2_approx(m_used - m_new);  // 1 for rows not flagged
+          const float alpha = ex2_approx(m_used - m_new);  // 1 for rows kept
           l *= alpha;
 #pragma unroll 1
           for (int c = 0; c < KPW / 32; ++c) {
