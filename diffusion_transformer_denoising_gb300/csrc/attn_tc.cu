@@ -31,11 +31,11 @@
 // rows.  Both warps get the same reduction, so they always take the same
 // path and their barriers stay matched.
 //
-// Two loader warps stream K and V with TMA through two 3-stage rings (K_j is
-// loaded once S_{j-3} has completed, V_j once PV_{j-3} has).  Completions are
-// signalled by one tcgen05.commit per MMA group to rings s_done[3] /
-// pv_done[3]; every waiter's next completion on a barrier needs an action of
-// its own first, so a parity wait never aliases.
+// Two loader warps stream K and V with TMA through rings of KST and VST
+// stages (K_j is loaded once S_{j-KST} has completed, V_j once PV_{j-VST}
+// has).  Completions are signalled by one tcgen05.commit per MMA group to
+// rings s_done[SR] / pv_done[PR]; every waiter's next completion on a barrier
+// needs an action of its own first, so a parity wait never aliases.
 //
 // All waits are bounded (common.cuh); on a timeout the CTA flags *err, keeps
 // the softmax warps' named barriers matched, waits for its own copies and
@@ -46,7 +46,12 @@
 namespace dit {
 
 namespace fa {
-constexpr int BQ = 128, BKV = 128, HD = 128, KST = 3, VST = 3;
+constexpr int BQ = 128, BKV = 128, HD = 128;
+// K stages, V stages, and the completion rings of S_j and PV_j.  S runs about
+// two tiles ahead of PV, so K needs less lead than V.  A ring must be at least
+// as long as the stage count its loader waits on (SR >= KST, PR >= VST) so that
+// no parity wait can alias.
+constexpr int KST = 2, VST = 4, SR = 3, PR = 4;
 constexpr int TILE_BYTES = 128 * HD * 2;   // 32 KB: two 16 KB swizzle blocks of 64 channels
 constexpr int Q_OFF = 0;
 constexpr int K_OFF = Q_OFF + TILE_BYTES;
@@ -62,6 +67,7 @@ constexpr int SM_WARPS = 8;                       // softmax warps
 constexpr int NQ = SM_WARPS / 4;                  // warps per TMEM lane quadrant
 constexpr int KPW = BKV / NQ;                     // key columns per softmax warp
 constexpr int SMEM_BYTES = XCH_OFF + 2 * NQ * BQ * 2;
+static_assert(SR >= KST && PR >= VST && VST <= 4, "completion rings shorter than the stage rings");
 static_assert(NQ * BQ * 4 <= 2 * NQ * BQ * 2, "row sums must fit the exchange area");
 constexpr int NUM_THREADS = 32 * (SM_WARPS + 4);  // + K/Q loader, S-MMA, PV-MMA, V loader warps
 constexpr int TMA_WARP = SM_WARPS, S_WARP = SM_WARPS + 1, PV_WARP = SM_WARPS + 2, VTMA_WARP = SM_WARPS + 3;
@@ -104,14 +110,14 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
   uint64_t* q_full = bars;         // Q tile
-  uint64_t* kf = bars + 1;         // [3] K stage loaded
-  uint64_t* vf = bars + 4;         // [3] V stage loaded
-  uint64_t* s_done = bars + 7;     // [3] S_j complete (ring by j % 3)
-  uint64_t* pv_done = bars + 10;   // [3] PV_j complete (ring by j % 3)
-  uint64_t* s_free = bars + 13;    // [2] softmax has copied S slot j % 2 (one arrival per softmax warp)
-  uint64_t* p_ready = bars + 15;   // [2] P slot j % 2 written (one arrival per softmax warp)
-  uint64_t* drain = bars + 17;     // [2] final commit of each MMA thread
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+  uint64_t* kf = bars + 1;              // [KST] K stage loaded
+  uint64_t* vf = kf + KST;              // [VST] V stage loaded
+  uint64_t* s_done = vf + VST;          // [SR] S_j complete (ring by j % SR)
+  uint64_t* pv_done = s_done + SR;      // [PR] PV_j complete (ring by j % PR)
+  uint64_t* s_free = pv_done + PR;      // [2] softmax has copied S slot j % 2 (one arrival per softmax warp)
+  uint64_t* p_ready = s_free + 2;       // [2] P slot j % 2 written (one arrival per softmax warp)
+  uint64_t* drain = p_ready + 2;        // [2] final commit of each MMA thread
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   __nv_bfloat16* xmax = reinterpret_cast<__nv_bfloat16*>(smem + XCH_OFF);
   float* xsum = reinterpret_cast<float*>(smem + XCH_OFF);
@@ -126,12 +132,10 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 3; ++s) {
-      mbar_init(&kf[s], 1);
-      mbar_init(&vf[s], 1);
-      mbar_init(&s_done[s], 1);
-      mbar_init(&pv_done[s], 1);
-    }
+    for (int i = 0; i < KST; ++i) mbar_init(&kf[i], 1);
+    for (int i = 0; i < VST; ++i) mbar_init(&vf[i], 1);
+    for (int i = 0; i < SR; ++i) mbar_init(&s_done[i], 1);
+    for (int i = 0; i < PR; ++i) mbar_init(&pv_done[i], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_free[b], SM_WARPS);
       mbar_init(&p_ready[b], SM_WARPS);
@@ -165,7 +169,8 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       const bool is_k = warp == TMA_WARP;
       uint64_t* full = is_k ? kf : vf;
       uint64_t* consumed = is_k ? s_done : pv_done;
-      int issued[3] = {0, 0, 0};
+      const int nst = is_k ? KST : VST, ring = is_k ? SR : PR;
+      int issued[4] = {0, 0, 0, 0};
       bool ok = true;
       if (is_k) {
         mbar_arrive_expect_tx(q_full, TILE_BYTES);
@@ -173,17 +178,20 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
         tma_load_3d(smem + Q_OFF + TILE_BYTES / 2, &tmQ, q_full, 64, q0, bh);
       }
       for (int j = 0; j < nkv; ++j) {
-        // stage j%3 was last read by S_{j-3} (K) or PV_{j-3} (V)
-        if (j >= 3) ok = mbar_wait(&consumed[j % 3], (uint32_t)(((j - 3) / 3) & 1), abort_flag, err, is_k ? 21 : 22);
+        // stage j % nst was last read by S_{j-nst} (K) or PV_{j-nst} (V)
+        if (j >= nst) {
+          const int c = j - nst;
+          ok = mbar_wait(&consumed[c % ring], (uint32_t)((c / ring) & 1), abort_flag, err, is_k ? 21 : 22);
+        }
         if (!ok) break;
-        load_tile(is_k ? &tmK : &tmV, smem + (is_k ? K_OFF : V_OFF) + (j % 3) * TILE_BYTES, &full[j % 3], j);
-        ++issued[j % 3];
+        load_tile(is_k ? &tmK : &tmV, smem + (is_k ? K_OFF : V_OFF) + (j % nst) * TILE_BYTES, &full[j % nst], j);
+        ++issued[j % nst];
       }
       if (!ok) {
         // wind down: every copy this thread started lands before the CTA exits
         volatile int no_abort = 0;
         if (is_k) mbar_wait(q_full, 0, &no_abort, nullptr, 0);
-        for (int s = 0; s < 3; ++s)
+        for (int s = 0; s < nst; ++s)
           if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1), &no_abort, nullptr, 0);
       }
     }
@@ -197,7 +205,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       for (int j = 0; ok && j < nkv; ++j) {
         // slot j%2 is free once the softmax has copied S_{j-2}
         if (j >= 2) ok = mbar_wait(&s_free[j & 1], (uint32_t)(((j - 2) >> 1) & 1), abort_flag, err, 24);
-        ok = ok && mbar_wait(&kf[j % 3], (uint32_t)((j / 3) & 1), abort_flag, err, 25);
+        ok = ok && mbar_wait(&kf[j % KST], (uint32_t)((j / KST) & 1), abort_flag, err, 25);
         if (!ok) break;
         tc_fence_after();
         const uint64_t kd = umma_desc_add(k_desc, (j % KST) * TILE_BYTES);
@@ -207,7 +215,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
           const uint32_t off = (kk >> 2) * (TILE_BYTES / 2) + (kk & 3) * 32;
           umma_ss(d_tmem, umma_desc_add(q_desc, off), umma_desc_add(kd, off), IDESC_S, kk != 0);
         }
-        umma_commit(&s_done[j % 3]);
+        umma_commit(&s_done[j % SR]);
       }
       // all MMAs issued by this thread complete before tensor memory is released
       umma_commit(&drain[0]);
@@ -222,7 +230,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       bool ok = true;
       for (int j = 0; ok && j < nkv; ++j) {
         ok = mbar_wait(&p_ready[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, err, 26) &&
-             mbar_wait(&vf[j % 3], (uint32_t)((j / 3) & 1), abort_flag, err, 27);
+             mbar_wait(&vf[j % VST], (uint32_t)((j / VST) & 1), abort_flag, err, 27);
         if (!ok) break;
         tc_fence_after();
         const uint64_t vd = umma_desc_add(v_desc, (j % VST) * TILE_BYTES);
@@ -232,7 +240,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
           // keys 16kk..16kk+15: P columns 8kk.. (bf16 pairs), V rows 16kk.. (8-row groups 1 KB apart)
           umma_ts(tmem + TM_O, p_tmem + kk * 8, umma_desc_add(vd, kk * 2048), IDESC_O, (j | kk) != 0);
         }
-        umma_commit(&pv_done[j % 3]);
+        umma_commit(&pv_done[j % PR]);
       }
       umma_commit(&drain[1]);
       volatile int no_abort = 0;
@@ -254,7 +262,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       uint32_t pk[KPW / 2];
       float tsum = 0.f;
       bool big = true;  // a warp that skipped its work asks for the slow path
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(&s_done[j % 3], (uint32_t)((j / 3) & 1), abort_flag, err, 31));
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&s_done[j % SR], (uint32_t)((j / SR) & 1), abort_flag, err, 31));
       if (ok) {
         tc_fence_after();
         {
@@ -313,7 +321,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
         if (j > 0) {
           // O (and l) move to the new reference; O must hold PV_{j-1} first
           ok = __all_sync(0xffffffffu,
-                          mbar_wait(&pv_done[(j - 1) % 3], (uint32_t)(((j - 1) / 3) & 1), abort_flag, err, 32));
+                          mbar_wait(&pv_done[(j - 1) % PR], (uint32_t)(((j - 1) / PR) & 1), abort_flag, err, 32));
           if (!ok) continue;
           tc_fence_after();
           const float alpha = ex2_approx(m_used - m_new);  // 1 for rows kept
@@ -338,7 +346,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       // P slot j%2 held P_{j-2}: PV_{j-2} must have read it
       if (j >= 2) {
         ok = __all_sync(0xffffffffu,
-                        mbar_wait(&pv_done[(j - 2) % 3], (uint32_t)(((j - 2) / 3) & 1), abort_flag, err, 33));
+                        mbar_wait(&pv_done[(j - 2) % PR], (uint32_t)(((j - 2) / PR) & 1), abort_flag, err, 33));
         if (!ok) continue;
         tc_fence_after();
       }
@@ -354,7 +362,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     }
     // O is final once PV_{nkv-1} has completed
     ok = ok && __all_sync(0xffffffffu,
-                          mbar_wait(&pv_done[(nkv - 1) % 3], (uint32_t)(((nkv - 1) / 3) & 1), abort_flag, err, 34));
+                          mbar_wait(&pv_done[(nkv - 1) % PR], (uint32_t)(((nkv - 1) / PR) & 1), abort_flag, err, 34));
     // the quadrant's partial row sums (same reference max) go through the
     // exchange buffer once every warp of the quadrant has read its maxima
     named_bar_sync(1 + q, 32 * NQ);
