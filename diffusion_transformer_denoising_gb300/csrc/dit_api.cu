@@ -1013,6 +1013,14 @@ extern "C" dit_status dit_synchronize(dit_model* m, void* stream) {
   return DIT_OK;
 }
 
+extern "C" dit_status dit_debug_stall(dit_model* m, void* stream) {
+  g_last_error[0] = 0;
+  if (!m) return fail(DIT_ERR_INVALID_ARG, "model is NULL");
+  CU_TRY(cudaSetDevice(m->device));
+  K_TRY(debug_stall(m->d_err, DIT_DEBUG_STALL_SITE, static_cast<cudaStream_t>(stream)));
+  return DIT_OK;
+}
+
 extern "C" dit_status dit_profile_start(dit_model* m, int timing) {
   g_last_error[0] = 0;
   if (!m) return fail(DIT_ERR_INVALID_ARG, "model is NULL");

@@ -379,4 +379,24 @@ cudaError_t bf16_to_f32(const void* in, float* out, int64_t n, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Test hook for the bounded-wait failure path: one warp waits on an mbarrier
+// that nothing ever arrives on.  The wait gives up after DIT_WAIT_LIMIT_NS,
+// records `site` in *err and the kernel returns; the context stays usable.
+__global__ void debug_stall_kernel(int* err, int site) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, err, site);
+}
+
+cudaError_t debug_stall(int* err, int site, cudaStream_t s) {
+  debug_stall_kernel<<<1, 32, 0, s>>>(err, site);
+  return cudaGetLastError();
+}
+
 }  // namespace dit

@@ -99,4 +99,7 @@ cudaError_t euler_kernel(float* x, const float* v, float dsig, int64_t n, cudaSt
 cudaError_t f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t s);
 cudaError_t bf16_to_f32(const void* in, float* out, int64_t n, cudaStream_t s);
 
+// Test hook: a kernel whose bounded wait runs out and records `site` in *err.
+cudaError_t debug_stall(int* err, int site, cudaStream_t s);
+
 }  // namespace dit

@@ -253,6 +253,16 @@ const char* dit_last_error(void);
  * DIT_ERR_OOM (0 disables).  Host-side only; used to test failure paths. */
 void dit_debug_fail_alloc_after(int n);
 
+/* Test hook for the device-side failure path.  Enqueues on `stream` a kernel
+ * whose bounded wait on a barrier that nothing ever arrives on gives up after
+ * the library's wait limit (1.5 s) and records DIT_DEBUG_STALL_SITE in the
+ * model's error word; the next dit_synchronize then returns DIT_ERR_TIMEOUT
+ * (and clears the word).  Nothing faults or hangs, and the model stays
+ * usable.  Returns DIT_ERR_INVALID_ARG for a NULL model, DIT_ERR_CUDA if the
+ * launch fails. */
+enum { DIT_DEBUG_STALL_SITE = 99 };
+dit_status dit_debug_stall(dit_model* m, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

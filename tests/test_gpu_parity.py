@@ -275,3 +275,22 @@ def test_injected_allocation_failure():
     assert e.value.status == dit.DIT_ERR_OOM
     dit.dit_debug_fail_alloc_after(0)
     dit.DiT(cfg).close()
+
+
+def test_device_wait_timeout_is_reported_and_model_stays_usable(tiny):
+    """A bounded device wait that nothing completes gives up after the wait
+    limit: the failure surfaces as DIT_ERR_TIMEOUT at the next synchronize,
+    the error word is cleared, and the same model keeps producing correct
+    results (no fault, no hang, context intact)."""
+    cfg, W, m = tiny
+    m.dit_debug_stall()
+    with pytest.raises(dit.DitError) as e:
+        m.dit_synchronize()
+    assert e.value.status == dit.DIT_ERR_TIMEOUT
+    assert "site 99" in str(e.value)
+    m.dit_synchronize()  # the word was cleared
+    t = np.array([500.0], np.float32)
+    out = empty(1, 6 * cfg["hidden"])
+    m.dit_timestep_modulation(t, out)
+    m.dit_synchronize()
+    assert rel_max_err(host(out)[0], O.timestep_modulation(500.0, W, cfg)) < TOL_F32
