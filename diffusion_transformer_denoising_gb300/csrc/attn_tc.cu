@@ -33,9 +33,13 @@
 //
 // Two loader warps stream K and V with TMA through rings of KST and VST
 // stages (K_j is loaded once S_{j-KST} has completed, V_j once PV_{j-VST}
-// has).  Completions are signalled by one tcgen05.commit per MMA group to
-// rings s_done[SR] / pv_done[PR]; every waiter's next completion on a barrier
-// needs an action of its own first, so a parity wait never aliases.
+// has).  Completions are signalled by tcgen05.commit to rings s_done[SR]
+// (loader of K), pv_done[PR] (loader of V, O rescale, end) and tile_ready[SR],
+// which takes two commits per tile -- S_j from the S thread and PV_{j-2} from
+// the PV thread -- so the softmax of tile j makes a single wait for "S_j is
+// in tensor memory and P slot j%2 is free".  Every waiter's next completion
+// on a barrier needs an action of its own first, so a parity wait never
+// aliases.
 //
 // All waits are bounded (common.cuh); on a timeout the CTA flags *err, keeps
 // the softmax warps' named barriers matched, waits for its own copies and
@@ -117,7 +121,8 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   uint64_t* s_free = pv_done + PR;      // [2] softmax has copied S slot j % 2 (one arrival per softmax warp)
   uint64_t* p_ready = s_free + 2;       // [2] P slot j % 2 written (one arrival per softmax warp)
   uint64_t* drain = p_ready + 2;        // [2] final commit of each MMA thread
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+  uint64_t* tile_ready = drain + 2;     // [SR] S_j and PV_{j-2} complete (two commits)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tile_ready + SR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   __nv_bfloat16* xmax = reinterpret_cast<__nv_bfloat16*>(smem + XCH_OFF);
   float* xsum = reinterpret_cast<float*>(smem + XCH_OFF);
@@ -136,6 +141,10 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     for (int i = 0; i < VST; ++i) mbar_init(&vf[i], 1);
     for (int i = 0; i < SR; ++i) mbar_init(&s_done[i], 1);
     for (int i = 0; i < PR; ++i) mbar_init(&pv_done[i], 1);
+    for (int i = 0; i < SR; ++i) mbar_init(&tile_ready[i], 2);
+    // tiles 0 and 1 have no PV_{j-2}: its arrival is made up front
+    mbar_arrive(&tile_ready[0]);
+    mbar_arrive(&tile_ready[1 % SR]);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_free[b], SM_WARPS);
       mbar_init(&p_ready[b], SM_WARPS);
@@ -216,6 +225,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
           umma_ss(d_tmem, umma_desc_add(q_desc, off), umma_desc_add(kd, off), IDESC_S, kk != 0);
         }
         umma_commit(&s_done[j % SR]);
+        umma_commit(&tile_ready[j % SR]);
       }
       // all MMAs issued by this thread complete before tensor memory is released
       umma_commit(&drain[0]);
@@ -241,6 +251,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
           umma_ts(tmem + TM_O, p_tmem + kk * 8, umma_desc_add(vd, kk * 2048), IDESC_O, (j | kk) != 0);
         }
         umma_commit(&pv_done[j % PR]);
+        umma_commit(&tile_ready[(j + 2) % SR]);
       }
       umma_commit(&drain[1]);
       volatile int no_abort = 0;
@@ -262,7 +273,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       uint32_t pk[KPW / 2];
       float tsum = 0.f;
       bool big = true;  // a warp that skipped its work asks for the slow path
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(&s_done[j % SR], (uint32_t)((j / SR) & 1), abort_flag, err, 31));
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&tile_ready[j % SR], (uint32_t)((j / SR) & 1), abort_flag, err, 31));
       if (ok) {
         tc_fence_after();
         {
@@ -343,13 +354,6 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       }
       if (!ok) continue;
       l += tsum;
-      // P slot j%2 held P_{j-2}: PV_{j-2} must have read it
-      if (j >= 2) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&pv_done[(j - 2) % PR], (uint32_t)(((j - 2) / PR) & 1), abort_flag, err, 33));
-        if (!ok) continue;
-        tc_fence_after();
-      }
       const uint32_t p_col = tmem + TM_P + (j & 1) * 64 + h * (KPW / 2) + lane_off;
       if constexpr (KPW == 64)
         tmem_st32(p_col, *reinterpret_cast<const uint32_t(*)[32]>(pk));
