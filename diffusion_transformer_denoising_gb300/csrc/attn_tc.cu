@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       uint32_t pk[KPW / 2];
       float tsum = 0.f;
       bool big = true;  // a warp that skipped its work asks for the slow path
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(&tile_ready[j % SR], (uint32_t)((j / SR) & 1), abort_flag, err, 31));
+      ok = ok && mbar_wait_warp(&tile_ready[j % SR], (uint32_t)((j / SR) & 1), abort_flag, err, 31);
       if (ok) {
         tc_fence_after();
         {
@@ -331,8 +331,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
         const float m_new = row_big ? m_tile : m_used;
         if (j > 0) {
           // O (and l) move to the new reference; O must hold PV_{j-1} first
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(&pv_done[(j - 1) % PR], (uint32_t)(((j - 1) / PR) & 1), abort_flag, err, 32));
+          ok = mbar_wait_warp(&pv_done[(j - 1) % PR], (uint32_t)(((j - 1) / PR) & 1), abort_flag, err, 32);
           if (!ok) continue;
           tc_fence_after();
           const float alpha = ex2_approx(m_used - m_new);  // 1 for rows kept
@@ -365,8 +364,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(&p_ready[j & 1]);
     }
     // O is final once PV_{nkv-1} has completed
-    ok = ok && __all_sync(0xffffffffu,
-                          mbar_wait(&pv_done[(nkv - 1) % PR], (uint32_t)(((nkv - 1) / PR) & 1), abort_flag, err, 34));
+    ok = ok && mbar_wait_warp(&pv_done[(nkv - 1) % PR], (uint32_t)(((nkv - 1) / PR) & 1), abort_flag, err, 34);
     // the quadrant's partial row sums (same reference max) go through the
     // exchange buffer once every warp of the quadrant has read its maxima
     named_bar_sync(1 + q, 32 * NQ);

@@ -141,6 +141,14 @@ DIT_DEV bool named_bar_or(int id, int nthreads, bool v) {
   return r != 0;
 }
 
+// Bounded wait by all 32 lanes of a converged warp; true on every lane when
+// the phase has completed.  The common case (already complete) is one
+// try_wait per lane and a vote.
+DIT_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err, int site) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  return __all_sync(0xffffffffu, mbar_wait_slow(bar, parity, abort_flag, err, site));
+}
+
 // ---------------------------------------------------------------- TMA
 DIT_DEV void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

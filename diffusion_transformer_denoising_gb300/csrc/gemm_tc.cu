@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
       const uint32_t acc = local & 1, aphase = (local >> 1) & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], aphase, abort_flag, err, 14));
+      ok = mbar_wait_warp(&tfull[acc], aphase, abort_flag, err, 14);
       if (!ok) break;
       tc_fence_after();
       const int mb = tile / n_tiles, nb = tile - mb * n_tiles;
