@@ -5,7 +5,7 @@ output for a sample of rows (first, last, ragged-tail and spread rows)."""
 import numpy as np
 import pytest
 
-from diffusion_transformer_denoising_gb300 import synth
+from diffusion_transformer_denoising_gb300 import dit, synth
 from oracle import dit_oracle as O
 from tests.gpu_util import COS_BF16_LOOP, assert_block_close, cosine, dev, empty, host, make_model, rel_max_err
 
@@ -134,6 +134,33 @@ def test_image_loop_full_tokens_reduced_depth(image_model):
     assert cosine(got - lat[0], ref - lat[0]) >= 0.99
 
 
+def test_video_loop_bf16_tracks_fp32_path_full_tokens():
+    """Transitive full-loop check at the video token count: the bf16
+    production path against the fp32 test-precision path (itself pinned to
+    the oracle at 1e-4 on complete loops), same bf16-rounded weights and
+    condition, depth 4, two CFG + Euler steps over 32760 tokens."""
+    cfg_b = synth.config("video", depth=4)
+    cfg_f = dict(cfg_b, precision=synth.PREC_F32)
+    W = synth.make_weights(cfg_b, seed=41)  # bf16-rounded values, read as fp32 by the test path
+    L = cfg_b["cond_len"]
+    lat = synth.make_latent(cfg_b, batch=1, seed=42)
+    cond = synth.make_cond(cfg_b, batch=1, seed=43)
+    unc = np.zeros_like(cond)
+    sig = O.shift_sigma(O.sigma_schedule(cfg_b["steps"]), cfg_b["shift"])[:3].astype(np.float32)
+    out = {}
+    for name, cfg in (("bf16", cfg_b), ("fp32", cfg_f)):
+        m = make_model(cfg, W)
+        x = dev(lat)
+        m.dit_denoise_loop(x, 1, cfg["latent"], dev(cond), dev(unc), L, sig, cfg["guidance"],
+                           flags=dit.LOOP_PARTIAL_SCHEDULE)
+        m.dit_synchronize()
+        out[name] = host(x)[0]
+        m.close()
+    assert np.isfinite(out["bf16"]).all()
+    assert cosine(out["bf16"], out["fp32"]) >= COS_BF16_LOOP
+    assert cosine(out["bf16"] - lat[0], out["fp32"] - lat[0]) >= 0.99
+
+
 def test_video_embed_head_and_cfg_euler_full_size(video_block):
     """Patch embedding, final layer and guidance + Euler at the full video
     latent size (16 x 21 x 60 x 104)."""
@@ -159,7 +186,6 @@ def test_video_embed_head_and_cfg_euler_full_size(video_block):
     for b in range(2):
         ref = O.unpatchify(O.final_layer(xs[b], mods[b], W, cfg), cfg["patch"], (cfg["in_channels"],) + thw)
         assert_block_close(gv[b], ref)
-    from diffusion_transformer_denoising_gb300 import dit
     n = gv[0].size
     out = empty(n)
     dit.cfg_combine(dev(gv[0]), dev(gv[1]), 5.0, out, n)
