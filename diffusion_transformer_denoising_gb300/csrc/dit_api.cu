@@ -475,10 +475,19 @@ static dit_status ensure_rope(dit_model* m, const int32_t g[3]) {
     cudaFree(m->rope);
     m->rope = nullptr;
   }
-  const size_t bytes = tab.size() * sizeof(float2);
+  // followed by the inverse frequency of each pair, for kernels that form
+  // the angles themselves
+  std::vector<float> inv(half);
+  for (int a = 0, p = 0; a < 3; ++a)
+    for (int j = 0; j < c.rope_axes[a] / 2; ++j, ++p)
+      inv[p] = (float)pow((double)c.rope_theta, -2.0 * j / c.rope_axes[a]);
+  const size_t tab_bytes = tab.size() * sizeof(float2);
+  const size_t bytes = tab_bytes + half * sizeof(float);
   DIT_TRY(dev_alloc(reinterpret_cast<void**>(&m->rope), bytes));
   m->rope_bytes = bytes;
-  CU_TRY(cudaMemcpy(m->rope, tab.data(), bytes, cudaMemcpyHostToDevice));
+  CU_TRY(cudaMemcpy(m->rope, tab.data(), tab_bytes, cudaMemcpyHostToDevice));
+  CU_TRY(cudaMemcpy(reinterpret_cast<uint8_t*>(m->rope) + tab_bytes, inv.data(), half * sizeof(float),
+                    cudaMemcpyHostToDevice));
   memcpy(m->rope_grid, g, sizeof(m->rope_grid));
   return DIT_OK;
 }
@@ -545,6 +554,14 @@ static EpiParams epi_heads(const dit_model* m, const float* bias, void* d0, void
   e.tok_off = tok_off;
   e.rope_mask = m->rope ? rope_mask : 0;
   e.rope = m->rope;
+  if (m->rope) {
+    const int64_t n = (int64_t)m->rope_grid[0] * m->rope_grid[1] * m->rope_grid[2];
+    e.rope_inv = reinterpret_cast<const float*>(m->rope + n * (m->cfg.head_dim / 2));
+    e.rope_g1 = m->rope_grid[1];
+    e.rope_g2 = m->rope_grid[2];
+    e.rope_b0 = m->cfg.rope_axes[0] / 2;
+    e.rope_b1 = (m->cfg.rope_axes[0] + m->cfg.rope_axes[1]) / 2;
+  }
   return e;
 }
 static EpiParams epi_resid(const float* bias, float* x, const float* gate, int64_t gate_bstride, int rpb) {

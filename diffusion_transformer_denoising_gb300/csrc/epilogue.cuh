@@ -103,16 +103,47 @@ DIT_DEV void epilogue_values(const EpiParams& p, int64_t row, int col0, float (&
     const int c = (col0 - sec * p.D) % p.hd;
     const int t = (int)(row % p.rows_per_batch);
     if (p.rope && ((p.rope_mask >> sec) & 1)) {
-      // two (cos, sin) pairs per 16-byte load: c is a multiple of 4 channels
-      const float4* cs = reinterpret_cast<const float4*>(p.rope + (int64_t)t * (p.hd / 2) + c / 2);
+      if constexpr (kFast && NV % 8 == 0) {
+        // The angle pos * inv_freq is formed here instead of read from the
+        // (cos, sin) table: one lane per row would fetch 16 bytes from a
+        // different table row per load, a scattered stream that costs the
+        // epilogue more than the main loop.  The angle (at most a few
+        // hundred radians) is reduced to [-pi, pi] with a two-constant
+        // Cody-Waite step (2 pi = 6.28125 + 1.9353...e-3, the first part
+        // exact for small multiples), then passed to the fast sincos.
+        const int iw = t % p.rope_g2, th = t / p.rope_g2;
+        const float pos_t = (float)(th / p.rope_g1), pos_h = (float)(th % p.rope_g1), pos_w = (float)iw;
+        const float4* inv4 = reinterpret_cast<const float4*>(p.rope_inv + c / 2);
 #pragma unroll
-      for (int j = 0; j < NV; j += 4) {
-        const float4 r = __ldg(cs + j / 4);
-        const float a0 = v[j], b0 = v[j + 1], a1 = v[j + 2], b1 = v[j + 3];
-        v[j] = a0 * r.x - b0 * r.y;
-        v[j + 1] = a0 * r.y + b0 * r.x;
-        v[j + 2] = a1 * r.z - b1 * r.w;
-        v[j + 3] = a1 * r.w + b1 * r.z;
+        for (int j = 0; j < NV; j += 8) {
+          const float4 f4 = __ldg(inv4 + j / 8);
+          const float fr[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int pp = c / 2 + j / 2 + k;
+            const float pos = pp < p.rope_b0 ? pos_t : (pp < p.rope_b1 ? pos_h : pos_w);
+            const float ang = pos * fr[k];
+            const float n = rintf(ang * 0.159154943091895336f);
+            const float r = fmaf(-n, 1.93530717958647692e-3f, fmaf(-n, 6.28125f, ang));
+            float sn, cs;
+            __sincosf(r, &sn, &cs);
+            const float a0 = v[j + 2 * k], b0 = v[j + 2 * k + 1];
+            v[j + 2 * k] = a0 * cs - b0 * sn;
+            v[j + 2 * k + 1] = a0 * sn + b0 * cs;
+          }
+        }
+      } else {
+        // two (cos, sin) pairs per 16-byte load: c is a multiple of 4 channels
+        const float4* cs = reinterpret_cast<const float4*>(p.rope + (int64_t)t * (p.hd / 2) + c / 2);
+#pragma unroll
+        for (int j = 0; j < NV; j += 4) {
+          const float4 r = __ldg(cs + j / 4);
+          const float a0 = v[j], b0 = v[j + 1], a1 = v[j + 2], b1 = v[j + 3];
+          v[j] = a0 * r.x - b0 * r.y;
+          v[j + 1] = a0 * r.y + b0 * r.x;
+          v[j + 2] = a1 * r.z - b1 * r.w;
+          v[j + 3] = a1 * r.w + b1 * r.z;
+        }
       }
     }
   }

@@ -32,6 +32,11 @@ struct EpiParams {
   void* dst[3] = {nullptr, nullptr, nullptr};
   int D = 0, hd = 0, H = 0, seq_total = 0, tok_off = 0, rope_mask = 0;
   const float2* rope = nullptr;  // [rows_per_batch][hd / 2] (cos, sin)
+  // the same rotation evaluated in the kernel (bf16 tensor-core path): token
+  // t = (it * rope_g1 + ih) * rope_g2 + iw; channel pair p turns by
+  // pos * rope_inv[p], pos = it for p < rope_b0, ih for p < rope_b1, else iw
+  const float* rope_inv = nullptr;  // [hd / 2]
+  int rope_g1 = 0, rope_g2 = 0, rope_b0 = 0, rope_b1 = 0;
   // set by the tensor-core GEMM launcher when its output tensor maps are valid
   // (the epilogue then stores through shared memory with TMA)
   int tma = 0;
