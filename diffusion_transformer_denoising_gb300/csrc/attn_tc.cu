@@ -41,6 +41,19 @@
 // on a barrier needs an action of its own first, so a parity wait never
 // aliases.
 //
+// Persistent mode (short key ranges, e.g. cross-attention over 4 tiles): a
+// CTA per item would spend more on start-up (barrier set-up, tensor memory,
+// the first Q and K loads) than on the item's tiles, so one CTA per SM walks
+// every gridDim-th item.  Tiles are counted over all of a CTA's items,
+// so every ring runs on across item boundaries; the K loader refills the Q
+// buffer once the previous item's last S product has completed, and the
+// first PV product of an item (which overwrites O) waits until the softmax
+// warps have read out the previous item's O (o_free).
+//
+// Per-tile integer work on the softmax path is kept to compares and adds
+// (the ring slots and the rotated key tile advance incrementally): a
+// division or modulo by a runtime value there costs several percent.
+//
 // All waits are bounded (common.cuh); on a timeout the CTA flags *err, keeps
 // the softmax warps' named barriers matched, waits for its own copies and
 // MMAs, frees tensor memory and exits.
@@ -84,6 +97,11 @@ constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 // the row's tile sum stays below this (each p <= 2^14, far from overflow:
 // bf16 and fp32 keep their relative precision at any such magnitude).
 constexpr float SUM_LIMIT = 16384.0f;
+// Key ranges of at most this many tiles run on persistent CTAs (one per SM,
+// each walking several items so that one item's start overlaps the previous
+// one's end); longer ones use one CTA per item, whose fixed cost is small
+// next to the item.
+constexpr int PERSIST_MAX_KV_TILES = 64;
 
 // p = 2^(s*c - m) for the KPW scores of one row, packed to bf16 pairs; returns
 // the row sum of the (unrounded) p.  Masked keys (s = -inf) give exactly 0.
@@ -103,6 +121,7 @@ DIT_DEV float exp_tile(const float (&s)[NV], uint32_t (&pk)[NV / 2], float scale
 }
 }  // namespace fa
 
+template <bool PERSIST>
 __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, AttnArgs a, float scale_log2, int* err) {
@@ -121,19 +140,40 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   uint64_t* s_free = pv_done + PR;      // [2] softmax has copied S slot j % 2 (one arrival per softmax warp)
   uint64_t* p_ready = s_free + 2;       // [2] P slot j % 2 written (one arrival per softmax warp)
   uint64_t* drain = p_ready + 2;        // [2] final commit of each MMA thread
-  uint64_t* tile_ready = drain + 2;     // [SR] S_j and PV_{j-2} complete (two commits)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tile_ready + SR);
+  uint64_t* tile_ready = drain + 2;     // [SR] S_G and PV_{G-2} complete (two commits)
+  uint64_t* o_free = tile_ready + SR;   // O of an item read out (one arrival per softmax warp)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   __nv_bfloat16* xmax = reinterpret_cast<__nv_bfloat16*>(smem + XCH_OFF);
   float* xsum = reinterpret_cast<float*>(smem + XCH_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.z * a.H + blockIdx.y;
-  const int q0 = blockIdx.x * BQ;
+  const int nq = (a.Lq + BQ - 1) / BQ;
   const int nkv = (a.Lk + BKV - 1) / BKV;
-  // Each CTA walks the key tiles in a rotated order (the result does not
-  // depend on the order), so CTAs running together read different K/V tiles.
-  const int kv_rot = (int)(blockIdx.x % (unsigned)nkv);
+  // An item is one (query tile, batch*head).  A persistent CTA takes items
+  // blockIdx.x, + gridDim.x, ... (the grid never exceeds the item count);
+  // otherwise the CTA is the single item of its grid position.  Key tiles are
+  // counted over all items of the CTA (G), so every ring runs on across item
+  // boundaries.
+  int my_items = 1;
+  if constexpr (PERSIST) {
+    const int n_items = a.B * a.H * nq;
+    my_items = (n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  }
+  auto item_bh = [&](int k) -> int {
+    if constexpr (PERSIST) return ((int)blockIdx.x + k * (int)gridDim.x) / nq;
+    return (int)(blockIdx.z * a.H + blockIdx.y);
+  };
+  auto item_qt = [&](int k) -> int {
+    if constexpr (PERSIST) return ((int)blockIdx.x + k * (int)gridDim.x) % nq;
+    return (int)blockIdx.x;
+  };
+  // Each item walks the key tiles in a rotated order (the result does not
+  // depend on the order), so items running together read different K/V tiles.
+  auto item_rot = [&](int k) -> int {
+    if constexpr (PERSIST) return item_qt(k) % nkv;
+    return (int)(blockIdx.x % (unsigned)nkv);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -145,6 +185,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     // tiles 0 and 1 have no PV_{j-2}: its arrival is made up front
     mbar_arrive(&tile_ready[0]);
     mbar_arrive(&tile_ready[1 % SR]);
+    if (PERSIST) mbar_init(o_free, SM_WARPS);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_free[b], SM_WARPS);
       mbar_init(&p_ready[b], SM_WARPS);
@@ -164,44 +205,57 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  auto load_tile = [&](const CUtensorMap* tm, uint8_t* dst, uint64_t* bar, int tile) {
-    const int jt = (tile + kv_rot) % nkv;
-    mbar_arrive_expect_tx(bar, TILE_BYTES);
-    tma_load_3d(dst, tm, bar, 0, jt * BKV, bh);
-    tma_load_3d(dst + TILE_BYTES / 2, tm, bar, 64, jt * BKV, bh);
-  };
   if (warp == TMA_WARP || warp == VTMA_WARP) {
     // ------------------------------------------------ TMA producers (one thread each)
     // K and V run on separate threads: S runs about two tiles ahead of PV,
-    // so a K load must not queue behind the wait for a V stage.
+    // so a K load must not queue behind the wait for a V stage.  The K
+    // thread also loads each item's Q tile, once the previous item's last
+    // S product has read the buffer.
     if (lane == 0) {
       const bool is_k = warp == TMA_WARP;
+      const CUtensorMap* tm = is_k ? &tmK : &tmV;
       uint64_t* full = is_k ? kf : vf;
       uint64_t* consumed = is_k ? s_done : pv_done;
       const int nst = is_k ? KST : VST, ring = is_k ? SR : PR;
+      uint8_t* stages = smem + (is_k ? K_OFF : V_OFF);
       int issued[4] = {0, 0, 0, 0};
+      int q_issued = 0;
       bool ok = true;
-      if (is_k) {
-        mbar_arrive_expect_tx(q_full, TILE_BYTES);
-        tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, q0, bh);
-        tma_load_3d(smem + Q_OFF + TILE_BYTES / 2, &tmQ, q_full, 64, q0, bh);
-      }
-      for (int j = 0; j < nkv; ++j) {
-        // stage j % nst was last read by S_{j-nst} (K) or PV_{j-nst} (V)
-        if (j >= nst) {
-          const int c = j - nst;
-          ok = mbar_wait(&consumed[c % ring], (uint32_t)((c / ring) & 1), abort_flag, err, is_k ? 21 : 22);
+      int G = 0;
+      for (int k = 0; ok && k < my_items; ++k) {
+        const int bh = item_bh(k), qt = item_qt(k), kv_rot = item_rot(k);
+        if (is_k) {
+          if (PERSIST && k > 0) {
+            const int c = G - 1;  // the previous item's last S product
+            ok = mbar_wait(&s_done[c % SR], (uint32_t)((c / SR) & 1), abort_flag, err, 21);
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx(q_full, TILE_BYTES);
+          tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, qt * BQ, bh);
+          tma_load_3d(smem + Q_OFF + TILE_BYTES / 2, &tmQ, q_full, 64, qt * BQ, bh);
+          ++q_issued;
         }
-        if (!ok) break;
-        load_tile(is_k ? &tmK : &tmV, smem + (is_k ? K_OFF : V_OFF) + (j % nst) * TILE_BYTES, &full[j % nst], j);
-        ++issued[j % nst];
+        for (int j = 0; j < nkv; ++j, ++G) {
+          // stage G % nst was last read by S_{G-nst} (K) or PV_{G-nst} (V)
+          if (G >= nst) {
+            const int c = G - nst;
+            ok = mbar_wait(&consumed[c % ring], (uint32_t)((c / ring) & 1), abort_flag, err, is_k ? 21 : 22);
+            if (!ok) break;
+          }
+          const int jt = j + kv_rot < nkv ? j + kv_rot : j + kv_rot - nkv;
+          uint8_t* dst = stages + (G % nst) * TILE_BYTES;
+          mbar_arrive_expect_tx(&full[G % nst], TILE_BYTES);
+          tma_load_3d(dst, tm, &full[G % nst], 0, jt * BKV, bh);
+          tma_load_3d(dst + TILE_BYTES / 2, tm, &full[G % nst], 64, jt * BKV, bh);
+          ++issued[G % nst];
+        }
       }
       if (!ok) {
         // wind down: every copy this thread started lands before the CTA exits
         volatile int no_abort = 0;
-        if (is_k) mbar_wait(q_full, 0, &no_abort, nullptr, 0);
-        for (int s = 0; s < nst; ++s)
-          if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1), &no_abort, nullptr, 0);
+        if (q_issued > 0) mbar_wait(q_full, (uint32_t)((q_issued - 1) & 1), &no_abort, nullptr, 0);
+        for (int st = 0; st < nst; ++st)
+          if (issued[st] > 0) mbar_wait(&full[st], (uint32_t)((issued[st] - 1) & 1), &no_abort, nullptr, 0);
       }
     }
     __syncwarp();
@@ -210,22 +264,27 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     if (lane == 0) {
       const uint64_t q_desc = umma_desc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
       const uint64_t k_desc = umma_desc_sw128(smem_u32(smem + K_OFF), 16, 1024);
-      bool ok = mbar_wait(q_full, 0, abort_flag, err, 23);
-      for (int j = 0; ok && j < nkv; ++j) {
-        // slot j%2 is free once the softmax has copied S_{j-2}
-        if (j >= 2) ok = mbar_wait(&s_free[j & 1], (uint32_t)(((j - 2) >> 1) & 1), abort_flag, err, 24);
-        ok = ok && mbar_wait(&kf[j % KST], (uint32_t)((j / KST) & 1), abort_flag, err, 25);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t kd = umma_desc_add(k_desc, (j % KST) * TILE_BYTES);
-        const uint32_t d_tmem = tmem + TM_S + (j & 1) * 128;
+      bool ok = true;
+      int G = 0;
+      for (int k = 0; ok && k < my_items; ++k) {
+        // Q of item k
+        ok = mbar_wait(q_full, (uint32_t)(k & 1), abort_flag, err, 23);
+        for (int j = 0; ok && j < nkv; ++j, ++G) {
+          // slot G%2 is free once the softmax has copied S_{G-2}
+          if (G >= 2) ok = mbar_wait(&s_free[G & 1], (uint32_t)(((G - 2) >> 1) & 1), abort_flag, err, 24);
+          ok = ok && mbar_wait(&kf[G % KST], (uint32_t)((G / KST) & 1), abort_flag, err, 25);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t kd = umma_desc_add(k_desc, (G % KST) * TILE_BYTES);
+          const uint32_t d_tmem = tmem + TM_S + (G & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (TILE_BYTES / 2) + (kk & 3) * 32;
-          umma_ss(d_tmem, umma_desc_add(q_desc, off), umma_desc_add(kd, off), IDESC_S, kk != 0);
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (TILE_BYTES / 2) + (kk & 3) * 32;
+            umma_ss(d_tmem, umma_desc_add(q_desc, off), umma_desc_add(kd, off), IDESC_S, kk != 0);
+          }
+          umma_commit(&s_done[G % SR]);
+          umma_commit(&tile_ready[G % SR]);
         }
-        umma_commit(&s_done[j % SR]);
-        umma_commit(&tile_ready[j % SR]);
       }
       // all MMAs issued by this thread complete before tensor memory is released
       umma_commit(&drain[0]);
@@ -238,20 +297,26 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     if (lane == 0) {
       const uint64_t v_desc = umma_desc_sw128(smem_u32(smem + V_OFF), 16384, 1024);
       bool ok = true;
-      for (int j = 0; ok && j < nkv; ++j) {
-        ok = mbar_wait(&p_ready[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, err, 26) &&
-             mbar_wait(&vf[j % VST], (uint32_t)((j / VST) & 1), abort_flag, err, 27);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t vd = umma_desc_add(v_desc, (j % VST) * TILE_BYTES);
-        const uint32_t p_tmem = tmem + TM_P + (j & 1) * 64;
+      int G = 0;
+      for (int k = 0; ok && k < my_items; ++k) {
+        for (int j = 0; ok && j < nkv; ++j, ++G) {
+          ok = mbar_wait(&p_ready[G & 1], (uint32_t)((G >> 1) & 1), abort_flag, err, 26) &&
+               mbar_wait(&vf[G % VST], (uint32_t)((G / VST) & 1), abort_flag, err, 27);
+          // the first product of an item overwrites O: the previous item's O
+          // must have been read out
+          if (PERSIST && j == 0 && k > 0) ok = ok && mbar_wait(o_free, (uint32_t)((k - 1) & 1), abort_flag, err, 28);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t vd = umma_desc_add(v_desc, (G % VST) * TILE_BYTES);
+          const uint32_t p_tmem = tmem + TM_P + (G & 1) * 64;
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk) {
-          // keys 16kk..16kk+15: P columns 8kk.. (bf16 pairs), V rows 16kk.. (8-row groups 1 KB apart)
-          umma_ts(tmem + TM_O, p_tmem + kk * 8, umma_desc_add(vd, kk * 2048), IDESC_O, (j | kk) != 0);
+          for (int kk = 0; kk < BKV / 16; ++kk) {
+            // keys 16kk..16kk+15: P columns 8kk.. (bf16 pairs), V rows 16kk.. (8-row groups 1 KB apart)
+            umma_ts(tmem + TM_O, p_tmem + kk * 8, umma_desc_add(vd, kk * 2048), IDESC_O, (j | kk) != 0);
+          }
+          umma_commit(&pv_done[G % PR]);
+          umma_commit(&tile_ready[(G + 2) % SR]);
         }
-        umma_commit(&pv_done[j % PR]);
-        umma_commit(&tile_ready[(j + 2) % SR]);
       }
       umma_commit(&drain[1]);
       volatile int no_abort = 0;
@@ -264,23 +329,33 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const uint32_t o_col = tmem + TM_O + h * KPW + lane_off;  // this warp's O (and output) channels
     const int row = q * 32 + lane;
-    float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    int G = 0;
+    int tr_slot = 0;
+    uint32_t tr_phase = 0;  // tile_ready slot G % SR and its parity
+    for (int k = 0; k < my_items; ++k) {
+    const int kv_rot = item_rot(k);
+    int jt = kv_rot;  // key tile of the item's tile j
+    float m_used = -INFINITY, l = 0.f;
     // The loop never breaks: after a failed wait the warp skips the work but
     // still meets its quadrant partners at every named barrier.
-    for (int j = 0; j < nkv; ++j) {
+    for (int j = 0; j < nkv; ++j, ++G, jt = (jt + 1 == nkv) ? 0 : jt + 1) {
       float s[KPW];
       uint32_t pk[KPW / 2];
       float tsum = 0.f;
       bool big = true;  // a warp that skipped its work asks for the slow path
-      ok = ok && mbar_wait_warp(&tile_ready[j % SR], (uint32_t)((j / SR) & 1), abort_flag, err, 31);
+      ok = ok && mbar_wait_warp(&tile_ready[tr_slot], tr_phase, abort_flag, err, 31);
+      if (++tr_slot == SR) {
+        tr_slot = 0;
+        tr_phase ^= 1u;
+      }
       if (ok) {
         tc_fence_after();
         {
           uint32_t r[KPW];
 #pragma unroll
           for (int c = 0; c < KPW / 32; ++c)
-            tmem_ld32(tmem + TM_S + (j & 1) * 128 + h * KPW + c * 32 + lane_off,
+            tmem_ld32(tmem + TM_S + (G & 1) * 128 + h * KPW + c * 32 + lane_off,
                       *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
           tmem_ld_wait();
 #pragma unroll
@@ -289,8 +364,8 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
         // S slot j%2 may now take S_{j+2}
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[j & 1]);
-        const int valid = a.Lk - ((j + kv_rot) % nkv) * BKV - h * KPW;
+        if (lane == 0) mbar_arrive(&s_free[G & 1]);
+        const int valid = a.Lk - jt * BKV - h * KPW;
         if (valid < KPW) {
 #pragma unroll
           for (int i = 0; i < KPW; ++i)
@@ -331,7 +406,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
         const float m_new = row_big ? m_tile : m_used;
         if (j > 0) {
           // O (and l) move to the new reference; O must hold PV_{j-1} first
-          ok = mbar_wait_warp(&pv_done[(j - 1) % PR], (uint32_t)(((j - 1) / PR) & 1), abort_flag, err, 32);
+          ok = mbar_wait_warp(&pv_done[(G - 1) % PR], (uint32_t)(((G - 1) / PR) & 1), abort_flag, err, 32);
           if (!ok) continue;
           tc_fence_after();
           const float alpha = ex2_approx(m_used - m_new);  // 1 for rows kept
@@ -353,7 +428,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       }
       if (!ok) continue;
       l += tsum;
-      const uint32_t p_col = tmem + TM_P + (j & 1) * 64 + h * (KPW / 2) + lane_off;
+      const uint32_t p_col = tmem + TM_P + (G & 1) * 64 + h * (KPW / 2) + lane_off;
       if constexpr (KPW == 64)
         tmem_st32(p_col, *reinterpret_cast<const uint32_t(*)[32]>(pk));
       else
@@ -361,10 +436,10 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_ready[j & 1]);
+      if (lane == 0) mbar_arrive(&p_ready[G & 1]);
     }
     // O is final once PV_{nkv-1} has completed
-    ok = ok && mbar_wait_warp(&pv_done[(nkv - 1) % PR], (uint32_t)(((nkv - 1) / PR) & 1), abort_flag, err, 34);
+    ok = ok && mbar_wait_warp(&pv_done[(G - 1) % PR], (uint32_t)(((G - 1) / PR) & 1), abort_flag, err, 34);
     // the quadrant's partial row sums (same reference max) go through the
     // exchange buffer once every warp of the quadrant has read its maxima
     named_bar_sync(1 + q, 32 * NQ);
@@ -376,15 +451,15 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
 #pragma unroll
       for (int w = 0; w < NQ; ++w) lt += xsum[w * BQ + row];
       const float inv = 1.f / lt;
-      const int tok = q0 + row;
+      const int tok = item_qt(k) * BQ + row;
+      const int bh = item_bh(k), b = bh / a.H, head = bh - b * a.H;
       const int D = a.H * HD;
       __nv_bfloat16* out = nullptr;
       if (tok < a.Lq) {
         out = (tok < a.split)
-                  ? static_cast<__nv_bfloat16*>(a.o1) + ((int64_t)blockIdx.z * a.split + tok) * D
-                  : static_cast<__nv_bfloat16*>(a.o2) +
-                        ((int64_t)blockIdx.z * (a.Lq - a.split) + (tok - a.split)) * D;
-        out += blockIdx.y * HD + h * KPW;
+                  ? static_cast<__nv_bfloat16*>(a.o1) + ((int64_t)b * a.split + tok) * D
+                  : static_cast<__nv_bfloat16*>(a.o2) + ((int64_t)b * (a.Lq - a.split) + (tok - a.split)) * D;
+        out += head * HD + h * KPW;
       }
 #pragma unroll 1
       for (int c = 0; c < KPW / 32; ++c) {
@@ -398,6 +473,13 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
           store_chunk<__nv_bfloat16, 32>(out + c * 32, v);
         }
       }
+    }
+    if constexpr (PERSIST) {
+      // O may now take the next item's products
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+    }
     }
   }
   tc_fence_before();
@@ -421,15 +503,29 @@ cudaError_t attention_bf16_tc(const AttnArgs& a, int* err, cudaStream_t s) {
   if (!make_tmap_bf16(&tq, a.q, 3, dq, sq, box) || !make_tmap_bf16(&tk, a.k, 3, dk, sk, box) ||
       !make_tmap_bf16(&tv, a.v, 3, dk, sk, box))
     return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  static int num_sms = 0;
+  if (!num_sms) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    int dev = 0;
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
-  dim3 grid((a.Lq + BQ - 1) / BQ, a.H, a.B);
+  const int nq = (a.Lq + BQ - 1) / BQ, nkv = (a.Lk + BKV - 1) / BKV;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
-  attn_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tq, tk, tv, a, scale_log2, err);
+  if (nkv <= PERSIST_MAX_KV_TILES) {
+    // short key ranges: one CTA per SM walking every gridDim-th item, so each
+    // item's start overlaps the previous one's end
+    const int64_t items = (int64_t)a.B * a.H * nq;
+    if (items > INT32_MAX) return cudaErrorInvalidValue;
+    const int grid = (int)(items < num_sms ? items : num_sms);
+    attn_tc_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tq, tk, tv, a, scale_log2, err);
+  } else {
+    dim3 grid(nq, a.H, a.B);
+    attn_tc_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tq, tk, tv, a, scale_log2, err);
+  }
   return cudaGetLastError();
 }
 
