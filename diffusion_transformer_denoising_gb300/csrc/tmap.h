@@ -21,11 +21,13 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
-// Tensor of rank 2 or 3, dims innermost first, 128-byte swizzle,
-// out-of-bounds elements read as zero.  Returns false if the driver rejects it
-// (base not 16-byte aligned, stride not a multiple of 16 bytes, ...).
+// Tensor of rank 2 or 3, dims innermost first, 128-byte swizzle unless told
+// otherwise, out-of-bounds elements read as zero.  Returns false if the driver
+// rejects it (base not 16-byte aligned, stride not a multiple of 16 bytes, a
+// swizzled box row over 128 bytes, ...).
 inline bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank, const uint64_t* dims,
-                      const uint64_t* stride_bytes, const uint32_t* box) {
+                      const uint64_t* stride_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = tmap_encoder();
   if (!enc) return false;
   cuuint64_t d[3], st[2];
@@ -36,7 +38,7 @@ inline bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, 
   }
   for (int i = 0; i < rank - 1; ++i) st[i] = stride_bytes[i];
   CUresult r = enc(m, dt, rank, const_cast<void*>(base), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 inline bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
