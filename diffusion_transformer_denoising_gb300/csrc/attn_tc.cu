@@ -344,6 +344,8 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       uint32_t pk[KPW / 2];
       float tsum = 0.f;
       bool big = true;  // a warp that skipped its work asks for the slow path
+      bool p_stored = false;
+      const uint32_t p_col = tmem + TM_P + (G & 1) * 64 + h * (KPW / 2) + lane_off;
       ok = ok && mbar_wait_warp(&tile_ready[tr_slot], tr_phase, abort_flag, err, 31);
       if (++tr_slot == SR) {
         tr_slot = 0;
@@ -377,6 +379,14 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
         if (j > 0) {
           tsum = exp_tile(s, pk, scale_log2, m_used);
           big = !(tsum <= SUM_LIMIT);
+          // P_j goes to tensor memory now, while the quadrant agrees on the
+          // path below (the store's latency overlaps the barrier); a slow
+          // path stores it again before P_j is signalled
+          if constexpr (KPW == 64)
+            tmem_st32(p_col, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+          else
+            tmem_st16(p_col, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+          p_stored = true;
         }
       }
       // one barrier of the quadrant's warps that ORs their flags: all of them
@@ -425,19 +435,23 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
           m_used = m_new;
           tsum = exp_tile(s, pk, scale_log2, m_used);
         }
+        if (p_stored) tmem_st_wait();  // the early store lands before it is replaced
+        p_stored = false;
       }
       if (!ok) continue;
       l += tsum;
-      const uint32_t p_col = tmem + TM_P + (G & 1) * 64 + h * (KPW / 2) + lane_off;
-      if constexpr (KPW == 64)
-        tmem_st32(p_col, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-      else
-        tmem_st16(p_col, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+      if (!p_stored) {
+        if constexpr (KPW == 64)
+          tmem_st32(p_col, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+        else
+          tmem_st16(p_col, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_ready[G & 1]);
     }
+    tmem_st_wait();  // a P store left in flight by a failed wait lands before tensor memory is reused
     // O is final once PV_{nkv-1} has completed
     ok = ok && mbar_wait_warp(&pv_done[(G - 1) % PR], (uint32_t)(((G - 1) / PR) & 1), abort_flag, err, 34);
     // the quadrant's partial row sums (same reference max) go through the
