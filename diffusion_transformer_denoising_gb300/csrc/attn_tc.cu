@@ -103,6 +103,25 @@ constexpr float SUM_LIMIT = 16384.0f;
 // next to the item.
 constexpr int PERSIST_MAX_KV_TILES = 64;
 
+// tcgen05.ld of 64 columns (one instruction) straight into float registers
+DIT_DEV void tmem_ld64f(uint32_t taddr, float (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7]),
+        "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15]),
+        "=f"(r[16]), "=f"(r[17]), "=f"(r[18]), "=f"(r[19]), "=f"(r[20]), "=f"(r[21]), "=f"(r[22]), "=f"(r[23]),
+        "=f"(r[24]), "=f"(r[25]), "=f"(r[26]), "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31]),
+        "=f"(r[32]), "=f"(r[33]), "=f"(r[34]), "=f"(r[35]), "=f"(r[36]), "=f"(r[37]), "=f"(r[38]), "=f"(r[39]),
+        "=f"(r[40]), "=f"(r[41]), "=f"(r[42]), "=f"(r[43]), "=f"(r[44]), "=f"(r[45]), "=f"(r[46]), "=f"(r[47]),
+        "=f"(r[48]), "=f"(r[49]), "=f"(r[50]), "=f"(r[51]), "=f"(r[52]), "=f"(r[53]), "=f"(r[54]), "=f"(r[55]),
+        "=f"(r[56]), "=f"(r[57]), "=f"(r[58]), "=f"(r[59]), "=f"(r[60]), "=f"(r[61]), "=f"(r[62]), "=f"(r[63])
+      : "r"(taddr));
+}
+
 // p = 2^(s*c - m) for the KPW scores of one row, packed to bf16 pairs; returns
 // the row sum of the (unrounded) p.  Masked keys (s = -inf) give exactly 0.
 template <int NV>
@@ -150,6 +169,9 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = (a.Lq + BQ - 1) / BQ;
   const int nkv = (a.Lk + BKV - 1) / BKV;
+  // the key tile that has fewer than BKV keys, if any (its masked columns
+  // read -inf)
+  const int partial_jt = (a.Lk % BKV) ? nkv - 1 : -1;
   // An item is one (query tile, batch*head).  A persistent CTA takes items
   // blockIdx.x, + gridDim.x, ... (the grid never exceeds the item count);
   // otherwise the CTA is the single item of its grid position.  Key tiles are
@@ -354,21 +376,17 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       if (ok) {
         tc_fence_after();
         {
-          uint32_t r[KPW];
-#pragma unroll
-          for (int c = 0; c < KPW / 32; ++c)
-            tmem_ld32(tmem + TM_S + (G & 1) * 128 + h * KPW + c * 32 + lane_off,
-                      *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+          static_assert(KPW == 64, "one 64-column load per tile");
+          tmem_ld64f(tmem + TM_S + (G & 1) * 128 + h * KPW + lane_off, s);
           tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < KPW; ++i) s[i] = __uint_as_float(r[i]);
         }
         // S slot j%2 may now take S_{j+2}
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[G & 1]);
-        const int valid = a.Lk - jt * BKV - h * KPW;
-        if (valid < KPW) {
+        // only the last key tile can be partial
+        if (jt == partial_jt) {
+          const int valid = a.Lk - jt * BKV - h * KPW;
 #pragma unroll
           for (int i = 0; i < KPW; ++i)
             if (i >= valid) s[i] = -INFINITY;
