@@ -50,11 +50,11 @@ WORKLOADS = {
 # valid only for the exact kernel source it was captured on.
 TRAFFIC = {
     # kernel source file -> (sha256 prefix of the source, workload, bytes per launch).
-    # attn_tc.cu: dram__bytes_read.sum + dram__bytes_write.sum = 387.8 MB for one
+    # attn_tc.cu: dram__bytes_read.sum + dram__bytes_write.sum = 387.9 MB for one
     # batch-1 video self-attention launch (profiles/attn_tc_video_block.md),
     # scaled x2 to the batch-2 launch the step runs (traffic grows with the
     # number of query rows).
-    "attn_tc.cu": ("951d41b875e50f50", "video", 2 * 387.8e6),
+    "attn_tc.cu": ("1f4735d2c107031b", "video", 2 * 387.9e6),
 }
 
 
