@@ -511,6 +511,42 @@ static dit_status do_gemm(dit_model* m, int kind, const void* A, int64_t M, int 
   return DIT_OK;
 }
 
+// Two GEMMs with the same N and K (the image and condition streams of a
+// dual-stream block): one launch on the tensor-core path, two on the fp32 path.
+static dit_status do_gemm_pair(dit_model* m, int kind, const void* A0, int64_t M0, const void* W0, const EpiParams& ep0,
+                               const void* A1, int64_t M1, const void* W1, const EpiParams& ep1, int K, int N,
+                               cudaStream_t s) {
+  GemmArgs g[2];
+  const void* A[2] = {A0, A1};
+  const void* W[2] = {W0, W1};
+  const int64_t M[2] = {M0, M1};
+  const EpiParams* ep[2] = {&ep0, &ep1};
+  for (int i = 0; i < 2; ++i) {
+    g[i].A = A[i];
+    g[i].M = M[i];
+    g[i].K = K;
+    g[i].lda = K;
+    g[i].W = W[i];
+    g[i].N = N;
+    g[i].epi = *ep[i];
+    g[i].epi.M = (int)M[i];
+    g[i].epi.N = N;
+  }
+  cudaError_t e = cudaSuccess;
+  if (m->bf16) {
+    Launch l_(m, kind, 1, s);
+    e = gemm_bf16_tc_pair(g[0], g[1], m->d_err, m->num_sms, s);
+  } else {
+    Launch l_(m, kind, 2, s);
+    e = gemm_f32(g[0], s);
+    if (e == cudaSuccess) e = gemm_f32(g[1], s);
+  }
+  if (e != cudaSuccess)
+    return fail(DIT_ERR_CUDA, "GEMM pair launch (M=%lld+%lld N=%d K=%d) failed: %s", (long long)M0, (long long)M1, N, K,
+                cudaGetErrorString(e));
+  return DIT_OK;
+}
+
 static dit_status do_attn(dit_model* m, int kind, const void* q, const void* k, const void* v, int B, int Lq, int Lk,
                           void* o1, void* o2, int split, cudaStream_t s) {
   AttnArgs a;
@@ -595,6 +631,8 @@ struct BlockBufs {
   void* cond_act;  // [B, L, Dc] act (cross mode, bf16 copy of the condition)
   void* kc;        // [B, H, L, hd] act (cross mode, this block's keys)
   void* vc;
+  void* hc;        // [B, L, D] act (joint: condition-stream LN output)
+  void* gc;        // [B, L, F] act (joint: condition-stream MLP hidden)
 };
 
 static size_t block_ws_bytes(const dit_model* m, int B, int N, int L) {
@@ -612,6 +650,10 @@ static size_t block_ws_bytes(const dit_model* m, int B, int N, int L) {
   add((int64_t)B * L * c.cond_dim, a);     // cond_act
   add((int64_t)B * L * c.hidden, a);       // kc
   add((int64_t)B * L * c.hidden, a);       // vc
+  if (c.cond_mode == DIT_COND_JOINT) {
+    add((int64_t)B * L * c.hidden, a);     // hc
+    add((int64_t)B * L * c.mlp, a);        // gc
+  }
   return t;
 }
 
@@ -631,6 +673,11 @@ static BlockBufs carve_block(const dit_model* m, Workspace& w, int B, int N, int
   b.cond_act = w.take((size_t)B * L * c.cond_dim * a);
   b.kc = w.take((size_t)B * L * c.hidden * a);
   b.vc = w.take((size_t)B * L * c.hidden * a);
+  b.hc = b.gc = nullptr;
+  if (c.cond_mode == DIT_COND_JOINT) {
+    b.hc = w.take((size_t)B * L * c.hidden * a);
+    b.gc = w.take((size_t)B * L * c.mlp * a);
+  }
   return b;
 }
 
@@ -677,31 +724,51 @@ static dit_status run_block(dit_model* m, int blk, float* x, float* xc, const fl
                     epi_resid(m->V(m->blk(blk, "mlp.fc2.bias")), x, mod + 5 * D, mod_bstride, N), s));
     return DIT_OK;
   }
-  // joint (dual-stream) block: sequence [condition; image]
+  // joint (dual-stream) block: sequence [condition; image].  The two streams'
+  // GEMMs of equal shape run as one launch (image rows first, condition rows
+  // after), so the condition stream's 1024 rows fill the image GEMM's last wave.
   const int S = L + N;
   const int64_t R = (int64_t)B * N, Rc = (int64_t)B * L;
-  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(xc, Rc, D, L, modc + 0 * D, modc + 1 * D, mod_bstride, eps, bb.h, bf, s));
-  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_QKV, bb.h, Rc, D, D, m->W(m->blk(blk, "ctx.attn.qkv.weight")), 3 * D,
-                  epi_heads(m, m->V(m->blk(blk, "ctx.attn.qkv.bias")), bb.q, bb.k, bb.v, L, S, 0, 0), s));
+  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(xc, Rc, D, L, modc + 0 * D, modc + 1 * D, mod_bstride, eps, bb.hc, bf, s));
   LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, bf, s));
-  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_QKV, bb.h, R, D, D, m->W(m->blk(blk, "attn.qkv.weight")), 3 * D,
-                  epi_heads(m, m->V(m->blk(blk, "attn.qkv.bias")), bb.q, bb.k, bb.v, N, S, L, 0x3), s));
+  DIT_TRY(do_gemm_pair(m, DIT_KERNEL_GEMM_QKV,
+                       bb.h, R, m->W(m->blk(blk, "attn.qkv.weight")),
+                       epi_heads(m, m->V(m->blk(blk, "attn.qkv.bias")), bb.q, bb.k, bb.v, N, S, L, 0x3),
+                       bb.hc, Rc, m->W(m->blk(blk, "ctx.attn.qkv.weight")),
+                       epi_heads(m, m->V(m->blk(blk, "ctx.attn.qkv.bias")), bb.q, bb.k, bb.v, L, S, 0, 0),
+                       D, 3 * D, s));
   DIT_TRY(do_attn(m, DIT_KERNEL_ATTN_SELF, bb.q, bb.k, bb.v, B, S, S, bb.ac, bb.a, L, s));
-  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, m->W(m->blk(blk, "attn.out.weight")), D,
-                  epi_resid(m->V(m->blk(blk, "attn.out.bias")), x, mod + 2 * D, mod_bstride, N), s));
+  if (!ctx_out_needed) {
+    // last block: the condition stream's output is never read
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, m->W(m->blk(blk, "attn.out.weight")), D,
+                    epi_resid(m->V(m->blk(blk, "attn.out.bias")), x, mod + 2 * D, mod_bstride, N), s));
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, s));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN1, bb.h, R, D, D, m->W(m->blk(blk, "mlp.fc1.weight")), F,
+                    epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F), s));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN2, bb.g, R, F, F, m->W(m->blk(blk, "mlp.fc2.weight")), D,
+                    epi_resid(m->V(m->blk(blk, "mlp.fc2.bias")), x, mod + 5 * D, mod_bstride, N), s));
+    return DIT_OK;
+  }
+  DIT_TRY(do_gemm_pair(m, DIT_KERNEL_GEMM_OUT,
+                       bb.a, R, m->W(m->blk(blk, "attn.out.weight")),
+                       epi_resid(m->V(m->blk(blk, "attn.out.bias")), x, mod + 2 * D, mod_bstride, N),
+                       bb.ac, Rc, m->W(m->blk(blk, "ctx.attn.out.weight")),
+                       epi_resid(m->V(m->blk(blk, "ctx.attn.out.bias")), xc, modc + 2 * D, mod_bstride, L),
+                       D, D, s));
   LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, s));
-  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN1, bb.h, R, D, D, m->W(m->blk(blk, "mlp.fc1.weight")), F,
-                  epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F), s));
-  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN2, bb.g, R, F, F, m->W(m->blk(blk, "mlp.fc2.weight")), D,
-                  epi_resid(m->V(m->blk(blk, "mlp.fc2.bias")), x, mod + 5 * D, mod_bstride, N), s));
-  if (!ctx_out_needed) return DIT_OK;
-  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.ac, Rc, D, D, m->W(m->blk(blk, "ctx.attn.out.weight")), D,
-                  epi_resid(m->V(m->blk(blk, "ctx.attn.out.bias")), xc, modc + 2 * D, mod_bstride, L), s));
-  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(xc, Rc, D, L, modc + 3 * D, modc + 4 * D, mod_bstride, eps, bb.h, bf, s));
-  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN1, bb.h, Rc, D, D, m->W(m->blk(blk, "ctx.mlp.fc1.weight")), F,
-                  epi_store(EPI_GELU, m->V(m->blk(blk, "ctx.mlp.fc1.bias")), bb.g, F), s));
-  DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN2, bb.g, Rc, F, F, m->W(m->blk(blk, "ctx.mlp.fc2.weight")), D,
-                  epi_resid(m->V(m->blk(blk, "ctx.mlp.fc2.bias")), xc, modc + 5 * D, mod_bstride, L), s));
+  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(xc, Rc, D, L, modc + 3 * D, modc + 4 * D, mod_bstride, eps, bb.hc, bf, s));
+  DIT_TRY(do_gemm_pair(m, DIT_KERNEL_GEMM_FFN1,
+                       bb.h, R, m->W(m->blk(blk, "mlp.fc1.weight")),
+                       epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F),
+                       bb.hc, Rc, m->W(m->blk(blk, "ctx.mlp.fc1.weight")),
+                       epi_store(EPI_GELU, m->V(m->blk(blk, "ctx.mlp.fc1.bias")), bb.gc, F),
+                       D, F, s));
+  DIT_TRY(do_gemm_pair(m, DIT_KERNEL_GEMM_FFN2,
+                       bb.g, R, m->W(m->blk(blk, "mlp.fc2.weight")),
+                       epi_resid(m->V(m->blk(blk, "mlp.fc2.bias")), x, mod + 5 * D, mod_bstride, N),
+                       bb.gc, Rc, m->W(m->blk(blk, "ctx.mlp.fc2.weight")),
+                       epi_resid(m->V(m->blk(blk, "ctx.mlp.fc2.bias")), xc, modc + 5 * D, mod_bstride, L),
+                       F, D, s));
   return DIT_OK;
 }
 

@@ -59,6 +59,31 @@ struct EpiMaps {
   CUtensorMap m[3];
 };
 
+// The problems of one launch: NP GEMMs with the same N and K, each with its
+// own operands, row count and epilogue.  Their tile lists run back to back
+// (problem 0 first), so the tiles of a small problem fill the last wave of a
+// large one instead of running as a short launch of their own (the two
+// streams of a dual-stream block: 8192 image rows and 1024 condition rows).
+template <int NP>
+struct GemmBatch {
+  CUtensorMap tmA[NP];
+  CUtensorMap tmB[NP];
+  EpiMaps maps[NP];
+  EpiParams ep[NP];
+  int64_t M[NP];
+  int tile_end[NP];  // end (exclusive) of problem p's tiles in the launch's tile list
+};
+
+// Problem of a launch-wide tile index; *t = the tile's index within it.
+template <int NP>
+DIT_DEV int locate_tile(const GemmBatch<NP>& P, int tile, int* t) {
+  int p = 0;
+#pragma unroll
+  for (int i = 0; i + 1 < NP; ++i) p += tile >= P.tile_end[i] ? 1 : 0;
+  *t = p ? tile - P.tile_end[p - 1] : tile;
+  return p;
+}
+
 // Drain one accumulator tile through shared memory and TMA.  UW = columns per
 // 128-byte unit (64 bf16 or 32 fp32).  The warp owns rows row0..row0+31 and
 // units u = half, half+2, ...; it releases the accumulator (tempty) as soon
@@ -143,10 +168,9 @@ DIT_DEV void drain_tile_tma(const EpiParams& ep, const EpiMaps& maps, uint32_t t
   }
 }
 
-template <int BN>
+template <int BN, int NP>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int64_t M,
-                   int N, int K, EpiParams ep, const __grid_constant__ EpiMaps maps, int* err) {
+    gemm_tc_kernel(const __grid_constant__ GemmBatch<NP> P, int N, int K, int* err) {
   using C = TcGemmCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -173,8 +197,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      tma_prefetch_desc(&P.tmA[p]);
+      tma_prefetch_desc(&P.tmB[p]);
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
@@ -182,10 +209,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int m_tiles = (int)((M + C::BM - 1) / C::BM);
   const int n_tiles = (N + BN - 1) / BN;
   const int k_blocks = (K + C::BK - 1) / C::BK;
-  const int num_tiles = m_tiles * n_tiles;
+  const int num_tiles = P.tile_end[NP - 1];
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (one thread)
@@ -199,20 +225,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // streamed A rows (FFN2, whose A is the 1.2 GB MLP hidden, 3 % faster)
       const uint64_t w_policy = l2_policy_evict_last();
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int mb = tile / n_tiles, nb = tile - mb * n_tiles;
+        int t;
+        const int p = locate_tile(P, tile, &t);
+        const int mb = t / n_tiles, nb = t - mb * n_tiles;
+        const CUtensorMap* tmA = &P.tmA[p];
+        const CUtensorMap* tmB = &P.tmB[p];
         // Short main loops (K <= 2048): the residual rows this tile adds into
         // go to L2 now, so the epilogue's reduce-add a tile later does not
         // wait for DRAM (0.54 -> 0.51 ms for a video block's two
         // out-projections).  With long main loops the reduce has time to
         // spare and the prefetch only slowed the GEMM (FFN2 +3 %).
-        if (ep.kind == EPI_RESID && ep.tma && k_blocks <= 32) tma_prefetch_l2_2d(&maps.m[1], nb * BN, mb * C::BM);
+        if (P.ep[p].kind == EPI_RESID && P.ep[p].tma && k_blocks <= 32)
+          tma_prefetch_l2_2d(&P.maps[p].m[1], nb * BN, mb * C::BM);
         for (int kb = 0; kb < k_blocks; ++kb) {
           ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, 11);
           if (!ok) break;
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(sa, &tmA, &full[stage], kb * C::BK, mb * C::BM);
-          tma_load_2d_hint(sa + C::A_BYTES, &tmB, &full[stage], kb * C::BK, nb * BN, w_policy);
+          tma_load_2d(sa, tmA, &full[stage], kb * C::BK, mb * C::BM);
+          tma_load_2d_hint(sa + C::A_BYTES, tmB, &full[stage], kb * C::BK, nb * BN, w_policy);
           ++issued[stage];
           if (++stage == C::STAGES) {
             stage = 0;
@@ -273,7 +304,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int half = (warp - 2) / 4;
     const int row_in_tile = q * 32 + lane;
     uint8_t* stg = smem + C::STG_OFF + (warp - 2) * C::STG_BYTES;
-    const bool fp32_out = ep.kind == EPI_F32 || ep.kind == EPI_RESID;
     uint32_t local = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
@@ -281,14 +311,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       ok = mbar_wait_warp(&tfull[acc], aphase, abort_flag, err, 14);
       if (!ok) break;
       tc_fence_after();
-      const int mb = tile / n_tiles, nb = tile - mb * n_tiles;
+      int t;
+      const int p = locate_tile(P, tile, &t);
+      const int mb = t / n_tiles, nb = t - mb * n_tiles;
+      const EpiParams& ep = P.ep[p];
+      const int64_t M = P.M[p];
       const uint32_t tacc = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if (ep.tma) {
         const int64_t row0 = (int64_t)mb * C::BM + q * 32;
-        if (fp32_out)
-          drain_tile_tma<BN, 32>(ep, maps, tacc, row0, M, N, nb, half, stg, &tempty[acc]);
+        if (ep.kind == EPI_F32 || ep.kind == EPI_RESID)
+          drain_tile_tma<BN, 32>(ep, P.maps[p], tacc, row0, M, N, nb, half, stg, &tempty[acc]);
         else
-          drain_tile_tma<BN, 64>(ep, maps, tacc, row0, M, N, nb, half, stg, &tempty[acc]);
+          drain_tile_tma<BN, 64>(ep, P.maps[p], tacc, row0, M, N, nb, half, stg, &tempty[acc]);
         continue;
       }
       const int64_t row = (int64_t)mb * C::BM + row_in_tile;
@@ -366,40 +400,67 @@ static bool make_epi_maps(const EpiParams& e, int64_t M, int N, EpiMaps* maps) {
   return false;
 }
 
-template <int BN>
-static cudaError_t launch_gemm_tc(const GemmArgs& g, int* err, int num_sms, cudaStream_t s) {
+template <int BN, int NP>
+static cudaError_t launch_gemm_tc(const GemmArgs* gs, int* err, int num_sms, cudaStream_t s) {
   using C = TcGemmCfg<BN>;
-  CUtensorMap ta, tb;
-  const uint64_t da[2] = {(uint64_t)g.K, (uint64_t)g.M}, sa[1] = {(uint64_t)g.lda * 2};
-  const uint32_t ba[2] = {64, 128};
-  const uint64_t db[2] = {(uint64_t)g.K, (uint64_t)g.N}, sb[1] = {(uint64_t)g.K * 2};
-  const uint32_t bb[2] = {64, (uint32_t)BN};
-  if (!make_tmap_bf16(&ta, g.A, 2, da, sa, ba) || !make_tmap_bf16(&tb, g.W, 2, db, sb, bb))
-    return cudaErrorInvalidValue;
-  EpiParams ep = g.epi;
-  EpiMaps maps;
-  ep.tma = make_epi_maps(ep, g.M, g.N, &maps) ? 1 : 0;
+  GemmBatch<NP> P{};
+  const int n_tiles = (gs[0].N + BN - 1) / BN;
+  int tiles = 0;
+  for (int p = 0; p < NP; ++p) {
+    const GemmArgs& g = gs[p];
+    P.ep[p] = g.epi;
+    P.M[p] = g.M;
+    if (g.M > 0) {
+      const uint64_t da[2] = {(uint64_t)g.K, (uint64_t)g.M}, sa[1] = {(uint64_t)g.lda * 2};
+      const uint32_t ba[2] = {64, 128};
+      const uint64_t db[2] = {(uint64_t)g.K, (uint64_t)g.N}, sb[1] = {(uint64_t)g.K * 2};
+      const uint32_t bb[2] = {64, (uint32_t)BN};
+      if (!make_tmap_bf16(&P.tmA[p], g.A, 2, da, sa, ba) || !make_tmap_bf16(&P.tmB[p], g.W, 2, db, sb, bb))
+        return cudaErrorInvalidValue;
+      P.ep[p].tma = make_epi_maps(P.ep[p], g.M, g.N, &P.maps[p]) ? 1 : 0;
+    }
+    tiles += (int)((g.M + C::BM - 1) / C::BM) * n_tiles;
+    P.tile_end[p] = tiles;
+  }
+  if (tiles == 0) return cudaSuccess;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        cudaFuncSetAttribute(gemm_tc_kernel<BN, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int64_t tiles = ((g.M + 127) / 128) * ((g.N + BN - 1) / BN);
-  const int grid = (int)(tiles < num_sms ? tiles : num_sms);
-  gemm_tc_kernel<BN><<<grid, GEMM_THREADS, C::SMEM_BYTES, s>>>(ta, tb, g.M, g.N, g.K, ep, maps, err);
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  gemm_tc_kernel<BN, NP><<<grid, GEMM_THREADS, C::SMEM_BYTES, s>>>(P, gs[0].N, gs[0].K, err);
   return cudaGetLastError();
+}
+
+// alignment rules of the operand tensor maps: 16-byte rows and bases
+static bool operands_ok(const GemmArgs& g) {
+  return !((g.K % 8) || (g.lda % 8) || (reinterpret_cast<uintptr_t>(g.A) & 15) ||
+           (reinterpret_cast<uintptr_t>(g.W) & 15));
+}
+
+template <int NP>
+static cudaError_t launch_by_width(const GemmArgs* gs, int* err, int num_sms, cudaStream_t s) {
+  const int N = gs[0].N;
+  if (N % 256 == 0) return launch_gemm_tc<256, NP>(gs, err, num_sms, s);
+  if (N % 128 == 0) return launch_gemm_tc<128, NP>(gs, err, num_sms, s);
+  return launch_gemm_tc<64, NP>(gs, err, num_sms, s);
 }
 
 cudaError_t gemm_bf16_tc(const GemmArgs& g, int* err, int num_sms, cudaStream_t s) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
-  // alignment rules of the tensor maps: 16-byte rows and bases
-  if ((g.K % 8) || (g.lda % 8) || (reinterpret_cast<uintptr_t>(g.A) & 15) || (reinterpret_cast<uintptr_t>(g.W) & 15))
-    return cudaErrorInvalidValue;
-  if (g.N % 256 == 0) return launch_gemm_tc<256>(g, err, num_sms, s);
-  if (g.N % 128 == 0) return launch_gemm_tc<128>(g, err, num_sms, s);
-  return launch_gemm_tc<64>(g, err, num_sms, s);
+  if (!operands_ok(g)) return cudaErrorInvalidValue;
+  return launch_by_width<1>(&g, err, num_sms, s);
+}
+
+cudaError_t gemm_bf16_tc_pair(const GemmArgs& g0, const GemmArgs& g1, int* err, int num_sms, cudaStream_t s) {
+  if (g0.N != g1.N || g0.K != g1.K) return cudaErrorInvalidValue;
+  if (g0.N == 0 || (g0.M == 0 && g1.M == 0)) return cudaSuccess;
+  if ((g0.M > 0 && !operands_ok(g0)) || (g1.M > 0 && !operands_ok(g1))) return cudaErrorInvalidValue;
+  const GemmArgs gs[2] = {g0, g1};
+  return launch_by_width<2>(gs, err, num_sms, s);
 }
 
 }  // namespace dit

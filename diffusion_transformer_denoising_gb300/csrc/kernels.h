@@ -57,6 +57,9 @@ cudaError_t gemm_f32(const GemmArgs& g, cudaStream_t s);
 // bf16 tcgen05 GEMM (production precision); err = device error word for
 // bounded waits; num_sms = persistent grid size.
 cudaError_t gemm_bf16_tc(const GemmArgs& g, int* err, int num_sms, cudaStream_t s);
+// Two bf16 GEMMs with the same N and K in one persistent launch (g0's tiles
+// first, then g1's); either may have M = 0.
+cudaError_t gemm_bf16_tc_pair(const GemmArgs& g0, const GemmArgs& g1, int* err, int num_sms, cudaStream_t s);
 
 // ------------------------------------------------------------------ attention
 // Q [B, H, Lq, hd], K/V [B, H, Lk, hd] head-major; output token-major rows of
