@@ -210,6 +210,14 @@ DIT_DEV void tma_reduce_add_2d(const void* tmap, const void* src, int x, int y) 
                "r"(x), "r"(y), "r"(smem_u32(src))
                : "memory");
 }
+// Untiled bulk copy global -> shared, completing `bytes` on the mbarrier
+// (both addresses 16-byte aligned, bytes a multiple of 16).
+DIT_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 DIT_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 DIT_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 DIT_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }

@@ -703,21 +703,21 @@ static dit_status run_block(dit_model* m, int blk, float* x, float* xc, const fl
   if (c.cond_mode == DIT_COND_CROSS) {
     const int64_t R = (int64_t)B * N;
     // self-attention half
-    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, bf, s));
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, bf, m->d_err, m->num_sms, s));
     DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_QKV, bb.h, R, D, D, m->W(m->blk(blk, "attn.qkv.weight")), 3 * D,
                     epi_heads(m, m->V(m->blk(blk, "attn.qkv.bias")), bb.q, bb.k, bb.v, N, N, 0, 0x3), s));
     DIT_TRY(do_attn(m, DIT_KERNEL_ATTN_SELF, bb.q, bb.k, bb.v, B, N, N, bb.a, nullptr, N, s));
     DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, m->W(m->blk(blk, "attn.out.weight")), D,
                     epi_resid(m->V(m->blk(blk, "attn.out.bias")), x, mod + 2 * D, mod_bstride, N), s));
     // cross-attention half: plain LN, no rotation, ungated residual
-    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, nullptr, nullptr, 0, eps, bb.h, bf, s));
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, nullptr, nullptr, 0, eps, bb.h, bf, m->d_err, m->num_sms, s));
     DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_CROSS_Q, bb.h, R, D, D, m->W(m->blk(blk, "cross.q.weight")), D,
                     epi_heads(m, m->V(m->blk(blk, "cross.q.bias")), bb.q, nullptr, nullptr, N, N, 0, 0), s));
     DIT_TRY(do_attn(m, DIT_KERNEL_ATTN_CROSS, bb.q, kc, vc, B, N, L, bb.a, nullptr, N, s));
     DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, m->W(m->blk(blk, "cross.out.weight")), D,
                     epi_resid(m->V(m->blk(blk, "cross.out.bias")), x, nullptr, 0, N), s));
     // MLP half
-    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, s));
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, m->d_err, m->num_sms, s));
     DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN1, bb.h, R, D, D, m->W(m->blk(blk, "mlp.fc1.weight")), F,
                     epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F), s));
     DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN2, bb.g, R, F, F, m->W(m->blk(blk, "mlp.fc2.weight")), D,
@@ -729,8 +729,8 @@ static dit_status run_block(dit_model* m, int blk, float* x, float* xc, const fl
   // after), so the condition stream's 1024 rows fill the image GEMM's last wave.
   const int S = L + N;
   const int64_t R = (int64_t)B * N, Rc = (int64_t)B * L;
-  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(xc, Rc, D, L, modc + 0 * D, modc + 1 * D, mod_bstride, eps, bb.hc, bf, s));
-  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, bf, s));
+  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(xc, Rc, D, L, modc + 0 * D, modc + 1 * D, mod_bstride, eps, bb.hc, bf, m->d_err, m->num_sms, s));
+  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, bf, m->d_err, m->num_sms, s));
   DIT_TRY(do_gemm_pair(m, DIT_KERNEL_GEMM_QKV,
                        bb.h, R, m->W(m->blk(blk, "attn.qkv.weight")),
                        epi_heads(m, m->V(m->blk(blk, "attn.qkv.bias")), bb.q, bb.k, bb.v, N, S, L, 0x3),
@@ -742,7 +742,7 @@ static dit_status run_block(dit_model* m, int blk, float* x, float* xc, const fl
     // last block: the condition stream's output is never read
     DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, m->W(m->blk(blk, "attn.out.weight")), D,
                     epi_resid(m->V(m->blk(blk, "attn.out.bias")), x, mod + 2 * D, mod_bstride, N), s));
-    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, s));
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, m->d_err, m->num_sms, s));
     DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN1, bb.h, R, D, D, m->W(m->blk(blk, "mlp.fc1.weight")), F,
                     epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F), s));
     DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN2, bb.g, R, F, F, m->W(m->blk(blk, "mlp.fc2.weight")), D,
@@ -755,8 +755,8 @@ static dit_status run_block(dit_model* m, int blk, float* x, float* xc, const fl
                        bb.ac, Rc, m->W(m->blk(blk, "ctx.attn.out.weight")),
                        epi_resid(m->V(m->blk(blk, "ctx.attn.out.bias")), xc, modc + 2 * D, mod_bstride, L),
                        D, D, s));
-  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, s));
-  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(xc, Rc, D, L, modc + 3 * D, modc + 4 * D, mod_bstride, eps, bb.hc, bf, s));
+  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, m->d_err, m->num_sms, s));
+  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(xc, Rc, D, L, modc + 3 * D, modc + 4 * D, mod_bstride, eps, bb.hc, bf, m->d_err, m->num_sms, s));
   DIT_TRY(do_gemm_pair(m, DIT_KERNEL_GEMM_FFN1,
                        bb.h, R, m->W(m->blk(blk, "mlp.fc1.weight")),
                        epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F),
@@ -944,7 +944,7 @@ extern "C" dit_status dit_final_layer(dit_model* m, const float* x, const float*
   void* h = w.take((size_t)batch * N * D * m->act);
   float* vt = static_cast<float*>(w.take((size_t)batch * N * P * 4));
   LAUNCH(DIT_KERNEL_SMALL, 1, add_tables(mod, batch, D, 2, m->V("head.mod_table"), 1, headtab, s));
-  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, batch * N, D, (int)N, headtab, headtab + D, 2 * D, c.ln_eps, h, m->bf16, s));
+  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, batch * N, D, (int)N, headtab, headtab + D, 2 * D, c.ln_eps, h, m->bf16, m->d_err, m->num_sms, s));
   DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_EMBED, h, batch * N, D, D, m->W("head.weight"), P, epi_store(EPI_F32, m->V("head.bias"), vt, P), s));
   LAUNCH(DIT_KERNEL_SMALL, 1, unpatchify(vt, batch, c.in_channels, thw[0], thw[1], thw[2], c.patch[0], c.patch[1], c.patch[2], v, s));
   return DIT_OK;
@@ -1073,7 +1073,7 @@ extern "C" dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, 
                         tabs_c ? tabs_c + (size_t)blk * 6 * D : nullptr, 0, kc, vc, B, N, L, blk + 1 < c.depth, bb,
                         s));
     }
-    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, (int64_t)B * N, D, N, headtab, headtab + D, 0, c.ln_eps, bb.h, m->bf16, s));
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, (int64_t)B * N, D, N, headtab, headtab + D, 0, c.ln_eps, bb.h, m->bf16, m->d_err, m->num_sms, s));
     DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_EMBED, bb.h, (int64_t)B * N, D, D, m->W("head.weight"), P,
                     epi_store(EPI_F32, m->V("head.bias"), vt, P), s));
     const float dsig = (float)((double)sigmas[i + 1] - (double)sigmas[i]);

@@ -83,6 +83,183 @@ __global__ void __launch_bounds__(256) ln_mod_kernel(const float* __restrict__ x
   }
 }
 
+// bf16-output variant with the rows staged in shared memory by bulk copies.
+// One CTA per SM walks rows blockIdx.x, blockIdx.x + gridDim.x, ...; lane 0
+// of warp 0 keeps up to `stages` rows in flight (bulk copies into a ring of
+// row slots), and each of the LN_CONSUMERS other warps takes every
+// LN_CONSUMERS-th row of the CTA: it moves the row from its slot into
+// registers (the slot goes back to the copier at once), forms the mean and
+// the centred variance with warp shuffles and writes the modulated bf16 row.
+// The modulation of every batch element (shift and 1 + scale) is copied to
+// shared memory once per CTA.  Against the register-resident kernel above,
+// which issues a warp's loads only when the warp starts and re-reads 2 D
+// floats of modulation per row through L1, each SM keeps ~150-190 KB of reads
+// in flight while its warps compute.
+constexpr int LN_CONSUMERS = 8;
+constexpr int LN_STAGED_THREADS = 32 * (1 + LN_CONSUMERS);
+constexpr int LN_MOD_SMEM = 64 * 1024;   // modulation of all batch elements, at most
+constexpr int LN_RING_SMEM = 200 * 1024; // ring + modulation
+
+template <int NCH>
+__global__ void __launch_bounds__(LN_STAGED_THREADS, 1)
+    ln_mod_staged_kernel(const float* __restrict__ x, int rows, int D, int rpb, const float* __restrict__ shift,
+                         const float* __restrict__ scale, int64_t mbs, float eps, __nv_bfloat16* __restrict__ out,
+                         int stages, int nbatch, int* err) {
+  extern __shared__ __align__(16) uint8_t ln_smem[];
+  float* ring = reinterpret_cast<float*>(ln_smem);
+  float4* smod = reinterpret_cast<float4*>(ln_smem + (size_t)stages * D * 4);  // [nbatch][2][D/4]
+  const int n4 = D >> 2;
+  const size_t mod_f4 = shift ? (size_t)nbatch * 2 * n4 : 0;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smod + mod_f4);
+  uint64_t* empty = full + stages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + stages);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (shift) {
+    for (int i = threadIdx.x; i < nbatch * n4; i += blockDim.x) {
+      const int b = i / n4, c = i - b * n4;
+      const float4 a = __ldg(reinterpret_cast<const float4*>(scale + b * mbs) + c);
+      smod[(size_t)(2 * b) * n4 + c] = __ldg(reinterpret_cast<const float4*>(shift + b * mbs) + c);
+      smod[(size_t)(2 * b + 1) * n4 + c] = make_float4(1.f + a.x, 1.f + a.y, 1.f + a.z, 1.f + a.w);
+    }
+  }
+  __syncthreads();
+  const int nloc = rows > (int)blockIdx.x ? (rows - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  if (warp == 0) {
+    // ------------------------------------------------ copier (one thread)
+    if (lane == 0) {
+      const uint32_t row_bytes = (uint32_t)D * 4u;
+      int issued = 0, slot = 0;
+      uint32_t use = 0;
+      bool ok = true;
+      for (int k = 0; k < nloc; ++k) {
+        if (use > 0) {
+          ok = mbar_wait(&empty[slot], (use - 1) & 1, abort_flag, err, 41);
+          if (!ok) break;
+        }
+        const int64_t row = (int64_t)blockIdx.x + (int64_t)k * gridDim.x;
+        mbar_arrive_expect_tx(&full[slot], row_bytes);
+        bulk_load(ring + (size_t)slot * D, x + row * D, row_bytes, &full[slot]);
+        ++issued;
+        if (++slot == stages) {
+          slot = 0;
+          ++use;
+        }
+      }
+      if (!ok) {
+        // wind down: the last copy into each slot lands before the CTA exits
+        volatile int no_abort = 0;
+        for (int sl = 0; sl < stages && sl < issued; ++sl)
+          mbar_wait(&full[sl], (uint32_t)((issued - 1 - sl) / stages) & 1, &no_abort, nullptr, 0);
+      }
+    }
+    return;
+  }
+  // -------------------------------------------------- consumer warps
+  const float inv_d = 1.0f / (float)D;
+  for (int k = warp - 1; k < nloc; k += LN_CONSUMERS) {
+    const int slot = k % stages;
+    if (!mbar_wait_warp(&full[slot], (uint32_t)(k / stages) & 1, abort_flag, err, 42)) break;
+    const float4* src = reinterpret_cast<const float4*>(ring + (size_t)slot * D);
+    float4 v[NCH];
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const int c = lane + 32 * i;
+      if (c < n4) {
+        v[i] = src[c];
+        sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+      } else {
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    const float mean = warp_sum(sum) * inv_d;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const int c = lane + 32 * i;
+      if (c < n4) {
+        const float a = v[i].x - mean, b = v[i].y - mean, cc = v[i].z - mean, d = v[i].w - mean;
+        q += (a * a + b * b) + (cc * cc + d * d);
+      }
+    }
+    const float rstd = 1.0f / sqrtf(warp_sum(q) * inv_d + eps);
+    const int64_t row = (int64_t)blockIdx.x + (int64_t)k * gridDim.x;
+    const int bi = (int)(row / rpb);
+    const float4* sh4 = smod + (size_t)(2 * bi) * n4;
+    const float4* sc4 = sh4 + n4;
+    uint2* dst = reinterpret_cast<uint2*>(out + row * D);
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const int c = lane + 32 * i;
+      if (c >= n4) continue;
+      float4 y = make_float4((v[i].x - mean) * rstd, (v[i].y - mean) * rstd, (v[i].z - mean) * rstd,
+                             (v[i].w - mean) * rstd);
+      if (shift) {
+        const float4 a = sc4[c], b = sh4[c];
+        y.x = fmaf(y.x, a.x, b.x);
+        y.y = fmaf(y.y, a.y, b.y);
+        y.z = fmaf(y.z, a.z, b.z);
+        y.w = fmaf(y.w, a.w, b.w);
+      }
+      uint2 u;
+      u.x = pack_bf16x2(y.x, y.y);
+      u.y = pack_bf16x2(y.z, y.w);
+      dst[c] = u;
+    }
+  }
+}
+
+// Staged launch; false (nothing launched) when the modulation of all batch
+// elements does not fit its shared-memory budget.  Ring: what is left of
+// ~200 KB, at most 24 rows (144 KB of 1536-wide rows, more than one SM needs
+// in flight to cover DRAM latency at its share of the bandwidth), a multiple
+// of LN_CONSUMERS; one CTA per SM (fewer when there are fewer rows).
+template <int NCH>
+static bool ln_staged_launch(const float* x, int64_t rows, int D, int rpb, const float* sh, const float* sc,
+                             int64_t mbs, float eps, void* out, int* err, int num_sms, cudaStream_t s,
+                             cudaError_t* status) {
+  const int row_bytes = D * 4;
+  const int nbatch = (int)((rows + rpb - 1) / rpb);
+  const size_t mod_bytes = sh ? (size_t)nbatch * 2 * D * 4 : 0;
+  if (mod_bytes > (size_t)LN_MOD_SMEM) return false;
+  // The ring holds a multiple of LN_CONSUMERS rows, so slot s only ever
+  // holds rows of consumer warp s % LN_CONSUMERS, which takes its rows in
+  // order: a warp then never waits on a slot whose previous fill it has not
+  // consumed itself, and the one-bit phase parity of the slot barriers cannot
+  // alias (a warp running two fills ahead of the copier would otherwise pass
+  // a stale phase and arrive on the slot twice).
+  int stages = (int)((LN_RING_SMEM - mod_bytes) / row_bytes);
+  if (stages > 24) stages = 24;
+  stages -= stages % LN_CONSUMERS;
+  if (stages < LN_CONSUMERS) return false;
+  const size_t smem = (size_t)stages * row_bytes + mod_bytes + 2 * sizeof(uint64_t) * stages + 16;
+  static size_t attr_bytes = 0;
+  if (smem > attr_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(ln_mod_staged_kernel<NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) {
+      *status = e;
+      return true;
+    }
+    attr_bytes = smem;
+  }
+  const int grid = rows < num_sms ? (int)rows : num_sms;
+  ln_mod_staged_kernel<NCH><<<grid, LN_STAGED_THREADS, smem, s>>>(
+      x, (int)rows, D, rpb, sh, sc, mbs, eps, static_cast<__nv_bfloat16*>(out), stages, nbatch, err);
+  *status = cudaGetLastError();
+  return true;
+}
+
 template <int NCH>
 static cudaError_t ln_launch(const float* x, int64_t rows, int D, int rpb, const float* sh, const float* sc,
                              int64_t mbs, float eps, void* out, bool bf16, cudaStream_t s) {
@@ -95,10 +272,21 @@ static cudaError_t ln_launch(const float* x, int64_t rows, int D, int rpb, const
 }
 
 cudaError_t ln_modulate(const float* x, int64_t rows, int D, int rpb, const float* shift, const float* scale,
-                        int64_t mbs, float eps, void* out, bool out_bf16, cudaStream_t s) {
+                        int64_t mbs, float eps, void* out, bool out_bf16, int* err, int num_sms, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   if (D % 4) return cudaErrorInvalidValue;
   const int nch = (D / 4 + 31) / 32;
+  // bf16 output: rows staged through shared memory (the row start is 16-byte
+  // aligned when x is, since D % 4 == 0)
+  if (out_bf16 && rows < (int64_t)1 << 31 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+      (reinterpret_cast<uintptr_t>(out) & 7) == 0) {
+    cudaError_t st = cudaSuccess;
+    if (nch <= 4 && ln_staged_launch<4>(x, rows, D, rpb, shift, scale, mbs, eps, out, err, num_sms, s, &st)) return st;
+    if (nch > 4 && nch <= 12 && ln_staged_launch<12>(x, rows, D, rpb, shift, scale, mbs, eps, out, err, num_sms, s, &st))
+      return st;
+    if (nch > 12 && nch <= 24 && ln_staged_launch<24>(x, rows, D, rpb, shift, scale, mbs, eps, out, err, num_sms, s, &st))
+      return st;
+  }
   if (nch <= 1) return ln_launch<1>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
   if (nch <= 2) return ln_launch<2>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
   if (nch <= 4) return ln_launch<4>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);

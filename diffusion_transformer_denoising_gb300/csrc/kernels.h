@@ -78,10 +78,12 @@ cudaError_t attention_bf16_tc(const AttnArgs& a, int* err, cudaStream_t s);
 
 // ------------------------------------------------------------------ elementwise
 // h[r, :] = LN(x[r, :]) * (1 + scale[b]) + shift[b], b = r / rows_per_batch;
-// shift/scale NULL = plain LN.  Output bf16 (out_bf16) or fp32.
+// shift/scale NULL = plain LN.  Output bf16 (out_bf16) or fp32.  The bf16
+// path stages rows through shared memory on a grid of at most num_sms CTAs;
+// err = device error word for its bounded waits.
 cudaError_t ln_modulate(const float* x, int64_t rows, int D, int rows_per_batch, const float* shift,
-                        const float* scale, int64_t mod_bstride, float eps, void* out, bool out_bf16,
-                        cudaStream_t s);
+                        const float* scale, int64_t mod_bstride, float eps, void* out, bool out_bf16, int* err,
+                        int num_sms, cudaStream_t s);
 // Sinusoidal timestep embedding + 2-layer MLP: mod[b, 6D] for each t[b].
 // hidden_scratch: float[batch * D].
 // t_dev NULL: every batch element uses t0.
