@@ -547,6 +547,17 @@ static dit_status do_gemm_pair(dit_model* m, int kind, const void* A0, int64_t M
   return DIT_OK;
 }
 
+// The two streams' LayerNorms of a dual-stream block (one launch on the
+// staged bf16 path).
+static dit_status ln_pair(dit_model* m, const LnArgs& a, const LnArgs& b, cudaStream_t s) {
+  Launch l_(m, DIT_KERNEL_LN, 0, s);
+  int n = 0;
+  cudaError_t e = ln_modulate_pair(a, b, m->cfg.hidden, m->cfg.ln_eps, m->bf16, m->d_err, m->num_sms, s, &n);
+  l_.n = n;
+  if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "LayerNorm pair launch failed: %s", cudaGetErrorString(e));
+  return DIT_OK;
+}
+
 static dit_status do_attn(dit_model* m, int kind, const void* q, const void* k, const void* v, int B, int Lq, int Lk,
                           void* o1, void* o2, int split, cudaStream_t s) {
   AttnArgs a;
@@ -729,8 +740,8 @@ static dit_status run_block(dit_model* m, int blk, float* x, float* xc, const fl
   // after), so the condition stream's 1024 rows fill the image GEMM's last wave.
   const int S = L + N;
   const int64_t R = (int64_t)B * N, Rc = (int64_t)B * L;
-  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(xc, Rc, D, L, modc + 0 * D, modc + 1 * D, mod_bstride, eps, bb.hc, bf, m->d_err, m->num_sms, s));
-  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, bf, m->d_err, m->num_sms, s));
+  DIT_TRY(ln_pair(m, LnArgs{x, R, N, mod + 0 * D, mod + 1 * D, mod_bstride, bb.h},
+                  LnArgs{xc, Rc, L, modc + 0 * D, modc + 1 * D, mod_bstride, bb.hc}, s));
   DIT_TRY(do_gemm_pair(m, DIT_KERNEL_GEMM_QKV,
                        bb.h, R, m->W(m->blk(blk, "attn.qkv.weight")),
                        epi_heads(m, m->V(m->blk(blk, "attn.qkv.bias")), bb.q, bb.k, bb.v, N, S, L, 0x3),
@@ -755,8 +766,8 @@ static dit_status run_block(dit_model* m, int blk, float* x, float* xc, const fl
                        bb.ac, Rc, m->W(m->blk(blk, "ctx.attn.out.weight")),
                        epi_resid(m->V(m->blk(blk, "ctx.attn.out.bias")), xc, modc + 2 * D, mod_bstride, L),
                        D, D, s));
-  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, m->d_err, m->num_sms, s));
-  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(xc, Rc, D, L, modc + 3 * D, modc + 4 * D, mod_bstride, eps, bb.hc, bf, m->d_err, m->num_sms, s));
+  DIT_TRY(ln_pair(m, LnArgs{x, R, N, mod + 3 * D, mod + 4 * D, mod_bstride, bb.h},
+                  LnArgs{xc, Rc, L, modc + 3 * D, modc + 4 * D, mod_bstride, bb.hc}, s));
   DIT_TRY(do_gemm_pair(m, DIT_KERNEL_GEMM_FFN1,
                        bb.h, R, m->W(m->blk(blk, "mlp.fc1.weight")),
                        epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F),

@@ -93,27 +93,43 @@ __global__ void __launch_bounds__(256) ln_mod_kernel(const float* __restrict__ x
 // The modulation of every batch element (shift and 1 + scale) is copied to
 // shared memory once per CTA.  Against the register-resident kernel above,
 // which issues a warp's loads only when the warp starts and re-reads 2 D
-// floats of modulation per row through L1, each SM keeps ~150-190 KB of reads
-// in flight while its warps compute.
+// floats of modulation per row through L1, each SM keeps ~100-150 KB of reads
+// in flight while its warps compute.  One launch may normalise two row sets
+// of the same width (the image and condition streams of a dual-stream
+// block): their rows are numbered back to back.
 constexpr int LN_CONSUMERS = 8;
 constexpr int LN_STAGED_THREADS = 32 * (1 + LN_CONSUMERS);
-constexpr int LN_MOD_SMEM = 64 * 1024;   // modulation of all batch elements, at most
+constexpr int LN_MOD_SMEM = 96 * 1024;   // modulation of all batch elements, at most
 constexpr int LN_RING_SMEM = 200 * 1024; // ring + modulation
+
+struct LnSeg {
+  const float* x = nullptr;        // [rows, D]
+  __nv_bfloat16* out = nullptr;    // [rows, D]
+  const float* shift = nullptr;    // [batch] rows of stride mbs; NULL in both segments = plain LN
+  const float* scale = nullptr;
+  int64_t mbs = 0;
+  int rows = 0, rpb = 1;
+  int mod0 = 0;                    // first modulation entry of this segment in shared memory
+};
+struct LnSegs {
+  LnSeg s[2];
+  int nmod = 0;                    // modulation entries (batch elements of both segments)
+};
 
 template <int NCH>
 __global__ void __launch_bounds__(LN_STAGED_THREADS, 1)
-    ln_mod_staged_kernel(const float* __restrict__ x, int rows, int D, int rpb, const float* __restrict__ shift,
-                         const float* __restrict__ scale, int64_t mbs, float eps, __nv_bfloat16* __restrict__ out,
-                         int stages, int nbatch, int* err) {
+    ln_mod_staged_kernel(const __grid_constant__ LnSegs P, int D, float eps, int stages, int* err) {
   extern __shared__ __align__(16) uint8_t ln_smem[];
+  const bool modulate = P.s[0].shift != nullptr;
   float* ring = reinterpret_cast<float*>(ln_smem);
-  float4* smod = reinterpret_cast<float4*>(ln_smem + (size_t)stages * D * 4);  // [nbatch][2][D/4]
+  float4* smod = reinterpret_cast<float4*>(ln_smem + (size_t)stages * D * 4);  // [nmod][2][D/4]
   const int n4 = D >> 2;
-  const size_t mod_f4 = shift ? (size_t)nbatch * 2 * n4 : 0;
+  const size_t mod_f4 = modulate ? (size_t)P.nmod * 2 * n4 : 0;
   uint64_t* full = reinterpret_cast<uint64_t*>(smod + mod_f4);
   uint64_t* empty = full + stages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows0 = P.s[0].rows, rows = rows0 + P.s[1].rows;
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init(&full[i], 1);
@@ -122,12 +138,15 @@ __global__ void __launch_bounds__(LN_STAGED_THREADS, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (shift) {
-    for (int i = threadIdx.x; i < nbatch * n4; i += blockDim.x) {
-      const int b = i / n4, c = i - b * n4;
-      const float4 a = __ldg(reinterpret_cast<const float4*>(scale + b * mbs) + c);
-      smod[(size_t)(2 * b) * n4 + c] = __ldg(reinterpret_cast<const float4*>(shift + b * mbs) + c);
-      smod[(size_t)(2 * b + 1) * n4 + c] = make_float4(1.f + a.x, 1.f + a.y, 1.f + a.z, 1.f + a.w);
+  if (modulate) {
+    for (int i = threadIdx.x; i < P.nmod * n4; i += blockDim.x) {
+      const int e = i / n4, c = i - e * n4;
+      const int sg = e >= P.s[1].mod0 && P.s[1].rows > 0 ? 1 : 0;
+      const LnSeg& g = P.s[sg];
+      const int64_t b = e - g.mod0;
+      const float4 a = __ldg(reinterpret_cast<const float4*>(g.scale + b * g.mbs) + c);
+      smod[(size_t)(2 * e) * n4 + c] = __ldg(reinterpret_cast<const float4*>(g.shift + b * g.mbs) + c);
+      smod[(size_t)(2 * e + 1) * n4 + c] = make_float4(1.f + a.x, 1.f + a.y, 1.f + a.z, 1.f + a.w);
     }
   }
   __syncthreads();
@@ -144,9 +163,10 @@ __global__ void __launch_bounds__(LN_STAGED_THREADS, 1)
           ok = mbar_wait(&empty[slot], (use - 1) & 1, abort_flag, err, 41);
           if (!ok) break;
         }
-        const int64_t row = (int64_t)blockIdx.x + (int64_t)k * gridDim.x;
+        const int row = (int)blockIdx.x + k * (int)gridDim.x;
+        const float* src = row < rows0 ? P.s[0].x + (int64_t)row * D : P.s[1].x + (int64_t)(row - rows0) * D;
         mbar_arrive_expect_tx(&full[slot], row_bytes);
-        bulk_load(ring + (size_t)slot * D, x + row * D, row_bytes, &full[slot]);
+        bulk_load(ring + (size_t)slot * D, src, row_bytes, &full[slot]);
         ++issued;
         if (++slot == stages) {
           slot = 0;
@@ -193,18 +213,21 @@ __global__ void __launch_bounds__(LN_STAGED_THREADS, 1)
       }
     }
     const float rstd = 1.0f / sqrtf(warp_sum(q) * inv_d + eps);
-    const int64_t row = (int64_t)blockIdx.x + (int64_t)k * gridDim.x;
-    const int bi = (int)(row / rpb);
-    const float4* sh4 = smod + (size_t)(2 * bi) * n4;
+    const int row = (int)blockIdx.x + k * (int)gridDim.x;
+    const int sg = row < rows0 ? 0 : 1;
+    const int lr = row - sg * rows0;
+    const LnSeg& g = P.s[sg];
+    const int e = g.mod0 + lr / g.rpb;
+    const float4* sh4 = smod + (size_t)(2 * e) * n4;
     const float4* sc4 = sh4 + n4;
-    uint2* dst = reinterpret_cast<uint2*>(out + row * D);
+    uint2* dst = reinterpret_cast<uint2*>(g.out + (int64_t)lr * D);
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
       const int c = lane + 32 * i;
       if (c >= n4) continue;
       float4 y = make_float4((v[i].x - mean) * rstd, (v[i].y - mean) * rstd, (v[i].z - mean) * rstd,
                              (v[i].w - mean) * rstd);
-      if (shift) {
+      if (modulate) {
         const float4 a = sc4[c], b = sh4[c];
         y.x = fmaf(y.x, a.x, b.x);
         y.y = fmaf(y.y, a.y, b.y);
@@ -219,18 +242,22 @@ __global__ void __launch_bounds__(LN_STAGED_THREADS, 1)
   }
 }
 
-// Staged launch; false (nothing launched) when the modulation of all batch
-// elements does not fit its shared-memory budget.  Ring: what is left of
-// ~200 KB, at most 24 rows (144 KB of 1536-wide rows, more than one SM needs
-// in flight to cover DRAM latency at its share of the bandwidth), a multiple
-// of LN_CONSUMERS; one CTA per SM (fewer when there are fewer rows).
+// Staged launch over one or two segments; false (nothing launched) when the
+// modulation of all batch elements does not fit its shared-memory budget.
+// Ring: what is left of ~200 KB, at most 24 rows (144 KB of 1536-wide rows,
+// more than one SM needs in flight to cover DRAM latency at its share of the
+// bandwidth), a multiple of LN_CONSUMERS; one CTA per SM (fewer when there
+// are fewer rows).
 template <int NCH>
-static bool ln_staged_launch(const float* x, int64_t rows, int D, int rpb, const float* sh, const float* sc,
-                             int64_t mbs, float eps, void* out, int* err, int num_sms, cudaStream_t s,
-                             cudaError_t* status) {
+static bool ln_staged_launch(LnSegs P, int D, float eps, int* err, int num_sms, cudaStream_t s, cudaError_t* status) {
   const int row_bytes = D * 4;
-  const int nbatch = (int)((rows + rpb - 1) / rpb);
-  const size_t mod_bytes = sh ? (size_t)nbatch * 2 * D * 4 : 0;
+  int nmod = 0;
+  for (int i = 0; i < 2; ++i) {
+    P.s[i].mod0 = nmod;
+    if (P.s[i].rows > 0) nmod += (P.s[i].rows + P.s[i].rpb - 1) / P.s[i].rpb;
+  }
+  P.nmod = nmod;
+  const size_t mod_bytes = P.s[0].shift ? (size_t)nmod * 2 * D * 4 : 0;
   if (mod_bytes > (size_t)LN_MOD_SMEM) return false;
   // The ring holds a multiple of LN_CONSUMERS rows, so slot s only ever
   // holds rows of consumer warp s % LN_CONSUMERS, which takes its rows in
@@ -253,11 +280,40 @@ static bool ln_staged_launch(const float* x, int64_t rows, int D, int rpb, const
     }
     attr_bytes = smem;
   }
-  const int grid = rows < num_sms ? (int)rows : num_sms;
-  ln_mod_staged_kernel<NCH><<<grid, LN_STAGED_THREADS, smem, s>>>(
-      x, (int)rows, D, rpb, sh, sc, mbs, eps, static_cast<__nv_bfloat16*>(out), stages, nbatch, err);
+  const int rows = P.s[0].rows + P.s[1].rows;
+  const int grid = rows < num_sms ? rows : num_sms;
+  ln_mod_staged_kernel<NCH><<<grid, LN_STAGED_THREADS, smem, s>>>(P, D, eps, stages, err);
   *status = cudaGetLastError();
   return true;
+}
+
+// The staged kernel takes a segment whose x is 16-byte and out 8-byte aligned.
+static bool staged_ok(const LnArgs& a) {
+  return (reinterpret_cast<uintptr_t>(a.x) & 15) == 0 && (reinterpret_cast<uintptr_t>(a.out) & 7) == 0;
+}
+
+static bool ln_staged(const LnArgs* a, int nseg, int D, float eps, int* err, int num_sms, cudaStream_t s,
+                      cudaError_t* status) {
+  LnSegs P;
+  int64_t rows = 0;
+  for (int i = 0; i < nseg; ++i) {
+    if (!staged_ok(a[i]) || a[i].rpb <= 0) return false;
+    if (i > 0 && (a[i].shift == nullptr) != (a[0].shift == nullptr)) return false;
+    P.s[i].x = a[i].x;
+    P.s[i].out = static_cast<__nv_bfloat16*>(a[i].out);
+    P.s[i].shift = a[i].shift;
+    P.s[i].scale = a[i].scale;
+    P.s[i].mbs = a[i].mbs;
+    P.s[i].rows = (int)a[i].rows;
+    P.s[i].rpb = a[i].rpb;
+    rows += a[i].rows;
+  }
+  if (rows >= (int64_t)1 << 31) return false;
+  const int nch = (D / 4 + 31) / 32;
+  if (nch <= 4) return ln_staged_launch<4>(P, D, eps, err, num_sms, s, status);
+  if (nch <= 12) return ln_staged_launch<12>(P, D, eps, err, num_sms, s, status);
+  if (nch <= 24) return ln_staged_launch<24>(P, D, eps, err, num_sms, s, status);
+  return false;
 }
 
 template <int NCH>
@@ -275,18 +331,12 @@ cudaError_t ln_modulate(const float* x, int64_t rows, int D, int rpb, const floa
                         int64_t mbs, float eps, void* out, bool out_bf16, int* err, int num_sms, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   if (D % 4) return cudaErrorInvalidValue;
-  const int nch = (D / 4 + 31) / 32;
-  // bf16 output: rows staged through shared memory (the row start is 16-byte
-  // aligned when x is, since D % 4 == 0)
-  if (out_bf16 && rows < (int64_t)1 << 31 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
-      (reinterpret_cast<uintptr_t>(out) & 7) == 0) {
+  if (out_bf16) {
+    const LnArgs a{x, rows, rpb, shift, scale, mbs, out};
     cudaError_t st = cudaSuccess;
-    if (nch <= 4 && ln_staged_launch<4>(x, rows, D, rpb, shift, scale, mbs, eps, out, err, num_sms, s, &st)) return st;
-    if (nch > 4 && nch <= 12 && ln_staged_launch<12>(x, rows, D, rpb, shift, scale, mbs, eps, out, err, num_sms, s, &st))
-      return st;
-    if (nch > 12 && nch <= 24 && ln_staged_launch<24>(x, rows, D, rpb, shift, scale, mbs, eps, out, err, num_sms, s, &st))
-      return st;
+    if (ln_staged(&a, 1, D, eps, err, num_sms, s, &st)) return st;
   }
+  const int nch = (D / 4 + 31) / 32;
   if (nch <= 1) return ln_launch<1>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
   if (nch <= 2) return ln_launch<2>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
   if (nch <= 4) return ln_launch<4>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
@@ -296,6 +346,21 @@ cudaError_t ln_modulate(const float* x, int64_t rows, int D, int rpb, const floa
   if (nch <= 24) return ln_launch<24>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
   if (nch <= 32) return ln_launch<32>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t ln_modulate_pair(const LnArgs& a, const LnArgs& b, int D, float eps, bool out_bf16, int* err,
+                             int num_sms, cudaStream_t s, int* launches) {
+  if (D % 4) return cudaErrorInvalidValue;
+  *launches = 1;
+  if (out_bf16 && a.rows > 0 && b.rows > 0) {
+    const LnArgs ab[2] = {a, b};
+    cudaError_t st = cudaSuccess;
+    if (ln_staged(ab, 2, D, eps, err, num_sms, s, &st)) return st;
+  }
+  *launches = (a.rows > 0) + (b.rows > 0);
+  cudaError_t e = ln_modulate(a.x, a.rows, D, a.rpb, a.shift, a.scale, a.mbs, eps, a.out, out_bf16, err, num_sms, s);
+  if (e != cudaSuccess) return e;
+  return ln_modulate(b.x, b.rows, D, b.rpb, b.shift, b.scale, b.mbs, eps, b.out, out_bf16, err, num_sms, s);
 }
 
 // ---------------------------------------------------------------- timestep MLP

@@ -84,6 +84,22 @@ cudaError_t attention_bf16_tc(const AttnArgs& a, int* err, cudaStream_t s);
 cudaError_t ln_modulate(const float* x, int64_t rows, int D, int rows_per_batch, const float* shift,
                         const float* scale, int64_t mod_bstride, float eps, void* out, bool out_bf16, int* err,
                         int num_sms, cudaStream_t s);
+// One LayerNorm of a pair: x [rows, D] -> out, modulation of batch element
+// r / rpb at shift/scale + (r / rpb) * mbs (both NULL = plain LN).
+struct LnArgs {
+  const float* x;
+  int64_t rows;
+  int rpb;
+  const float* shift;
+  const float* scale;
+  int64_t mbs;
+  void* out;
+};
+// Two LayerNorms of the same width in one launch where the staged bf16 path
+// takes them (both modulated or both plain), else one launch each;
+// *launches = the number of kernels launched.
+cudaError_t ln_modulate_pair(const LnArgs& a, const LnArgs& b, int D, float eps, bool out_bf16, int* err,
+                             int num_sms, cudaStream_t s, int* launches);
 // Sinusoidal timestep embedding + 2-layer MLP: mod[b, 6D] for each t[b].
 // hidden_scratch: float[batch * D].
 // t_dev NULL: every batch element uses t0.
