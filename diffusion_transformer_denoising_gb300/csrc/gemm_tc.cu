@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0 && lane == 0) {
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
+      if (P.M[p] == 0) continue;  // no tiles, no tensor maps
       tma_prefetch_desc(&P.tmA[p]);
       tma_prefetch_desc(&P.tmB[p]);
     }
