@@ -535,16 +535,16 @@ cudaError_t attention_bf16_tc(const AttnArgs& a, int* err, cudaStream_t s) {
   if (!make_tmap_bf16(&tq, a.q, 3, dq, sq, box) || !make_tmap_bf16(&tk, a.k, 3, dk, sk, box) ||
       !make_tmap_bf16(&tv, a.v, 3, dk, sk, box))
     return cudaErrorInvalidValue;
-  static int num_sms = 0;
-  if (!num_sms) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    int dev = 0;
-    if (e == cudaSuccess) e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-  }
+  static SmemAttr attr_one, attr_persist;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(attn_tc_kernel<false>), SMEM_BYTES, attr_one);
+  if (e == cudaSuccess)
+    e = ensure_smem_attr(reinterpret_cast<const void*>(attn_tc_kernel<true>), SMEM_BYTES, attr_persist);
+  static int sms_of[kMaxDevices] = {};
+  int dev = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess && !sms_of[dev]) e = cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int num_sms = sms_of[dev];
   const int nq = (a.Lq + BQ - 1) / BQ, nkv = (a.Lk + BKV - 1) / BKV;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   if (nkv <= PERSIST_MAX_KV_TILES) {

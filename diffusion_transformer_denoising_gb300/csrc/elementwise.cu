@@ -5,6 +5,7 @@
 #include <math.h>
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace dit {
 
@@ -270,15 +271,11 @@ static bool ln_staged_launch(LnSegs P, int D, float eps, int* err, int num_sms, 
   stages -= stages % LN_CONSUMERS;
   if (stages < LN_CONSUMERS) return false;
   const size_t smem = (size_t)stages * row_bytes + mod_bytes + 2 * sizeof(uint64_t) * stages + 16;
-  static size_t attr_bytes = 0;
-  if (smem > attr_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(ln_mod_staged_kernel<NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) {
-      *status = e;
-      return true;
-    }
-    attr_bytes = smem;
+  static SmemAttr attr;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ln_mod_staged_kernel<NCH>), (int)smem, attr);
+  if (e != cudaSuccess) {
+    *status = e;
+    return true;
   }
   const int rows = P.s[0].rows + P.s[1].rows;
   const int grid = rows < num_sms ? rows : num_sms;

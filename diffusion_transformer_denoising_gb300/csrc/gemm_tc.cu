@@ -424,13 +424,9 @@ static cudaError_t launch_gemm_tc(const GemmArgs* gs, int* err, int num_sms, cud
     P.tile_end[p] = tiles;
   }
   if (tiles == 0) return cudaSuccess;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel<BN, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static SmemAttr attr;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(gemm_tc_kernel<BN, NP>), C::SMEM_BYTES, attr);
+  if (e != cudaSuccess) return e;
   const int grid = tiles < num_sms ? tiles : num_sms;
   gemm_tc_kernel<BN, NP><<<grid, GEMM_THREADS, C::SMEM_BYTES, s>>>(P, gs[0].N, gs[0].K, err);
   return cudaGetLastError();

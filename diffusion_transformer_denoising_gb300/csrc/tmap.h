@@ -8,6 +8,24 @@
 
 namespace dit {
 
+// Opt-in dynamic shared memory of a kernel, set once per device: the
+// attribute belongs to the device's context, so a process that drives
+// several GPUs sets it on each of them (on the current device).
+constexpr int kMaxDevices = 64;
+struct SmemAttr {
+  int bytes[kMaxDevices] = {};
+};
+inline cudaError_t ensure_smem_attr(const void* func, int bytes, SmemAttr& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (done.bytes[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.bytes[dev] = bytes;
+  return e;
+}
+
 inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
