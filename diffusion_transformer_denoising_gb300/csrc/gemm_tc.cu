@@ -71,8 +71,26 @@ struct GemmBatch {
   EpiMaps maps[NP];
   EpiParams ep[NP];
   int64_t M[NP];
+  int m_tiles[NP];
   int tile_end[NP];  // end (exclusive) of problem p's tiles in the launch's tile list
+  int group_n;       // n-tiles per column group (see tile_coords)
 };
+
+// Tile t of a problem with m_tiles row tiles -> (mb, nb).  Tiles run in
+// column groups of gn n-tiles (the last group narrower), N-fastest within a
+// group: the CTAs of a wave then read one group's W columns, which stay in L2
+// while the group streams A, instead of every W column of the layer (an image
+// FFN1 layer's W is 75 MB; in plain N-fastest order its launch read 1.27 GB
+// from DRAM for 0.21 GB of operands).  gn = n_tiles is plain N-fastest order.
+DIT_DEV void tile_coords(int t, int m_tiles, int n_tiles, int gn, int* mb, int* nb) {
+  const int per_group = m_tiles * gn;
+  const int g = t / per_group;
+  const int within = t - g * per_group;
+  const int rest = n_tiles - g * gn;
+  const int width = rest < gn ? rest : gn;
+  *mb = within / width;
+  *nb = g * gn + (within - *mb * width);
+}
 
 // Problem of a launch-wide tile index; *t = the tile's index within it.
 template <int NP>
@@ -226,9 +244,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // streamed A rows (FFN2, whose A is the 1.2 GB MLP hidden, 3 % faster)
       const uint64_t w_policy = l2_policy_evict_last();
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        int t;
+        int t, mb, nb;
         const int p = locate_tile(P, tile, &t);
-        const int mb = t / n_tiles, nb = t - mb * n_tiles;
+        tile_coords(t, P.m_tiles[p], n_tiles, P.group_n, &mb, &nb);
         const CUtensorMap* tmA = &P.tmA[p];
         const CUtensorMap* tmB = &P.tmB[p];
         // Short main loops (K <= 2048): the residual rows this tile adds into
@@ -312,9 +330,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       ok = mbar_wait_warp(&tfull[acc], aphase, abort_flag, err, 14);
       if (!ok) break;
       tc_fence_after();
-      int t;
+      int t, mb, nb;
       const int p = locate_tile(P, tile, &t);
-      const int mb = t / n_tiles, nb = t - mb * n_tiles;
+      tile_coords(t, P.m_tiles[p], n_tiles, P.group_n, &mb, &nb);
       const EpiParams& ep = P.ep[p];
       const int64_t M = P.M[p];
       const uint32_t tacc = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
@@ -420,9 +438,21 @@ static cudaError_t launch_gemm_tc(const GemmArgs* gs, int* err, int num_sms, cud
         return cudaErrorInvalidValue;
       P.ep[p].tma = make_epi_maps(P.ep[p], g.M, g.N, &P.maps[p]) ? 1 : 0;
     }
-    tiles += (int)((g.M + C::BM - 1) / C::BM) * n_tiles;
+    P.m_tiles[p] = (int)((g.M + C::BM - 1) / C::BM);
+    tiles += P.m_tiles[p] * n_tiles;
     P.tile_end[p] = tiles;
   }
+  // Column groups whose W slice is at most ~40 MB (every W of the video
+  // layers fits whole: plain N-fastest order there).  Each group streams A
+  // once more, so groups are used only while A is no larger than W: the
+  // image FFN2 (A 226 MB, W 75 MB) read slightly more in two groups (887 MB)
+  // than in one (853 MB).
+  const int64_t w_tile_bytes = (int64_t)BN * gs[0].K * 2;
+  const int64_t a_bytes = gs[0].M * gs[0].K * 2, w_bytes = (int64_t)gs[0].N * gs[0].K * 2;
+  int64_t gn = ((int64_t)40 << 20) / w_tile_bytes;
+  if (gn < 1) gn = 1;
+  if (a_bytes > w_bytes) gn = n_tiles;
+  P.group_n = (int)(gn < n_tiles ? gn : n_tiles);
   if (tiles == 0) return cudaSuccess;
   static SmemAttr attr;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(gemm_tc_kernel<BN, NP>), C::SMEM_BYTES, attr);
