@@ -1,14 +1,16 @@
 """CPU oracle for the denoiser stage: a plain, slow, float64 restatement of
-what one denoising loop computes.  TEST INFRASTRUCTURE ONLY.
+what one denoising loop computes.  TEST INFRASTRUCTURE ONLY: the product
+path never imports it.
 
 Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline leg may use
 this module.  It shares no code with the CUDA path and imports nothing from
 it: every function takes plain numpy arrays and returns numpy arrays.
 
 What the pages fix, and where:
-  * the denoiser role = the DiT forward loop plus the scheduler stepping it
-    drives (SGLang-Diffusion "Disaggregated Diffusion Pipeline", Quick Start
-    role table);
+  * the denoiser role: the network's forward passes repeated over the step
+    loop, with the sampler advancing the latent between them
+    (SGLang-Diffusion "Disaggregated Diffusion Pipeline", Quick Start, role
+    table);
   * its inputs: latents, timesteps in the exact order, sigmas, positive and
     (with CFG) negative prompt embeddings, number of steps, raw latent shape
     (SGLang-Diffusion "Support New Diffusion Models", section 4 "Last-Resort
@@ -20,8 +22,8 @@ What the pages fix, and where:
     "Model Configuration Conventions", "Sampling And Geometry");
   * rotary position embeddings and latent packing as things a port must match
     (SGLang-Diffusion "Support New Diffusion Models", "Verify the Port").
-The block equations themselves are not on the pages; the readings taken are
-marked [R1]..[R14] below and listed with their reasons in the design notes.
+The block equations themselves are not on the pages; each reading taken where
+they are silent is marked [R1]..[R14] at the function that applies it.
 
 Arrays are float64 unless a caller passes another dtype.  Shapes: a token
 sequence is [N, D] for one batch element; batch loops are explicit.

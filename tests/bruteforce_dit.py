@@ -153,3 +153,62 @@ def timestep_modulation(t, W, cfg):
     h = _lin(e, _tolist(W["time_mlp.fc1.weight"]), _tolist(W["time_mlp.fc1.bias"]))
     h = [a / (1.0 + math.exp(-a)) for a in h]
     return _lin(h, _tolist(W["time_mlp.fc2.weight"]), _tolist(W["time_mlp.fc2.bias"]))
+
+
+def dit_forward(lat, t, ctx, W, cfg):
+    """Velocity for one latent [C][T][H][W] (nested lists or an array) at
+    network timestep t: patch vectors gathered by index arithmetic, the
+    blocks above, the head, and the velocity scattered back by index."""
+    C = len(lat)
+    T, H, Wd = len(lat[0]), len(lat[0][0]), len(lat[0][0][0])
+    pt, ph, pw = cfg["patch"]
+    gt, gh, gw = T // pt, H // ph, Wd // pw
+    D = cfg["hidden"]
+    w_pe, b_pe = _tolist(W["patch_embed.weight"]), _tolist(W["patch_embed.bias"])
+    positions, toks = [], []
+    for it in range(gt):
+        for ih in range(gh):
+            for iw in range(gw):
+                vec = [lat[c][it * pt + a][ih * ph + b][iw * pw + e]
+                       for c in range(C) for a in range(pt) for b in range(ph) for e in range(pw)]
+                toks.append(_lin(vec, w_pe, b_pe))
+                positions.append((it, ih, iw))
+    m = timestep_modulation(t, W, cfg)
+    if cfg["cond_mode"] == 0:
+        for blk in range(cfg["depth"]):
+            toks = block_cross(toks, m, ctx, W, blk, cfg, positions)
+    else:
+        xc = [list(r) for r in _tolist(ctx)]
+        for blk in range(cfg["depth"]):
+            toks, xc = block_joint(toks, xc, m, W, blk, cfg, positions)
+    vt = final_layer(toks, m, W, cfg)
+    v = [[[[0.0] * Wd for _ in range(H)] for _ in range(T)] for _ in range(C)]
+    for n, (it, ih, iw) in enumerate(positions):
+        k = 0
+        for c in range(C):
+            for a in range(pt):
+                for b in range(ph):
+                    for e in range(pw):
+                        v[c][it * pt + a][ih * ph + b][iw * pw + e] = vt[n][k]
+                        k += 1
+    assert len(vt[0]) == k and len(vt[0]) == C * pt * ph * pw and D == len(toks[0])
+    return v
+
+
+def denoise_loop(lat, cond, uncond, W, cfg, sigmas, timesteps, g):
+    """Flow-Euler loop with guidance, the timesteps given explicitly (so that
+    the sigma -> timestep conversion is not restated here): per step the
+    conditional and unconditional velocities, v = vu + g (vc - vu), then
+    x += (sigma_{i+1} - sigma_i) v element by element."""
+    x = [[[list(map(float, row)) for row in plane] for plane in ch] for ch in _tolist(lat)]
+    for i in range(len(sigmas) - 1):
+        vc = dit_forward(x, timesteps[i], cond, W, cfg)
+        vu = dit_forward(x, timesteps[i], uncond, W, cfg)
+        ds = sigmas[i + 1] - sigmas[i]
+        for c in range(len(x)):
+            for a in range(len(x[c])):
+                for b in range(len(x[c][a])):
+                    for e in range(len(x[c][a][b])):
+                        u = vu[c][a][b][e]
+                        x[c][a][b][e] += ds * (u + g * (vc[c][a][b][e] - u))
+    return x

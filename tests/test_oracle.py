@@ -1,8 +1,10 @@
 """Pins for the CPU oracle: each check ties it to something other than itself
 (hand-worked fixtures, closed forms, invariants, library special functions,
 or a naive scalar restatement on tiny inputs)."""
+import inspect
 import math
 import os
+import textwrap
 
 import numpy as np
 import pytest
@@ -50,6 +52,16 @@ def test_schedule_endpoints_and_monotone():
             sg = O.shift_sigma(O.sigma_schedule(n), s)
             assert len(sg) == n + 1 and sg[0] == 1.0 and sg[-1] == 0.0
             assert np.all(np.diff(sg) < 0)
+
+
+def test_schedule_and_timesteps_fixture():
+    # interior values, not only the endpoints: a curve through (0, 1) and
+    # (n, 0) that is not linear in i fails here
+    rows = np.array(_rows("schedule_n4.txt"))
+    np.testing.assert_array_equal(O.sigma_schedule(4), rows[:, 1])
+    np.testing.assert_allclose(O.shift_sigma(O.sigma_schedule(4), 3.0), rows[:, 2], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(O.timesteps_from_sigmas(rows[:, 2]), rows[:, 3], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(O.shift_sigma(O.sigma_schedule(4), 5.0), rows[:, 4], rtol=0, atol=1e-15)
 
 
 def test_euler_constant_velocity_closed_form():
@@ -300,20 +312,63 @@ def test_dit_forward_composition_against_scalar_loops():
     np.testing.assert_allclose(O.dit_forward(lat, 640.0, ctx, W, cfg), v, atol=1e-11)
 
 
+def test_dit_forward_joint_composition_against_scalar_loops():
+    # joint mode at depth 2: the condition stream must be carried from block
+    # to block (block 1 reads block 0's condition-stream output)
+    cfg = small_cfg(1, depth=2)
+    W = rand_weights(cfg, seed=6, std=0.25)
+    rng = np.random.default_rng(20)
+    lat, ctx = rng.standard_normal((2, 1, 4, 4)), rng.standard_normal((3, 8))
+    ref = np.array(BF.dit_forward(lat, 412.0, ctx, W, cfg))
+    np.testing.assert_allclose(O.dit_forward(lat, 412.0, ctx, W, cfg), ref, atol=1e-11)
+
+
+def _loop_case(mode, seed):
+    cfg = small_cfg(mode, depth=2)
+    W = rand_weights(cfg, seed=seed, std=0.25)
+    rng = np.random.default_rng(seed + 100)
+    lat = rng.standard_normal((2, 1, 4, 4))
+    cond = rng.standard_normal((3, cfg["cond_dim"]))
+    unc = rng.standard_normal((3, cfg["cond_dim"])) * 0.5   # a negative condition unlike the positive one
+    return cfg, W, lat, cond, unc
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_loop_against_scalar_loops_with_hand_worked_timesteps(mode):
+    # the full loop (guidance direction, sigma -> timestep wiring, Euler
+    # increments) against the scalar restatement fed the hand-worked
+    # schedule and timesteps of tests/golden/schedule_n4.txt (shift 3)
+    cfg, W, lat, cond, unc = _loop_case(mode, 7 + mode)
+    rows = np.array(_rows("schedule_n4.txt"))
+    sig, ts = rows[:, 2], rows[:, 3]
+    ref = np.array(BF.denoise_loop(lat, cond, unc, W, cfg, list(sig), list(ts), 4.0))
+    np.testing.assert_allclose(O.denoise_loop(lat, cond, unc, W, cfg, sig, 4.0), ref, atol=1e-11)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_loop_guidance_direction(mode):
+    # one step from sigma 0.9 to 0.75 (timestep 900): guidance 0 must follow
+    # the negative condition alone, guidance 1 the positive one
+    cfg, W, lat, cond, unc = _loop_case(mode, 9 + mode)
+    sig = np.array([0.9, 0.75])
+    for g, which in ((0.0, unc), (1.0, cond)):
+        v = np.array(BF.dit_forward(lat, 900.0, which, W, cfg))
+        np.testing.assert_allclose(O.denoise_loop(lat, cond, unc, W, cfg, sig, g), lat - 0.15 * v, atol=1e-11)
+
+
 # ---------------------------------------------------------------- the pins bite
-_MUTATIONS = {
-    "rope_turns_backwards": ("apply_rope", lambda f: (lambda x, a: f(x, -a))),
-    "modulate_without_one": ("modulate", lambda f: (lambda h, sh, sc: h * sc + sh)),
-    "gelu_erf_form": ("gelu_tanh", lambda f: (lambda x: 0.5 * x * (1 + np.vectorize(math.erf)(x / math.sqrt(2))))),
-    "attention_unscaled": ("attention", lambda f: (lambda q, k, v: O.softmax_rows(q @ k.T) @ v)),
-    "layer_norm_eps_outside": ("layer_norm", lambda f: (lambda x, eps: f(x, 0.0) + eps)),
-}
+def _source_mutant(fn_name, old, new):
+    """The oracle function `fn_name` with the text `old` of its source
+    replaced by `new` (a planted mistake), compiled against the oracle's
+    module namespace."""
+    src = textwrap.dedent(inspect.getsource(getattr(O, fn_name)))
+    assert old in src, (fn_name, old)
+    ns = dict(vars(O))
+    exec(compile(src.replace(old, new), O.__file__, "exec"), ns)
+    return ns[fn_name]
 
 
-@pytest.mark.parametrize("name", sorted(_MUTATIONS))
-def test_planted_oracle_mistakes_are_caught(name, monkeypatch):
-    attr, mk = _MUTATIONS[name]
-    monkeypatch.setattr(O, attr, mk(getattr(O, attr)))
+def _pin_block():
     cfg = small_cfg(0)
     W = rand_weights(cfg)
     rng = np.random.default_rng(12)
@@ -321,4 +376,43 @@ def test_planted_oracle_mistakes_are_caught(name, monkeypatch):
     x, ctx, m = rng.standard_normal((6, 8)), rng.standard_normal((3, 6)), rng.standard_normal(48) * 0.5
     pos = [tuple(p) for p in O.token_positions(grid)]
     ref = np.array(BF.block_cross(x, m, ctx, W, 0, cfg, pos))
-    assert np.max(np.abs(O.block_cross(x, m, ctx, W, 0, cfg, grid) - ref)) > 1e-9
+    np.testing.assert_allclose(O.block_cross(x, m, ctx, W, 0, cfg, grid), ref, atol=1e-9)
+
+
+def _pin_loops():
+    for mode in (0, 1):
+        test_loop_against_scalar_loops_with_hand_worked_timesteps(mode)
+        test_loop_guidance_direction(mode)
+
+
+# name -> (oracle function, replacement factory, the pin that must fail)
+_MUTATIONS = {
+    "rope_turns_backwards": ("apply_rope", lambda f: (lambda x, a: f(x, -a)), _pin_block),
+    "modulate_without_one": ("modulate", lambda f: (lambda h, sh, sc: h * sc + sh), _pin_block),
+    "gelu_erf_form": ("gelu_tanh", lambda f: (lambda x: 0.5 * x * (1 + np.vectorize(math.erf)(x / math.sqrt(2)))),
+                      _pin_block),
+    "attention_unscaled": ("attention", lambda f: (lambda q, k, v: O.softmax_rows(q @ k.T) @ v), _pin_block),
+    "layer_norm_eps_outside": ("layer_norm", lambda f: (lambda x, eps: f(x, 0.0) + eps), _pin_block),
+    # loop wiring
+    "cfg_cond_uncond_swapped": ("denoise_loop", lambda f: _source_mutant(
+        "denoise_loop", "cfg_combine(vc, dit_forward(x, ts[i], uncond, W, cfg), guidance)",
+        "cfg_combine(dit_forward(x, ts[i], uncond, W, cfg), vc, guidance)"), _pin_loops),
+    "timestep_not_scaled": ("timesteps_from_sigmas", lambda f: _source_mutant(
+        "timesteps_from_sigmas", "np.asarray(sigmas, dtype=F64) * scale", "np.asarray(sigmas, dtype=F64)"),
+        _pin_loops),
+    "joint_condition_stream_not_carried": ("dit_forward", lambda f: _source_mutant(
+        "dit_forward", "x, xc = block_joint(", "x, _ = block_joint("),
+        test_dit_forward_joint_composition_against_scalar_loops),
+    "schedule_squared": ("sigma_schedule", lambda f: _source_mutant(
+        "sigma_schedule", "1.0 - i / n_steps", "(1.0 - i / n_steps) ** 2"), test_schedule_and_timesteps_fixture),
+    "euler_step_reversed": ("euler_step", lambda f: (lambda x, v, s, sn: np.asarray(x) + (s - sn) * np.asarray(v)),
+                            _pin_loops),
+}
+
+
+@pytest.mark.parametrize("name", sorted(_MUTATIONS))
+def test_planted_oracle_mistakes_are_caught(name, monkeypatch):
+    attr, mk, pin = _MUTATIONS[name]
+    monkeypatch.setattr(O, attr, mk(getattr(O, attr)))
+    with pytest.raises(AssertionError):
+        pin()
