@@ -51,7 +51,7 @@ WORKLOADS = {
 TRAFFIC = {
     # kernel source file -> (sha256 prefix of the source, workload, bytes per launch).
     # attn_tc.cu: dram__bytes_read.sum + dram__bytes_write.sum = 387.9 MB for one
-    # batch-1 video self-attention launch (profiles/attn_tc_video_block.md),
+    # batch-1 video self-attention launch (ncu capture of the block case),
     # scaled x2 to the batch-2 launch the step runs (traffic grows with the
     # number of query rows).  The source hash was moved on by a change to the
     # host-side launcher only (per-device shared-memory attribute); the
@@ -371,7 +371,6 @@ def run_block_case(args):
     profiling."""
     import torch
     from diffusion_transformer_denoising_gb300 import dit
-    from oracle import dit_oracle as O  # noqa: F401
     torch.cuda.set_device(0)
     cfg = synth.config(WORKLOADS[args.workload]["cfg"], depth=1)
     grid = synth.grid(cfg)
