@@ -12,6 +12,14 @@ tokens), random bf16 weights, synthetic inputs.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload video|image]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 
+The headline loop is timed with one CUDA event pair around the whole call
+(launches are counted, nothing else is recorded on the stream); the
+per-kernel breakdown and the roofline figure come from a second, separately
+timed pass with an event pair around every launch.  On one GPU the default
+line also carries the 30-block image loop (`image_loop`), the seven points of
+the image block batch/sequence sweep (`sweep`) and the CPU oracle timings
+(`cpu_baseline`).
+
 With N > 1 (torchrun), each rank denoises its own request on its own GPU
 (independent replicas, no collective on the data path); the timing is the
 maximum over ranks and the value counts every rank's steps.
@@ -78,6 +86,16 @@ def step_flops(cfg: dict, B: int, N: int, L: int) -> dict:
                 total=depth * (gemm + attn_self + attn_cross), attn_self_per_launch=attn_self)
 
 
+def workload_config(workload: str, steps: int, world: int) -> dict:
+    """The `config` object of the JSON line, identical for both arms."""
+    cfg = synth.config(WORKLOADS[workload]["cfg"])
+    N = int(np.prod(synth.grid(cfg)))
+    return {"workload": WORKLOADS[workload]["desc"], "tokens": N, "cond_tokens": cfg["cond_len"], "cfg_batch": 2,
+            "schedule": f"first {steps} of {cfg['steps']} flow steps, shift {cfg['shift']}",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (activations >= 400 MB per step)"}
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -132,14 +150,24 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
-def cpu_oracle_sample(workload: str, reps: int = 1) -> dict:
+_ORACLE_WEIGHTS = {}
+
+
+def _oracle_block_weights(workload: str):
+    if workload not in _ORACLE_WEIGHTS:
+        cfg = synth.config(WORKLOADS[workload]["cfg"])
+        _ORACLE_WEIGHTS[workload] = (cfg, synth.make_weights(cfg, seed=0, blocks=[0]))
+    return _ORACLE_WEIGHTS[workload]
+
+
+def cpu_oracle_sample(workload: str) -> dict:
     """Time the CPU oracle on a bounded sample of one step: one block at two
     sampled query-row counts (keys/values over all tokens), split into a fixed
     and a per-row cost, extrapolated to a full step (all rows, every block,
-    both CFG passes).  Returns seconds per step and the description."""
+    both CFG passes).  Returns seconds per block and per step (extrapolated),
+    the seconds actually spent, and the description."""
     from oracle import dit_oracle as O
-    cfg = synth.config(WORKLOADS[workload]["cfg"])
-    W = synth.make_weights(cfg, seed=0, blocks=[0])
+    cfg, W = _oracle_block_weights(workload)
     grid = synth.grid(cfg)
     N, L, D = int(np.prod(grid)), cfg["cond_len"], cfg["hidden"]
     rng = np.random.default_rng(0)
@@ -148,48 +176,87 @@ def cpu_oracle_sample(workload: str, reps: int = 1) -> dict:
     m = O.timestep_modulation(700.0, W, cfg)
     angles = O.rope_angles(O.token_positions(grid), cfg["rope_axes"], cfg["rope_theta"])
     r1, r2 = 128, 384
-    times = {r1: [], r2: []}
-    for _ in range(reps):
-        for r in (r1, r2):
-            rows = np.linspace(0, N - 1, r).astype(np.int64)
-            t0 = time.perf_counter()
-            if cfg["cond_mode"] == synth.COND_CROSS:
-                O.block_cross(x, m, ctx, W, 0, cfg, grid, rows=rows, angles=angles)
-            else:
-                O.block_joint(x, ctx, m, W, 0, cfg, grid, rows=rows + L, angles=angles)
-            times[r].append(time.perf_counter() - t0)
-    t1, t2 = min(times[r1]), min(times[r2])
-    per_row = max((t2 - t1) / (r2 - r1), 0.0)
-    fixed = max(t1 - r1 * per_row, 0.0)
+    times = {}
+    for r in (r1, r2):
+        rows = np.linspace(0, N - 1, r).astype(np.int64)
+        t0 = time.perf_counter()
+        if cfg["cond_mode"] == synth.COND_CROSS:
+            O.block_cross(x, m, ctx, W, 0, cfg, grid, rows=rows, angles=angles)
+        else:
+            O.block_joint(x, ctx, m, W, 0, cfg, grid, rows=rows + L, angles=angles)
+        times[r] = time.perf_counter() - t0
+    per_row = max((times[r2] - times[r1]) / (r2 - r1), 0.0)
+    fixed = max(times[r1] - r1 * per_row, 0.0)
     rows_all = N if cfg["cond_mode"] == synth.COND_CROSS else N + L
     t_block = fixed + rows_all * per_row
     t_step = 2 * cfg["depth"] * t_block
     sample = (f"oracle (numpy float64) on one {workload} block at {r1} and {r2} sampled query rows "
               f"(keys/values over all {rows_all} tokens), split into fixed + per-row cost and extrapolated "
               f"x{rows_all} rows x{cfg['depth']} blocks x2 CFG passes")
-    return dict(t_step=t_step, sample_s=sum(times[r1]) + sum(times[r2]), sample=sample,
+    return dict(t_block=t_block, t_step=t_step, sample_s=times[r1] + times[r2], sample=sample,
                 cores=os.cpu_count())
+
+
+def cpu_oracle_tiny_loop() -> dict:
+    """The whole tiny loop (2 blocks, 64 tokens, 4 CFG + Euler steps) on the
+    CPU oracle: nothing extrapolated."""
+    from oracle import dit_oracle as O
+    cfg = synth.config("tiny")
+    W = synth.make_weights(cfg, seed=0)
+    lat, cond = synth.make_latent(cfg, seed=1)[0], synth.make_cond(cfg, seed=2)[0]
+    sig = O.shift_sigma(O.sigma_schedule(cfg["steps"]), cfg["shift"])
+    t0 = time.perf_counter()
+    O.denoise_loop(lat, cond, np.zeros_like(cond), W, cfg, sig, cfg["guidance"])
+    t = time.perf_counter() - t0
+    return dict(loop_s=t, steps_per_s=cfg["steps"] / t)
+
+
+def cpu_baseline_leg(workload: str) -> dict:
+    """The `cpu_baseline` object: the headline workload's extrapolated step
+    rate, with the tiny loop (complete) and one block of each large workload
+    (extrapolated from sampled rows) beside it."""
+    main = cpu_oracle_sample(workload)
+    other = "image" if workload == "video" else "video"
+    oth = cpu_oracle_sample(other)
+    tiny = cpu_oracle_tiny_loop()
+    return {"value": 1.0 / main["t_step"], "unit": "steps/s", "cores": main["cores"], "kind": "oracle",
+            "sample": main["sample"], "extrapolated": True,
+            "sample_seconds": main["sample_s"] + oth["sample_s"] + tiny["loop_s"],
+            "cases": {"tiny_loop": {"seconds": tiny["loop_s"], "steps_per_s": tiny["steps_per_s"],
+                                    "extrapolated": False, "what": "complete 4-step CFG loop of the tiny config"},
+                      f"{workload}_block": {"seconds": main["t_block"], "extrapolated": True,
+                                            "sample_seconds": main["sample_s"]},
+                      f"{other}_block": {"seconds": oth["t_block"], "extrapolated": True,
+                                         "sample_seconds": oth["sample_s"], "sample": oth["sample"]}}}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
+    _oracle_block_weights(args.workload)       # set-up outside the timed samples
     for _ in range(args.warmup):
         cpu_oracle_sample(args.workload)
-    ts, total = [], 0.0
+    ts, walls = [], []
     for _ in range(args.steps):
+        w0 = time.perf_counter()
         r = cpu_oracle_sample(args.workload)
+        walls.append(time.perf_counter() - w0)
         ts.append(r["t_step"])
-        total += r["sample_s"]
     t_step = statistics.median(ts)
     v = 1.0 / t_step
+    wall = sum(walls)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOADS[args.workload]["desc"], "sample": r["sample"]},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+            "extrapolated": True,
+            "step_is": "one bounded oracle sample: one block at two sampled query-row counts; `value` is the "
+                       "full denoising step rate extrapolated from it",
+            "ms_per_full_step_extrapolated": t_step * 1e3, "sample_seconds_total": wall,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(args.workload, args.steps, world),
             "cpu_baseline": {"value": v, "unit": "steps/s", "cores": r["cores"], "kind": "oracle",
-                             "sample": r["sample"]},
+                             "sample": r["sample"], "extrapolated": True},
             "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -213,6 +280,64 @@ def file_sha(path: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
+def _schedule(cfg: dict, k: int) -> np.ndarray:
+    """The first k steps of the workload's shifted schedule (a longer linear
+    one if k exceeds it)."""
+    full = np.array([1.0 - i / cfg["steps"] for i in range(cfg["steps"] + 1)])
+    full = (cfg["shift"] * full / (1 + (cfg["shift"] - 1) * full)).astype(np.float32)
+    if k <= cfg["steps"]:
+        return full[:k + 1].copy()
+    return np.linspace(1.0, 1e-3, k + 1).astype(np.float32)
+
+
+def run_image_loop(args, clocks_gpu: str) -> dict:
+    """Steps/s of the 30-block image DiT loop (4096 + 512 joint tokens, CFG
+    pair), device-timed over --steps steps after --warmup, no per-launch
+    instrumentation."""
+    import torch
+    from diffusion_transformer_denoising_gb300 import dit
+    cfg = synth.config("image")
+    L, C = cfg["cond_len"], cfg["in_channels"]
+    N = int(np.prod(synth.grid(cfg)))
+    m = dit.DiT(cfg)
+    W = synth.make_weights_torch(cfg, seed=0, device="cuda")
+    m.load_weights(W)
+    del W
+    torch.cuda.empty_cache()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2000)
+    lat0 = torch.randn((1, C) + cfg["latent"], generator=g, device="cuda")
+    cond = torch.randn((1, L, cfg["cond_dim"]), generator=g, device="cuda").to(torch.bfloat16).float()
+    unc = torch.zeros_like(cond)
+    flags = dit.LOOP_PARTIAL_SCHEDULE
+    lat = lat0.clone()
+    m.dit_denoise_loop(lat, 1, cfg["latent"], cond, unc, L, _schedule(cfg, args.warmup), cfg["guidance"], flags)
+    m.dit_synchronize()
+    lat = lat0.clone()
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(clocks_gpu)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    m.dit_denoise_loop(lat, 1, cfg["latent"], cond, unc, L, _schedule(cfg, args.steps), cfg["guidance"], flags)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    m.dit_synchronize()
+    t_step = e0.elapsed_time(e1) / 1e3 / args.steps
+    fl = step_flops(cfg, 2, N, L)
+    peaks = measured_peaks()
+    out = {"what": WORKLOADS["image"]["desc"] + f", first {args.steps} of {cfg['steps']} steps, shift {cfg['shift']}",
+           "steps_per_s": 1.0 / t_step, "ms_per_step": t_step * 1e3, "steps": args.steps,
+           "attn_gemm_tflops": fl["total"] / t_step / 1e12,
+           "pct_bf16_peak": 100 * fl["total"] / t_step / 1e12 / peaks["bf16"],
+           "finite": bool(torch.isfinite(lat).all().item()), "clocks": clk}
+    m.close()
+    del lat, lat0, cond, unc
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     import torch
     from diffusion_transformer_denoising_gb300 import dit
@@ -229,10 +354,11 @@ def run_gpu(args):
         torch.cuda.set_device(0)
     dev_idx = torch.cuda.current_device()
     stream = torch.cuda.current_stream()
+    uuid = str(torch.cuda.get_device_properties(dev_idx).uuid)
+    gpu_id = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
 
     wl = WORKLOADS[args.workload]
     cfg = synth.config(wl["cfg"])
-    T, H, Wd = cfg["latent"]
     N = int(np.prod(synth.grid(cfg)))
     L = cfg["cond_len"]
     C = cfg["in_channels"]
@@ -243,48 +369,49 @@ def run_gpu(args):
     torch.cuda.empty_cache()
     g = torch.Generator(device=f"cuda:{dev_idx}")
     g.manual_seed(1000 + rank)
-    lat0 = torch.randn((1, C, T, H, Wd), generator=g, device="cuda", dtype=torch.float32)
+    lat0 = torch.randn((1, C) + cfg["latent"], generator=g, device="cuda", dtype=torch.float32)
     cond = torch.randn((1, L, cfg["cond_dim"]), generator=g, device="cuda", dtype=torch.float32)
     cond = cond.to(torch.bfloat16).float()
     unc = torch.zeros_like(cond)
-    full = np.array([1.0 - i / cfg["steps"] for i in range(cfg["steps"] + 1)])
-    full = (cfg["shift"] * full / (1 + (cfg["shift"] - 1) * full)).astype(np.float32)
-
-    def schedule(k):
-        # the first k steps of the workload's schedule (a longer linear one if k exceeds it)
-        if k <= cfg["steps"]:
-            return full[:k + 1].copy()
-        return np.linspace(1.0, 1e-3, k + 1).astype(np.float32)
-
     flags = dit.LOOP_PARTIAL_SCHEDULE
+
     # warm-up
     lat = lat0.clone()
-    sw = schedule(args.warmup)
-    m.dit_denoise_loop(lat, 1, cfg["latent"], cond, unc, L, sw, cfg["guidance"], flags)
+    m.dit_denoise_loop(lat, 1, cfg["latent"], cond, unc, L, _schedule(cfg, args.warmup), cfg["guidance"], flags)
     m.dit_synchronize()
 
-    # timed region: exactly K steps in one loop call, per-kernel events on the stream
-    st = schedule(args.steps)
+    # timed region: exactly K steps in one loop call; launches are counted,
+    # nothing else is recorded on the stream
+    st = _schedule(cfg, args.steps)
     lat = lat0.clone()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    uuid = str(torch.cuda.get_device_properties(dev_idx).uuid)
-    clocks = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
-    m.dit_profile_start(timing=True)
+    clocks = ClockSampler(gpu_id)
+    m.dit_profile_start(timing=False)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     m.dit_denoise_loop(lat, 1, cfg["latent"], cond, unc, L, st, cfg["guidance"], flags)
     e1.record(stream)
-    prof = m.dit_profile_stop()
     torch.cuda.synchronize()
     clk = clocks.stop()
+    counts = m.dit_profile_stop()
     m.dit_synchronize()
     elapsed = e0.elapsed_time(e1) / 1e3
     if dist is not None:
         dist.barrier()
     t_max, value = aggregate(elapsed, args.steps, world, dist)
     ok = bool(torch.isfinite(lat).all().item())
+
+    # per-kernel breakdown: a separate pass over the same steps with a CUDA
+    # event pair around every launch on the launching stream
+    k_prof = max(1, min(args.steps, 3))
+    lat_p = lat0.clone()
+    m.dit_profile_start(timing=True)
+    m.dit_denoise_loop(lat_p, 1, cfg["latent"], cond, unc, L, _schedule(cfg, k_prof), cfg["guidance"], flags)
+    prof = m.dit_profile_stop()
+    m.dit_synchronize()
+    del lat_p
 
     # end to end through the public API with host buffers: every step copies
     # its inputs host->device and reads the latent back
@@ -294,6 +421,7 @@ def run_gpu(args):
     out_host = torch.empty_like(pin_lat).pin_memory()
     d_lat, d_cond, d_unc = torch.empty_like(lat0), torch.empty_like(cond), torch.empty_like(unc)
     k_e2e = max(1, min(args.steps, 3))
+    full = _schedule(cfg, cfg["steps"])
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -328,16 +456,15 @@ def run_gpu(args):
     traffic = tr[2] if tr and tr[0] == file_sha(src) and tr[1] == args.workload else None
     gemm_ms = sum(prof[k][1] for k in prof if k.startswith("gemm"))
     kern_ms = sum(v[1] for v in prof.values())
+    n_ce, ms_ce = prof["cfg_euler"]
+    ce_bytes = 16 * C * int(np.prod(cfg["latent"]))    # both passes' velocity read, latent read + write (fp32)
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (value / world / PAGES_STEPS_PER_S[args.workload]) if args.workload in PAGES_STEPS_PER_S
         else None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) latents/condition, N(0,0.02) bf16 weights)",
-        "config": {"workload": wl["desc"], "tokens": N, "cond_tokens": L, "cfg_batch": 2,
-                   "schedule": f"first {args.steps} of {cfg['steps']} flow steps, shift {cfg['shift']}",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (activations >= 400 MB per step)"},
+        "config": workload_config(args.workload, args.steps, world),
         "attn_gemm_tflops": tflops,
         "pct_bf16_peak": 100 * tflops / peaks["bf16"],
         "pct_bf16_peak_sustained": 100 * tflops / peaks["bf16_sustained"],
@@ -345,21 +472,30 @@ def run_gpu(args):
                      "achieved": attn_achieved, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                      "frac": attn_achieved / peaks["bf16_sustained"], "traffic": traffic,
                      "peak_kind": f"bf16 sustained ({peaks['source']}), kernel timed inside a long step",
-                     "per_launch_flops": fl["attn_self_per_launch"], "avg_launch_ms": attn_ms},
-        "kernel_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
+                     "per_launch_flops": fl["attn_self_per_launch"], "avg_launch_ms": attn_ms,
+                     "timed_by": f"event pair per launch, separate {k_prof}-step pass after the headline"},
+        "breakdown_steps": k_prof,
+        "kernel_ms_per_step": {k: v[1] / k_prof for k, v in prof.items()},
         "kernel_share": {k: v[1] / kern_ms for k, v in prof.items()} if kern_ms > 0 else None,
-        "gemm_tflops": fl["gemm"] / (gemm_ms / args.steps / 1e3) / 1e12 if gemm_ms > 0 else None,
-        "gpu_launches": int(sum(v[0] for v in prof.values())),
+        "gemm_tflops": fl["gemm"] / (gemm_ms / k_prof / 1e3) / 1e12 if gemm_ms > 0 else None,
+        "cfg_euler": {"us_per_launch": ms_ce / max(n_ce, 1) * 1e3, "bytes_per_launch": ce_bytes,
+                      "gbs": ce_bytes / (ms_ce / max(n_ce, 1) / 1e3) / 1e9 if ms_ce > 0 else None,
+                      "hbm_peak_gbs": peaks["hbm"]},
+        "gpu_launches": int(sum(v[0] for v in counts.values())),
         "clocks": clk,
         "finite": ok,
         "e2e": {"value": e2e_value, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": k_e2e, "note": "one dit_denoise_loop call per step from pinned host buffers; "
                                         "includes the per-call condition key/value projection"},
     }
+    if world == 1 and not args.no_extras and args.workload == "video":
+        m.close()
+        del lat, lat0, cond, unc, d_lat, d_cond, d_unc
+        torch.cuda.empty_cache()
+        line["image_loop"] = run_image_loop(args, gpu_id)
+        line["sweep"] = sweep_points(args, steps=3, warmup=1)
     if world == 1 and not args.no_cpu_baseline:
-        r = cpu_oracle_sample(args.workload)
-        line["cpu_baseline"] = {"value": 1.0 / r["t_step"], "unit": "steps/s", "cores": r["cores"],
-                                "kind": "oracle", "sample": r["sample"], "sample_seconds": r["sample_s"]}
+        line["cpu_baseline"] = cpu_baseline_leg(args.workload)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -407,18 +543,17 @@ def run_block_case(args):
 SWEEP_POINTS = [(1, 4096), (2, 4096), (4, 4096), (8, 4096), (1, 1024), (1, 16384), (1, 65536)]
 
 
-def run_sweep(args):
+def sweep_points(args, steps: int, warmup: int) -> list:
     """Batch/sequence sweep of the image DiT block: a depth-1 image model
     (hidden 3072, 24x128 heads, MLP 12288) at batch 1/2/4/8 with 4096 image
     tokens and at 1024/16384/65536 tokens with batch 1, always jointly with
     512 condition tokens.  Each point times one denoising step (timestep MLP,
     patch embed, the block on the CFG pair, final layer, guidance + Euler)
-    through dit_denoise_loop, device-timed over --steps calls."""
+    through dit_denoise_loop, device-timed over `steps` calls."""
     import torch
     from diffusion_transformer_denoising_gb300 import dit
-    torch.cuda.set_device(0)
     base = synth.config("image", depth=1)
-    L, C, D = base["cond_len"], base["in_channels"], base["hidden"]
+    L, C = base["cond_len"], base["in_channels"]
     _, ph, pw = base["patch"]
     W = synth.make_weights_torch(base, seed=0, device="cuda")
     sig = np.array([1.0, 1.0 - 1.0 / base["steps"]])
@@ -437,17 +572,17 @@ def run_sweep(args):
         cond = torch.randn((batch, L, cfg["cond_dim"]), generator=g, device="cuda").to(torch.bfloat16).float()
         unc = torch.zeros_like(cond)
         lat = lat0.clone()
-        for _ in range(max(1, args.warmup)):
+        for _ in range(max(1, warmup)):
             m.dit_denoise_loop(lat, batch, cfg["latent"], cond, unc, L, sig, cfg["guidance"], dit.LOOP_PARTIAL_SCHEDULE)
         m.dit_synchronize()
         lat = lat0.clone()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             m.dit_denoise_loop(lat, batch, cfg["latent"], cond, unc, L, sig, cfg["guidance"], dit.LOOP_PARTIAL_SCHEDULE)
         e1.record(stream)
         torch.cuda.synchronize()
-        t_step = e0.elapsed_time(e1) / 1e3 / args.steps
+        t_step = e0.elapsed_time(e1) / 1e3 / steps
         fl = step_flops(cfg, 2 * batch, side * side, L)
         tf = fl["total"] / t_step / 1e12
         points.append({"batch": batch, "image_tokens": side * side, "cond_tokens": L,
@@ -457,9 +592,18 @@ def run_sweep(args):
         m.close()
         del lat, lat0, cond, unc
         torch.cuda.empty_cache()
+    del W
+    torch.cuda.empty_cache()
+    return points
+
+
+def run_sweep(args):
+    import torch
+    torch.cuda.set_device(0)
+    points = sweep_points(args, steps=args.steps, warmup=args.warmup)
     print(json.dumps({"case": "image DiT block sweep: depth 1, one CFG + Euler step per point", "dtype": "bf16",
                       "data": "synthetic (seeded N(0,1) latents/condition, N(0,0.02) bf16 weights)",
-                      "steps": args.steps, "warmup": args.warmup, "peak_bf16_tflops": peaks["bf16"],
+                      "steps": args.steps, "warmup": args.warmup, "peak_bf16_tflops": measured_peaks()["bf16"],
                       "points": points}), flush=True)
 
 
@@ -471,6 +615,8 @@ def main():
     ap.add_argument("--workload", default="video", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the image loop and the sweep points that the default video line also carries")
     ap.add_argument("--batch", type=int, default=2, help="batch of the block case")
     ap.add_argument("--case", default="step", choices=["step", "block", "sweep"],
                     help="block: one DiT block repeatedly (small case for kernel profiling); "

@@ -257,6 +257,11 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
           tma_load_3d(smem + Q_OFF + TILE_BYTES / 2, &tmQ, q_full, 64, qt * BQ, bh);
           ++q_issued;
         }
+        if (!DIT_BOUNDS(bh >= 0 && bh < a.B * a.H && qt >= 0 && qt < nq && kv_rot >= 0 && kv_rot < nkv, err, 62)) {
+          *abort_flag = 1;  // every other wait of the CTA returns at once
+          ok = false;
+          break;
+        }
         for (int j = 0; j < nkv; ++j, ++G) {
           // stage G % nst was last read by S_{G-nst} (K) or PV_{G-nst} (V)
           if (G >= nst) {
@@ -487,7 +492,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       const int bh = item_bh(k), b = bh / a.H, head = bh - b * a.H;
       const int D = a.H * HD;
       __nv_bfloat16* out = nullptr;
-      if (tok < a.Lq) {
+      if (tok < a.Lq && DIT_BOUNDS(bh < a.B * a.H && tok >= 0, err, 63)) {
         out = (tok < a.split)
                   ? static_cast<__nv_bfloat16*>(a.o1) + ((int64_t)b * a.split + tok) * D
                   : static_cast<__nv_bfloat16*>(a.o2) + ((int64_t)b * (a.Lq - a.split) + (tok - a.split)) * D;

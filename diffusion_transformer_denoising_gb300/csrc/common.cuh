@@ -122,6 +122,22 @@ DIT_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
   return mbar_wait_slow(bar, parity, abort_flag, err, site);
 }
 
+// Debug build (-DDIT_DEBUG_BOUNDS): index and tile-coordinate checks that
+// record the first failing site (DIT_BOUNDS_SITE_MIN and up) in the model's
+// error word and tell the caller to skip the access and wind down.  No assert
+// and no trap: a failed check leaves the context usable, and the host learns
+// of it at the next dit_synchronize.  In the normal build every check is the
+// constant true and compiles away.
+#ifdef DIT_DEBUG_BOUNDS
+DIT_DEV bool dit_bounds_ok(bool ok, int* err, int site) {
+  if (!ok && err) atomicCAS(err, 0, site);
+  return ok;
+}
+#define DIT_BOUNDS(cond, err, site) dit_bounds_ok((cond), (err), (site))
+#else
+#define DIT_BOUNDS(cond, err, site) true
+#endif
+
 // Barrier over `nthreads` threads (whole warps) of the CTA; id 0 is __syncthreads.
 DIT_DEV void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -8,10 +8,11 @@
 #include <string.h>
 
 #include <algorithm>
-#include <mutex>
 #include <string>
 #include <unordered_map>
 #include <vector>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/dit.h"
 #include "kernels.h"
@@ -136,6 +137,14 @@ static dit_status validate_config(const dit_config* c) {
 }
 
 // ============================================================== model
+// Scratch of dit_timestep_modulation_noalloc: DIT_NOALLOC_MAX_BATCH timesteps
+// followed by DIT_NOALLOC_MAX_HIDDEN hidden activations, in module memory
+// that no call allocates or frees.  In host code the symbol is a host-side
+// stand-in; dit_create looks up its device address with the model's device
+// current (which also loads this file's module there) and keeps it in the
+// model, so the no-allocation call itself never triggers a module load.
+static __device__ __align__(256) float g_noalloc_scratch[DIT_NOALLOC_MAX_BATCH + DIT_NOALLOC_MAX_HIDDEN];
+
 struct Param {
   ParamSpec spec;
   bool matrix;  // linear weight: stored in the activation dtype
@@ -174,6 +183,15 @@ struct dit_model {
   void* ws = nullptr;
   size_t ws_bytes = 0;
   float2* rope = nullptr;
+  float* noalloc_scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  // dit_denoise_loop with DIT_LOOP_CUDA_GRAPH: one captured step, replayed
+  struct LoopGraph {
+    cudaGraphExec_t exec = nullptr;
+    std::vector<uint64_t> key;                // every pointer and scalar the captured step holds
+    int64_t counts[DIT_KERNEL_KINDS] = {};  // kernel launches of one step, by kind
+  } graph;
+  cudaStream_t capture_stream = nullptr;
+  bool capturing = false;
   int rope_grid[3] = {0, 0, 0};
   size_t rope_bytes = 0;
   // launch accounting (dit_profile_start / dit_profile_stop)
@@ -243,6 +261,8 @@ extern "C" void dit_destroy(dit_model* m) {
   cudaFree(m->ws);
   cudaFree(m->rope);
   for (auto e : m->prof_pool) cudaEventDestroy(e);
+  if (m->graph.exec) cudaGraphExecDestroy(m->graph.exec);
+  if (m->capture_stream) cudaStreamDestroy(m->capture_stream);
   cudaSetDevice(prev);
   delete m;
 }
@@ -315,6 +335,20 @@ extern "C" dit_status dit_create(const dit_config* cfg, int device, dit_model** 
   if (cudaMemset(m->d_err, 0, sizeof(int)) != cudaSuccess) {
     dit_destroy(m);
     return fail(DIT_ERR_CUDA, "cudaMemset failed");
+  }
+  {
+    // set-up of the no-allocation entry point, done here so that its calls
+    // never load a module: the fixed scratch's device address, and the
+    // timestep MLP kernels it launches
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e == cudaSuccess && !p) e = cudaErrorInvalidSymbol;
+    if (e == cudaSuccess) e = timestep_mlp_preload(m->bf16);
+    if (e != cudaSuccess) {
+      dit_destroy(m);
+      return fail(DIT_ERR_CUDA, "set-up of the fixed scratch failed: %s", cudaGetErrorString(e));
+    }
+    m->noalloc_scratch = static_cast<float*>(p);
   }
   if (getenv("DIT_VERBOSE"))
     fprintf(stderr,
@@ -400,8 +434,25 @@ static dit_status require_loaded(const dit_model* m) {
   return DIT_OK;
 }
 
-// Counts the kernels a launcher enqueues and, while timing is on, brackets
-// them with an event pair on the launching stream.
+// NVTX range names of the kernel kinds (host-side annotations for a profiler
+// timeline; without an attached tool each push/pop is a no-op call).
+static const char* const kKindNames[DIT_KERNEL_KINDS] = {
+    "gemm_qkv", "gemm_out", "gemm_cross_q", "gemm_cross_kv", "gemm_ffn1", "gemm_ffn2",
+    "gemm_embed", "attn_self", "attn_cross", "ln", "small", "cfg_euler"};
+
+// A named NVTX range for the lifetime of the object.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  NvtxRange(const char* fmt, int i) {
+    char buf[48];
+    snprintf(buf, sizeof(buf), fmt, i);
+    nvtxRangePushA(buf);
+  }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
+// Counts the kernels a launcher enqueues, names them with an NVTX range and,
+// while timing is on, brackets them with an event pair on the launching stream.
 struct Launch {
   dit_model* m;
   int kind, n;
@@ -416,9 +467,11 @@ struct Launch {
     return m->prof_pool[m->prof_next++];
   }
   Launch(dit_model* m_, int kind_, int n_, cudaStream_t s_) : m(m_), kind(kind_), n(n_), s(s_) {
-    if (m->prof_timing && (a = event(m))) cudaEventRecord(a, s);
+    nvtxRangePushA(kKindNames[kind]);
+    if (m->prof_timing && !m->capturing && (a = event(m))) cudaEventRecord(a, s);
   }
   ~Launch() {
+    nvtxRangePop();
     m->prof_counts[kind] += n;
     if (a) {
       cudaEvent_t b = event(m);
@@ -707,6 +760,7 @@ static dit_status cross_kv(dit_model* m, int blk, const void* cond_act, int B, i
 static dit_status run_block(dit_model* m, int blk, float* x, float* xc, const float* mod, const float* modc,
                             int64_t mod_bstride, const void* kc, const void* vc, int B, int N, int L,
                             bool ctx_out_needed, const BlockBufs& bb, cudaStream_t s) {
+  NvtxRange range("dit.block %d", blk);
   const dit_config& c = m->cfg;
   const int D = c.hidden, F = c.mlp;
   const float eps = c.ln_eps;
@@ -821,31 +875,6 @@ extern "C" dit_status dit_timestep_modulation(dit_model* m, const float* t_host,
   return DIT_OK;
 }
 
-// ------------------------------------------------------------ no-allocation variant
-// Scratch of dit_timestep_modulation_noalloc: DIT_NOALLOC_MAX_BATCH timesteps
-// followed by DIT_NOALLOC_MAX_HIDDEN hidden activations, in module memory
-// that is never allocated or freed by a call.  In host code the symbol is a
-// host-side stand-in, so its device address is looked up once per device.
-static __device__ __align__(256) float g_noalloc_scratch[DIT_NOALLOC_MAX_BATCH + DIT_NOALLOC_MAX_HIDDEN];
-static std::mutex g_noalloc_mutex;
-static std::unordered_map<int, float*> g_noalloc_addr;  // device -> device address of the scratch
-
-static dit_status noalloc_scratch(int device, float** out) {
-  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  auto it = g_noalloc_addr.find(device);
-  if (it != g_noalloc_addr.end()) {
-    *out = it->second;
-    return DIT_OK;
-  }
-  void* p = nullptr;
-  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // caller made `device` current
-  if (e != cudaSuccess || !p)
-    return fail(DIT_ERR_CUDA, "cudaGetSymbolAddress of the fixed scratch failed: %s", cudaGetErrorString(e));
-  g_noalloc_addr[device] = static_cast<float*>(p);
-  *out = static_cast<float*>(p);
-  return DIT_OK;
-}
-
 extern "C" dit_status dit_timestep_modulation_noalloc(dit_model* m, const float* t_host, int batch, float* mod,
                                                       void* stream) {
   g_last_error[0] = 0;
@@ -857,18 +886,20 @@ extern "C" dit_status dit_timestep_modulation_noalloc(dit_model* m, const float*
   if ((int64_t)batch * m->cfg.hidden > DIT_NOALLOC_MAX_HIDDEN)
     return fail(DIT_ERR_INVALID_ARG, "batch * hidden = %lld exceeds the fixed scratch limit of %d floats",
                 (long long)batch * m->cfg.hidden, (int)DIT_NOALLOC_MAX_HIDDEN);
+  if (m->cfg.hidden > kTimestepMlpMaxHidden || m->cfg.freq_dim > kTimestepMlpMaxHidden)
+    return fail(DIT_ERR_INVALID_ARG, "hidden %d / freq_dim %d exceed the timestep MLP limit of %d", m->cfg.hidden,
+                m->cfg.freq_dim, kTimestepMlpMaxHidden);
   for (int b = 0; b < batch; ++b)
     if (!isfinite(t_host[b])) return fail(DIT_ERR_INVALID_ARG, "timestep %d is not finite", b);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CU_TRY(cudaSetDevice(m->device));
-  float* scratch = nullptr;
-  DIT_TRY(noalloc_scratch(m->device, &scratch));
+  float* scratch = m->noalloc_scratch;
   float* t_dev = scratch;                          // [batch] timesteps
   float* hidden = scratch + DIT_NOALLOC_MAX_BATCH;  // [batch, hidden], fully written by fc1 before fc2 reads it
   CU_TRY(cudaMemcpyAsync(t_dev, t_host, batch * sizeof(float), cudaMemcpyHostToDevice, s));
-  K_TRY(timestep_mlp(t_dev, 0.0, batch, m->cfg.freq_dim, m->cfg.hidden, m->W("time_mlp.fc1.weight"),
-                     m->V("time_mlp.fc1.bias"), m->W("time_mlp.fc2.weight"), m->V("time_mlp.fc2.bias"), m->bf16,
-                     hidden, mod, s));
+  LAUNCH(DIT_KERNEL_SMALL, 2, timestep_mlp(t_dev, 0.0, batch, m->cfg.freq_dim, m->cfg.hidden, m->W("time_mlp.fc1.weight"),
+                                            m->V("time_mlp.fc1.bias"), m->W("time_mlp.fc2.weight"),
+                                            m->V("time_mlp.fc2.bias"), m->bf16, hidden, mod, s));
   return DIT_OK;
 }
 
@@ -990,7 +1021,10 @@ extern "C" dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, 
   if (!latents || !cond) return fail(DIT_ERR_INVALID_ARG, "NULL latents or cond");
   if (cond_len <= 0) return fail(DIT_ERR_SHAPE, "cond_len must be positive");
   if (n_steps <= 0 || !sigmas) return fail(DIT_ERR_INVALID_ARG, "need n_steps > 0 and n_steps + 1 sigmas");
-  if (flags & ~(uint32_t)DIT_LOOP_PARTIAL_SCHEDULE) return fail(DIT_ERR_INVALID_ARG, "unknown flags");
+  if (flags & ~(uint32_t)(DIT_LOOP_PARTIAL_SCHEDULE | DIT_LOOP_CUDA_GRAPH))
+    return fail(DIT_ERR_INVALID_ARG, "unknown flags");
+  if ((flags & DIT_LOOP_CUDA_GRAPH) && m->prof_timing)
+    return fail(DIT_ERR_INVALID_ARG, "DIT_LOOP_CUDA_GRAPH cannot be combined with per-launch timing (dit_profile_start)");
   if (!isfinite(guidance)) return fail(DIT_ERR_INVALID_ARG, "guidance is not finite");
   if (!uncond && guidance != 1.0f)
     return fail(DIT_ERR_INVALID_ARG, "guidance %g needs negative condition tokens (uncond is NULL)", guidance);
@@ -1020,6 +1054,7 @@ extern "C" dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, 
   need += (size_t)B * L * D * 4;                                                // xc
   need += (size_t)B * N * P * a + (size_t)B * N * P * 4;                        // tokens, vt
   if (c.cond_mode == DIT_COND_CROSS) need += (size_t)c.depth * 2 * B * L * D * a;  // K/V cache
+  need += (size_t)(n_steps + 1) * sizeof(float) + sizeof(int);                  // schedule, step counter
   need += 64 * 256;
   DIT_TRY(ensure_ws(m, need));
   Workspace w{m->ws, m->ws_bytes, 0};
@@ -1034,6 +1069,8 @@ extern "C" dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, 
   void* tokens = w.take((size_t)B * N * P * a);
   float* vt = static_cast<float*>(w.take((size_t)B * N * P * 4));
   void* kvcache = c.cond_mode == DIT_COND_CROSS ? w.take((size_t)c.depth * 2 * B * L * D * a) : nullptr;
+  int* step_dev = static_cast<int*>(w.take(sizeof(int)));
+  float* sig_dev = static_cast<float*>(w.take((size_t)(n_steps + 1) * sizeof(float)));
 
   // condition rows: [cond (Bq); uncond (Bq)]
   const size_t cond_bytes = (size_t)Bq * L * c.cond_dim * 4;
@@ -1057,10 +1094,18 @@ extern "C" dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, 
       DIT_TRY(cross_kv(m, blk, ca, B, L, kb, kb + per, s));
     }
   }
-  for (int i = 0; i < n_steps; ++i) {
-    const double t = (double)c.timestep_scale * (double)sigmas[i];
-    LAUNCH(DIT_KERNEL_SMALL, 2, timestep_mlp(nullptr, t, 1, c.freq_dim, D, m->W("time_mlp.fc1.weight"), m->V("time_mlp.fc1.bias"),
-                       m->W("time_mlp.fc2.weight"), m->V("time_mlp.fc2.bias"), m->bf16, thid, mvec, s));
+  // Device copy of the schedule and a step counter: every step reads its
+  // timestep and Euler increment from them, so the launches of a step are
+  // the same for every step (and can be captured once and replayed).
+  CU_TRY(cudaMemcpyAsync(sig_dev, sigmas, (size_t)(n_steps + 1) * sizeof(float), cudaMemcpyHostToDevice, s));
+  CU_TRY(cudaMemsetAsync(step_dev, 0, sizeof(int), s));
+  const size_t per = (size_t)B * L * D * a;
+  auto enqueue_step = [&](cudaStream_t s) -> dit_status {
+    NvtxRange range("dit.step");
+    LAUNCH(DIT_KERNEL_SMALL, 2, timestep_mlp_sched(sig_dev, step_dev, (double)c.timestep_scale, c.freq_dim, D,
+                                                   m->W("time_mlp.fc1.weight"), m->V("time_mlp.fc1.bias"),
+                                                   m->W("time_mlp.fc2.weight"), m->V("time_mlp.fc2.bias"), m->bf16,
+                                                   thid, mvec, s));
     LAUNCH(DIT_KERNEL_SMALL, 1, add_tables(mvec, 1, D, 6, m->V("blocks.0.mod_table"), c.depth, tabs, s));
     if (tabs_c) LAUNCH(DIT_KERNEL_SMALL, 1, add_tables(mvec, 1, D, 6, m->V("blocks.0.ctx.mod_table"), c.depth, tabs_c, s));
     LAUNCH(DIT_KERNEL_SMALL, 1, add_tables(mvec, 1, D, 2, m->V("head.mod_table"), 1, headtab, s));
@@ -1072,7 +1117,6 @@ extern "C" dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, 
       CU_TRY(cudaMemcpyAsync(xc, cond, cond_bytes, cudaMemcpyDeviceToDevice, s));
       if (cfg) CU_TRY(cudaMemcpyAsync(xc + (size_t)Bq * L * D, uncond, cond_bytes, cudaMemcpyDeviceToDevice, s));
     }
-    const size_t per = (size_t)B * L * D * a;
     for (int blk = 0; blk < c.depth; ++blk) {
       const void* kc = nullptr;
       const void* vc = nullptr;
@@ -1087,9 +1131,69 @@ extern "C" dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, 
     LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, (int64_t)B * N, D, N, headtab, headtab + D, 0, c.ln_eps, bb.h, m->bf16, m->d_err, m->num_sms, s));
     DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_EMBED, bb.h, (int64_t)B * N, D, D, m->W("head.weight"), P,
                     epi_store(EPI_F32, m->V("head.bias"), vt, P), s));
-    const float dsig = (float)((double)sigmas[i + 1] - (double)sigmas[i]);
-    LAUNCH(DIT_KERNEL_SMALL, 1, cfg_euler_tokens(vt, Bq, cfg, guidance, dsig, c.in_channels, thw[0], thw[1], thw[2], c.patch[0],
-                           c.patch[1], c.patch[2], latents, s));
+    LAUNCH(DIT_KERNEL_CFG_EULER, 1, cfg_euler_tokens(vt, Bq, cfg, guidance, sig_dev, step_dev, c.in_channels, thw[0], thw[1],
+                                                     thw[2], c.patch[0], c.patch[1], c.patch[2], latents, m->d_err, s));
+    LAUNCH(DIT_KERNEL_SMALL, 1, step_advance(step_dev, s));
+    return DIT_OK;
+  };
+  if (!(flags & DIT_LOOP_CUDA_GRAPH)) {
+    for (int i = 0; i < n_steps; ++i) DIT_TRY(enqueue_step(s));
+    return DIT_OK;
+  }
+  // Graph path: the step is captured once on the model's own stream (nothing
+  // runs during capture) and replayed n_steps times on the caller's stream.
+  // The capture is reused while every pointer and scalar it holds is the same.
+  float gbits = guidance;
+  uint32_t gu = 0;
+  memcpy(&gu, &gbits, sizeof(gu));
+  const std::vector<uint64_t> key = {
+      (uint64_t)(uintptr_t)latents, (uint64_t)(uintptr_t)cond,  (uint64_t)(uintptr_t)uncond,
+      (uint64_t)(uintptr_t)m->ws,   (uint64_t)m->ws_bytes,      (uint64_t)(uintptr_t)m->rope,
+      (uint64_t)Bq,                 (uint64_t)thw[0],           (uint64_t)thw[1],
+      (uint64_t)thw[2],             (uint64_t)L,                (uint64_t)gu,
+      (uint64_t)(uintptr_t)sig_dev, (uint64_t)(uintptr_t)step_dev};
+  if (!m->graph.exec || m->graph.key != key) {
+    if (m->graph.exec) {
+      cudaGraphExecDestroy(m->graph.exec);
+      m->graph.exec = nullptr;
+    }
+    if (!m->capture_stream) CU_TRY(cudaStreamCreateWithFlags(&m->capture_stream, cudaStreamNonBlocking));
+    // the capture stream starts after the schedule upload and counter reset above
+    cudaEvent_t ready = nullptr;
+    CU_TRY(cudaEventCreateWithFlags(&ready, cudaEventDisableTiming));
+    cudaError_t e = cudaEventRecord(ready, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(m->capture_stream, ready, 0);
+    cudaEventDestroy(ready);
+    if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "ordering the capture stream failed: %s", cudaGetErrorString(e));
+    int64_t before[DIT_KERNEL_KINDS];
+    memcpy(before, m->prof_counts, sizeof(before));
+    CU_TRY(cudaStreamBeginCapture(m->capture_stream, cudaStreamCaptureModeRelaxed));
+    m->capturing = true;
+    const dit_status st = enqueue_step(m->capture_stream);
+    m->capturing = false;
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(m->capture_stream, &graph);
+    if (st != DIT_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return st;
+    }
+    if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "capturing the loop step failed: %s", cudaGetErrorString(e));
+    e = cudaGraphInstantiate(&m->graph.exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+      m->graph.exec = nullptr;
+      return fail(DIT_ERR_CUDA, "instantiating the loop step graph failed: %s", cudaGetErrorString(e));
+    }
+    // the capture launched nothing: its launches are counted when replayed
+    for (int k = 0; k < DIT_KERNEL_KINDS; ++k) {
+      m->graph.counts[k] = m->prof_counts[k] - before[k];
+      m->prof_counts[k] = before[k];
+    }
+    m->graph.key = key;
+  }
+  for (int i = 0; i < n_steps; ++i) {
+    CU_TRY(cudaGraphLaunch(m->graph.exec, s));
+    for (int k = 0; k < DIT_KERNEL_KINDS; ++k) m->prof_counts[k] += m->graph.counts[k];
   }
   return DIT_OK;
 }
@@ -1103,6 +1207,8 @@ extern "C" dit_status dit_synchronize(dit_model* m, void* stream) {
   CU_TRY(cudaMemcpy(&h, m->d_err, sizeof(int), cudaMemcpyDeviceToHost));
   if (h) {
     CU_TRY(cudaMemset(m->d_err, 0, sizeof(int)));
+    if (h >= DIT_BOUNDS_SITE_MIN && h <= DIT_BOUNDS_SITE_MAX)
+      return fail(DIT_ERR_CUDA, "device bounds check failed (site %d, debug build); outputs are invalid", h);
     return fail(DIT_ERR_TIMEOUT, "a kernel abandoned a bounded wait (site %d); outputs are invalid", h);
   }
   return DIT_OK;

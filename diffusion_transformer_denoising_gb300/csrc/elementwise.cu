@@ -165,6 +165,11 @@ __global__ void __launch_bounds__(LN_STAGED_THREADS, 1)
           if (!ok) break;
         }
         const int row = (int)blockIdx.x + k * (int)gridDim.x;
+        if (!DIT_BOUNDS(row >= 0 && row < rows && slot >= 0 && slot < stages, err, 64)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
         const float* src = row < rows0 ? P.s[0].x + (int64_t)row * D : P.s[1].x + (int64_t)(row - rows0) * D;
         mbar_arrive_expect_tx(&full[slot], row_bytes);
         bulk_load(ring + (size_t)slot * D, src, row_bytes, &full[slot]);
@@ -219,6 +224,7 @@ __global__ void __launch_bounds__(LN_STAGED_THREADS, 1)
     const int lr = row - sg * rows0;
     const LnSeg& g = P.s[sg];
     const int e = g.mod0 + lr / g.rpb;
+    if (!DIT_BOUNDS(lr >= 0 && lr < g.rows && (!modulate || (e >= 0 && e < P.nmod)), err, 65)) break;
     const float4* sh4 = smod + (size_t)(2 * e) * n4;
     const float4* sc4 = sh4 + n4;
     uint2* dst = reinterpret_cast<uint2*>(g.out + (int64_t)lr * D);
@@ -371,12 +377,15 @@ DIT_DEV float wload<__nv_bfloat16>(const __nv_bfloat16* w, int64_t i) { return _
 // hidden[b, j] = SiLU(W1[j, :] . e(t_b) + b1[j]); one warp per output.
 // The sinusoid's arguments reach 1000 rad, so they are formed in double.
 template <typename WT>
-__global__ void __launch_bounds__(256) temb_fc1_kernel(const float* t_dev, double t0, int fq, int D,
+__global__ void __launch_bounds__(256) temb_fc1_kernel(const float* t_dev, double t0, const float* sig,
+                                                       const int* step, int fq, int D,
                                                        const WT* __restrict__ w1, const float* __restrict__ b1,
                                                        float* hidden) {
   extern __shared__ float e[];
   const int b = blockIdx.y;
-  const double t = t_dev ? (double)t_dev[b] : t0;
+  // t per batch element from t_dev, or t0 * sig[*step] (t0 = the timestep
+  // scale) from the loop's device schedule, or t0 itself
+  const double t = t_dev ? (double)t_dev[b] : (sig ? t0 * (double)sig[*step] : t0);
   const int half = fq / 2;
   for (int k = threadIdx.x; k < half; k += blockDim.x) {
     const double a = t * pow(10000.0, -(double)k / (double)half);
@@ -413,21 +422,52 @@ __global__ void __launch_bounds__(256) temb_fc2_kernel(int D, const WT* __restri
   if (lane == 0) mod[(int64_t)b * 6 * D + i] = acc + b2[i];
 }
 
-cudaError_t timestep_mlp(const float* t_dev, double t0, int batch, int fq, int D, const void* w1, const float* b1,
-                         const void* w2, const float* b2, bool w_bf16, float* hidden, float* mod, cudaStream_t s) {
+static cudaError_t timestep_mlp_any(const float* t_dev, double t0, const float* sig, const int* step, int batch,
+                                    int fq, int D, const void* w1, const float* b1, const void* w2, const float* b2,
+                                    bool w_bf16, float* hidden, float* mod, cudaStream_t s) {
   dim3 g1((D + 7) / 8, batch), g2((6 * D + 7) / 8, batch);
   if (w_bf16) {
     temb_fc1_kernel<__nv_bfloat16><<<g1, 256, fq * sizeof(float), s>>>(
-        t_dev, t0, fq, D, static_cast<const __nv_bfloat16*>(w1), b1, hidden);
+        t_dev, t0, sig, step, fq, D, static_cast<const __nv_bfloat16*>(w1), b1, hidden);
     temb_fc2_kernel<__nv_bfloat16><<<g2, 256, D * sizeof(float), s>>>(
         D, static_cast<const __nv_bfloat16*>(w2), b2, hidden, mod);
   } else {
-    temb_fc1_kernel<float><<<g1, 256, fq * sizeof(float), s>>>(t_dev, t0, fq, D, static_cast<const float*>(w1),
-                                                               b1, hidden);
+    temb_fc1_kernel<float><<<g1, 256, fq * sizeof(float), s>>>(t_dev, t0, sig, step, fq, D,
+                                                               static_cast<const float*>(w1), b1, hidden);
     temb_fc2_kernel<float><<<g2, 256, D * sizeof(float), s>>>(D, static_cast<const float*>(w2), b2, hidden,
                                                               mod);
   }
   return cudaGetLastError();
+}
+
+cudaError_t timestep_mlp(const float* t_dev, double t0, int batch, int fq, int D, const void* w1, const float* b1,
+                         const void* w2, const float* b2, bool w_bf16, float* hidden, float* mod, cudaStream_t s) {
+  return timestep_mlp_any(t_dev, t0, nullptr, nullptr, batch, fq, D, w1, b1, w2, b2, w_bf16, hidden, mod, s);
+}
+
+cudaError_t timestep_mlp_sched(const float* sig, const int* step, double scale, int fq, int D, const void* w1,
+                               const float* b1, const void* w2, const float* b2, bool w_bf16, float* hidden,
+                               float* mod, cudaStream_t s) {
+  return timestep_mlp_any(nullptr, scale, sig, step, 1, fq, D, w1, b1, w2, b2, w_bf16, hidden, mod, s);
+}
+
+__global__ void step_advance_kernel(int* step) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) *step += 1;
+}
+
+cudaError_t step_advance(int* step, cudaStream_t s) {
+  step_advance_kernel<<<1, 32, 0, s>>>(step);
+  return cudaGetLastError();
+}
+
+cudaError_t timestep_mlp_preload(bool w_bf16) {
+  cudaFuncAttributes a;
+  cudaError_t e = w_bf16 ? cudaFuncGetAttributes(&a, temb_fc1_kernel<__nv_bfloat16>)
+                         : cudaFuncGetAttributes(&a, temb_fc1_kernel<float>);
+  if (e == cudaSuccess)
+    e = w_bf16 ? cudaFuncGetAttributes(&a, temb_fc2_kernel<__nv_bfloat16>)
+               : cudaFuncGetAttributes(&a, temb_fc2_kernel<float>);
+  return e;
 }
 
 // ---------------------------------------------------------------- modulation tables
@@ -526,8 +566,17 @@ cudaError_t unpatchify(const float* tok, int B, int C, int T, int H, int W, int 
 }
 
 // ---------------------------------------------------------------- guidance + Euler
-__global__ void cfg_euler_tokens_kernel(const float* __restrict__ vt, int Bl, int cfg, float gs, float dsig,
-                                        PatchGeom g, float* __restrict__ lat) {
+// Euler increment of the loop's current step: sigma[i+1] - sigma[i] of the
+// device schedule, rounded once to fp32 (the host-side flow_euler_step rounds
+// the same difference of the same values).
+DIT_DEV float sched_dsig(const float* sig, const int* step) {
+  const int i = *step;
+  return (float)((double)sig[i + 1] - (double)sig[i]);
+}
+
+__global__ void cfg_euler_tokens_kernel(const float* __restrict__ vt, int Bl, int cfg, float gs, const float* sig,
+                                        const int* step, PatchGeom g, float* __restrict__ lat) {
+  const float dsig = sched_dsig(sig, step);
   const int64_t per = (int64_t)g.C * g.T * g.H * g.W;
   const int64_t n = (int64_t)Bl * per;
   const int64_t half = (int64_t)Bl * g.N * g.P;
@@ -547,12 +596,102 @@ __global__ void cfg_euler_tokens_kernel(const float* __restrict__ vt, int Bl, in
   }
 }
 
-cudaError_t cfg_euler_tokens(const float* vt, int Bl, bool cfg, float gs, float dsig, int C, int T, int H, int W,
-                             int pt, int ph, int pw, float* lat, cudaStream_t s) {
+// Coalesced form: one CTA per grid row of tokens (batch b, grid t index it,
+// grid h index ih; its gw tokens are gw*P contiguous floats in token layout).
+// One thread copies the row of both passes' velocities into shared memory
+// with bulk copies while every thread loads the latent float4s it will
+// update (the C*pt*ph latent rows the tokens cover), so all of a CTA's loads
+// are in flight together; then guidance + Euler and 128-bit stores.  Needs
+// W % 4 == 0, P % 4 == 0 and 16-byte aligned buffers.
+constexpr int CE_PER_THREAD = 4;  // latent float4s a thread keeps in flight
+__global__ void __launch_bounds__(128, 8) cfg_euler_rows_kernel(const float* __restrict__ vt, int Bl, int cfg, float gs,
+                                                            const float* sig, const int* step, PatchGeom g,
+                                                            float* __restrict__ lat, int* err) {
+  extern __shared__ __align__(16) uint8_t ce_smem[];
+  __shared__ int ce_abort;
+  const int row_floats = g.gw * g.P;
+  float* vcs = reinterpret_cast<float*>(ce_smem);
+  float* vus = vcs + row_floats;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(vus + row_floats);
+  const int ih = blockIdx.x % g.gh;
+  const int it = (blockIdx.x / g.gh) % g.gt;
+  const int b = blockIdx.x / (g.gh * g.gt);
+  const int64_t tok0 = ((int64_t)b * g.N + ((int64_t)it * g.gh + ih) * g.gw) * g.P;  // first float of the row
+  const int64_t half = (int64_t)Bl * g.N * g.P;
+  if (threadIdx.x == 0) {
+    ce_abort = 0;
+    mbar_init(bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t bytes = (uint32_t)row_floats * 4u;
+    mbar_arrive_expect_tx(bar, cfg ? 2 * bytes : bytes);
+    bulk_load(vcs, vt + tok0, bytes, bar);
+    if (cfg) bulk_load(vus, vt + half + tok0, bytes, bar);
+  }
+  const float dsig = sched_dsig(sig, step);
+  const int wq = g.W / 4;
+  const int n4 = g.C * g.pt * g.ph * wq;
+  // latent float4 k of the CTA: latent row (c, a, e) = k / wq, columns w0..w0+3
+  auto lat_index = [&](int k, int* jrow, int* w0) -> int64_t {
+    const int row = k / wq;
+    *w0 = (k - row * wq) * 4;
+    const int e = row % g.ph, a = (row / g.ph) % g.pt, c = row / (g.ph * g.pt);
+    *jrow = ((c * g.pt + a) * g.ph + e) * g.pw;  // patch index of (c, a, e, 0)
+    return ((((int64_t)b * g.C + c) * g.T + it * g.pt + a) * g.H + ih * g.ph + e) * g.W + *w0;
+  };
+  bool waited = false, ok = true;
+  for (int base = threadIdx.x; base < n4; base += blockDim.x * CE_PER_THREAD) {
+    float4 x[CE_PER_THREAD];
+#pragma unroll
+    for (int q = 0; q < CE_PER_THREAD; ++q) {
+      const int k = base + q * (int)blockDim.x;
+      if (k >= n4) break;
+      int jrow, w0;
+      x[q] = *reinterpret_cast<const float4*>(lat + lat_index(k, &jrow, &w0));
+    }
+    if (!waited) {
+      ok = mbar_wait(bar, 0, &ce_abort, err, 43);
+      waited = true;
+    }
+    if (!ok) break;
+#pragma unroll
+    for (int q = 0; q < CE_PER_THREAD; ++q) {
+      const int k = base + q * (int)blockDim.x;
+      if (k >= n4) break;
+      int jrow, w0;
+      const int64_t li = lat_index(k, &jrow, &w0);
+      float xv[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int w = w0 + r, iw = w / g.pw;
+        const int idx = iw * g.P + jrow + (w - iw * g.pw);
+        const float vc = vcs[idx];
+        const float v = cfg ? fmaf(gs, vc - vus[idx], vus[idx]) : vc;
+        xv[r] = fmaf(dsig, v, xv[r]);
+      }
+      *reinterpret_cast<float4*>(lat + li) = make_float4(xv[0], xv[1], xv[2], xv[3]);
+    }
+  }
+  // the copies land before the CTA exits, whichever threads had work
+  if (!waited && threadIdx.x == 0) mbar_wait(bar, 0, &ce_abort, err, 43);
+}
+
+cudaError_t cfg_euler_tokens(const float* vt, int Bl, bool cfg, float gs, const float* sig, const int* step, int C,
+                             int T, int H, int W, int pt, int ph, int pw, float* lat, int* err, cudaStream_t s) {
   const PatchGeom g = geom(C, T, H, W, pt, ph, pw);
   const int64_t n = (int64_t)Bl * C * T * H * W;
   if (n == 0) return cudaSuccess;
-  cfg_euler_tokens_kernel<<<blocks_for(n, 256), 256, 0, s>>>(vt, Bl, cfg ? 1 : 0, gs, dsig, g, lat);
+  const size_t row_bytes = (size_t)g.gw * g.P * sizeof(float);
+  const bool aligned = ((reinterpret_cast<uintptr_t>(vt) | reinterpret_cast<uintptr_t>(lat)) & 15) == 0;
+  const int64_t nrows = (int64_t)Bl * g.gt * g.gh;
+  const size_t smem = 2 * row_bytes + 16;
+  if (aligned && W % 4 == 0 && g.P % 4 == 0 && smem <= 48 * 1024 && nrows <= INT32_MAX) {
+    cfg_euler_rows_kernel<<<(int)nrows, 128, smem, s>>>(vt, Bl, cfg ? 1 : 0, gs, sig, step, g, lat, err);
+  } else {
+    cfg_euler_tokens_kernel<<<blocks_for(n, 256), 256, 0, s>>>(vt, Bl, cfg ? 1 : 0, gs, sig, step, g, lat);
+  }
   return cudaGetLastError();
 }
 

@@ -108,7 +108,7 @@ DIT_DEV int locate_tile(const GemmBatch<NP>& P, int tile, int* t) {
 // as its last tcgen05.ld has completed.
 template <int BN, int UW>
 DIT_DEV void drain_tile_tma(const EpiParams& ep, const EpiMaps& maps, uint32_t tacc, int64_t row0, int64_t M, int N,
-                            int nb, int half, uint8_t* stg, uint64_t* tempty_bar) {
+                            int nb, int half, uint8_t* stg, uint64_t* tempty_bar, int* err) {
   constexpr int NU = BN / UW;
   const int lane = threadIdx.x & 31;
   const int64_t row = row0 + lane;
@@ -177,7 +177,10 @@ DIT_DEV void drain_tile_tma(const EpiParams& ep, const EpiMaps& maps, uint32_t t
         const int sec = col0 / ep.D;
         const int cc = col0 - sec * ep.D;
         const int h = cc / ep.hd;
-        tma_store_3d(&maps.m[sec], stg, cc - h * ep.hd, ep.tok_off + t0, (int)(b * ep.H + h));
+        if (DIT_BOUNDS(sec >= 0 && sec < 3 && ep.dst[sec] && cc - h * ep.hd + UW <= ep.hd && h < ep.H &&
+                           ep.tok_off + t0 + 32 <= ep.seq_total && (b + 1) * ep.rows_per_batch <= M,
+                       err, 61))
+          tma_store_3d(&maps.m[sec], stg, cc - h * ep.hd, ep.tok_off + t0, (int)(b * ep.H + h));
       } else {
         tma_store_2d(&maps.m[0], stg, col0, (int)row0);
       }
@@ -247,6 +250,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         int t, mb, nb;
         const int p = locate_tile(P, tile, &t);
         tile_coords(t, P.m_tiles[p], n_tiles, P.group_n, &mb, &nb);
+        if (!DIT_BOUNDS(p >= 0 && p < NP && mb >= 0 && mb < P.m_tiles[p] && nb >= 0 && nb < n_tiles, err, 60)) {
+          *abort_flag = 1;  // the other roles' waits return at once: the CTA winds down
+          ok = false;
+          break;
+        }
         const CUtensorMap* tmA = &P.tmA[p];
         const CUtensorMap* tmB = &P.tmB[p];
         // Short main loops (K <= 2048): the residual rows this tile adds into
@@ -339,9 +347,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (ep.tma) {
         const int64_t row0 = (int64_t)mb * C::BM + q * 32;
         if (ep.kind == EPI_F32 || ep.kind == EPI_RESID)
-          drain_tile_tma<BN, 32>(ep, P.maps[p], tacc, row0, M, N, nb, half, stg, &tempty[acc]);
+          drain_tile_tma<BN, 32>(ep, P.maps[p], tacc, row0, M, N, nb, half, stg, &tempty[acc], err);
         else
-          drain_tile_tma<BN, 64>(ep, P.maps[p], tacc, row0, M, N, nb, half, stg, &tempty[acc]);
+          drain_tile_tma<BN, 64>(ep, P.maps[p], tacc, row0, M, N, nb, half, stg, &tempty[acc], err);
         continue;
       }
       const int64_t row = (int64_t)mb * C::BM + row_in_tile;

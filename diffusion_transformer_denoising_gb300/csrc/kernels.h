@@ -6,6 +6,12 @@
 
 namespace dit {
 
+// Error-word sites: bounded waits that gave up use 1..59 (and the stall test
+// hook its own site); the checks of the debug bounds build
+// (-DDIT_DEBUG_BOUNDS) use DIT_BOUNDS_SITE_MIN..DIT_BOUNDS_SITE_MAX.
+constexpr int DIT_BOUNDS_SITE_MIN = 60;
+constexpr int DIT_BOUNDS_SITE_MAX = 79;
+
 // ------------------------------------------------------------------ GEMM
 // C[M, N] = A[M, K] . W[N, K]^T (+ bias), followed by one fused epilogue.
 enum EpiKind : int {
@@ -106,6 +112,20 @@ cudaError_t ln_modulate_pair(const LnArgs& a, const LnArgs& b, int D, float eps,
 cudaError_t timestep_mlp(const float* t_dev, double t0, int batch, int freq_dim, int D, const void* w1, const float* b1,
                          const void* w2, const float* b2, bool w_bf16, float* hidden_scratch, float* mod,
                          cudaStream_t s);
+// Loads the timestep MLP's kernels for the current device (under lazy module
+// loading a kernel's code is otherwise loaded, and its device memory taken,
+// at its first launch).
+cudaError_t timestep_mlp_preload(bool w_bf16);
+// The loop's timestep MLP: t = scale * sig[*step] from the device schedule
+// and step counter (batch 1).
+cudaError_t timestep_mlp_sched(const float* sig, const int* step, double scale, int freq_dim, int D, const void* w1,
+                               const float* b1, const void* w2, const float* b2, bool w_bf16, float* hidden,
+                               float* mod, cudaStream_t s);
+// *step += 1 (one thread), enqueued at the end of every loop step.
+cudaError_t step_advance(int* step, cudaStream_t s);
+// Largest hidden width whose activation vector the second MLP kernel keeps
+// in shared memory without an opt-in (48 KB).
+constexpr int kTimestepMlpMaxHidden = 12288;
 // out[k, b, j, c] = mod[b, j*D + c] + tables[k, j, c] for k < ntab, j < rows
 // (tables contiguous [ntab, rows, D]).
 cudaError_t add_tables(const float* mod, int batch, int D, int rows, const float* tables, int ntab, float* out,
@@ -118,8 +138,11 @@ cudaError_t unpatchify(const float* tok, int B, int C, int T, int H, int W, int 
                        cudaStream_t s);
 // Fused guidance + Euler + unpatchify over velocity tokens vt [2*Bl or Bl, N, P]:
 // lat += dsig * (vu + g (vc - vu)) (or vc alone when !cfg).
-cudaError_t cfg_euler_tokens(const float* vt, int Bl, bool cfg, float g, float dsig, int C, int T, int H, int W,
-                             int pt, int ph, int pw, float* lat, cudaStream_t s);
+// Guidance + Euler update of the loop, reading velocity tokens; the Euler
+// increment of the current step comes from the device schedule sig and the
+// device step counter.
+cudaError_t cfg_euler_tokens(const float* vt, int Bl, bool cfg, float g, const float* sig, const int* step, int C,
+                             int T, int H, int W, int pt, int ph, int pw, float* lat, int* err, cudaStream_t s);
 cudaError_t cfg_combine_kernel(const float* vc, const float* vu, float g, float* v, int64_t n, cudaStream_t s);
 cudaError_t euler_kernel(float* x, const float* v, float dsig, int64_t n, cudaStream_t s);
 cudaError_t f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t s);

@@ -14,13 +14,16 @@ import os
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libdit.so")
+# DIT_LIB selects another build of the same library (the debug build with
+# device-side bounds checks, libdit_debug.so); default: the release build.
+LIB_PATH = os.environ.get("DIT_LIB") or os.path.join(_PKG, "libdit.so")
 
 DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_SHAPE, DIT_ERR_NOT_LOADED, DIT_ERR_OOM, DIT_ERR_CUDA, DIT_ERR_TIMEOUT = range(7)
 PREC_BF16, PREC_F32 = 0, 1
 COND_CROSS, COND_JOINT = 0, 1
 DTYPE_F32, DTYPE_BF16 = 0, 1
 LOOP_PARTIAL_SCHEDULE = 1
+LOOP_CUDA_GRAPH = 2
 
 # every symbol include/dit.h declares
 EXPORTS = ["dit_create", "dit_load_weights", "dit_num_params", "dit_param_info", "dit_timestep_modulation",
@@ -31,7 +34,7 @@ EXPORTS = ["dit_create", "dit_load_weights", "dit_num_params", "dit_param_info",
 NOALLOC_MAX_BATCH, NOALLOC_MAX_HIDDEN = 64, 262144
 
 KERNEL_KINDS = ["gemm_qkv", "gemm_out", "gemm_cross_q", "gemm_cross_kv", "gemm_ffn1", "gemm_ffn2", "gemm_embed",
-                "attn_self", "attn_cross", "ln", "small"]
+                "attn_self", "attn_cross", "ln", "small", "cfg_euler"]
 
 
 class DitConfig(C.Structure):

@@ -27,6 +27,12 @@
  *     failure is a status code, with a message from dit_last_error().
  *   - There is no CPU fallback and no silent precision change: a call the
  *     GPU path cannot serve returns an error.
+ *   - One model owns one device workspace that every forward call of that
+ *     model reuses (block scratch, loop state, the timestep MLP's hidden
+ *     activations).  Calls on the same model must therefore be ordered on
+ *     the GPU: issue them on one stream, or order the streams with events.
+ *     Calls of one model on two unordered streams race on the workspace.
+ *     Separate models share nothing and may run concurrently.
  *   - Floating-point tensors crossing the ABI are float32, row-major, densely
  *     packed, in the layouts given per call.  B is the batch of network
  *     passes; in the loop B = 2 x requests with CFG (conditional passes
@@ -56,7 +62,10 @@ enum { DIT_PREC_BF16 = 0, DIT_PREC_F32 = 1 };
 enum { DIT_COND_CROSS = 0, DIT_COND_JOINT = 1 };
 enum { DIT_DTYPE_F32 = 0, DIT_DTYPE_BF16 = 1 };
 /* dit_denoise_loop flags */
-enum { DIT_LOOP_PARTIAL_SCHEDULE = 1 /* allow sigmas[0] != 1 or sigmas[n] != 0 */ };
+enum {
+  DIT_LOOP_PARTIAL_SCHEDULE = 1, /* allow sigmas[0] != 1 or sigmas[n] != 0                     */
+  DIT_LOOP_CUDA_GRAPH = 2        /* replay one captured step as a CUDA graph (see the loop call) */
+};
 
 /*
  * Model configuration, copied by dit_create.  Mirrors the C++ "*Config"
@@ -144,17 +153,19 @@ dit_status dit_timestep_modulation(dit_model* m, const float* t_host, int batch,
  * its own pool allocator, so any allocation by this library would fail or
  * stall.  (The pages have no counterpart; this is an interface addition.)
  * The call allocates nothing: it never calls cudaMalloc, cudaFree or any
- * allocating library routine.  Its scratch (the timesteps and the MLP's
- * hidden activations) lives in one fixed array of this library's device
- * memory (about 1 MiB), which every GPU that loads the library holds until
- * the process exits.
- *   batch <= DIT_NOALLOC_MAX_BATCH and batch * hidden <= DIT_NOALLOC_MAX_HIDDEN,
- *   otherwise DIT_ERR_INVALID_ARG (nothing is launched).
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  All
- * calls share the one array: calls whose work overlaps on the GPU (for
- * example on two streams without ordering between them) race with each
- * other.  Every byte of scratch a call reads it has written itself first. */
+ * allocating library routine, and it loads no module.  Its scratch (the
+ * timesteps and the MLP's hidden activations) lives in one fixed array of
+ * this library's device memory (about 1 MiB), which every GPU that loads the
+ * library holds until the process exits.
+ *   batch <= DIT_NOALLOC_MAX_BATCH, batch * hidden <= DIT_NOALLOC_MAX_HIDDEN,
+ *   and hidden, freq_dim <= 12288 (one activation vector held in 48 KB of
+ *   shared memory); otherwise DIT_ERR_INVALID_ARG (nothing is launched).
+ * Set-up happens in dit_create, with the model's device current: it looks up
+ * the array's device address on that device and loads the kernels this call
+ * launches.  So create the model before any stream capture.  All calls share
+ * the one array: calls whose work overlaps on the GPU (for example on two
+ * streams without ordering between them) race with each other.  Every byte
+ * of scratch a call reads it has written itself first. */
 enum { DIT_NOALLOC_MAX_BATCH = 64, DIT_NOALLOC_MAX_HIDDEN = 262144 };
 dit_status dit_timestep_modulation_noalloc(dit_model* m, const float* t_host, int batch, float* mod, void* stream);
 
@@ -166,7 +177,12 @@ dit_status dit_timestep_modulation_noalloc(dit_model* m, const float* t_host, in
 dit_status dit_patch_embed(dit_model* m, const float* latents, int batch, const int32_t latent_thw[3],
                            float* x, void* stream);
 
-/* a3-a9: one DiT block, in place on the residual stream(s).
+/* a3-a9: one DiT block, in place on the residual stream(s).  The network
+ * call of the pages (hidden_states = x, encoder_hidden_states = cond or xc,
+ * the timestep through `mod`: SGLang-Diffusion "Support New Diffusion
+ * Models", section 2 "Pipeline Config"), restricted to one block; rotary
+ * positions follow the token grid ("Verify the Port": rotary shape and style
+ * must match).
  *   block   0 .. depth-1
  *   x       device float[batch, N, hidden], image/video token stream, in/out
  *   xc      joint mode: device float[batch, cond_len, hidden], condition-token
@@ -187,15 +203,29 @@ dit_status dit_final_layer(dit_model* m, const float* x, const float* mod, int b
                            const int32_t latent_thw[3], float* v, void* stream);
 
 /* a11 (first half): classifier-free guidance v = vu + g (vc - vu) over n
- * floats (device pointers; v may alias vc or vu). */
+ * floats (device pointers; v may alias vc or vu).  The positive and negative
+ * passes and the guidance scale: SGLang-Diffusion "Support New Diffusion
+ * Models", section 1 "Sampling Params" (guidance_scale) and section 2
+ * "Pipeline Config" (pos/neg kwargs).  n < 0, a NULL pointer with n > 0 or a
+ * non-finite g: DIT_ERR_INVALID_ARG. */
 dit_status cfg_combine(const float* vc, const float* vu, float g, float* v, int64_t n, void* stream);
 
 /* a11 (second half): flow-matching Euler update x += (sigma_next - sigma) v
- * over n floats, in place on device x. */
+ * over n floats, in place on device x.  Flow prediction integrated on the
+ * shifted sigma schedule: stable-diffusion.cpp "Model Configuration
+ * Conventions", "Sampling And Geometry" (flow prediction, default flow
+ * shift, flow denoisers).  n < 0, a NULL pointer with n > 0 or a non-finite
+ * sigma: DIT_ERR_INVALID_ARG. */
 dit_status flow_euler_step(float* x, const float* v, float sigma, float sigma_next, int64_t n,
                            void* stream);
 
-/* The whole denoiser stage for `batch` requests.
+/* The whole denoiser stage for `batch` requests: the denoiser role of
+ * SGLang-Diffusion "Disaggregated Diffusion Pipeline" (Quick Start, role
+ * table), with the inputs that "Support New Diffusion Models" section 4 lists
+ * for the denoising stage (latents, the sigma schedule in the order used,
+ * positive and negative condition embeddings, number of steps); the error
+ * cases follow that page's "Verify the Port" failure points (reversed
+ * timesteps, missing negative embeddings with CFG on, latent shape).
  *   latents  device float[batch, C, T, H, W], initial noise in, denoised out
  *   cond     device float[batch, cond_len, cond_dim] positive condition
  *   uncond   device float[batch, cond_len, cond_dim] negative condition, or
@@ -208,6 +238,15 @@ dit_status flow_euler_step(float* x, const float* v, float sigma, float sigma_ne
  *   latents += (sigmas[i+1] - sigmas[i]) v.  Condition-token keys/values of
  *   cross-attention are computed once per call (they do not depend on the
  *   step). */
+/*   With DIT_LOOP_CUDA_GRAPH the launches of one step are captured once (on
+ *   a stream the model owns; nothing runs during the capture) into a CUDA
+ *   graph that is then launched n_steps times on `stream`.  Every step reads
+ *   its timestep and Euler increment from a device copy of `sigmas` through a
+ *   device step counter, so the same graph serves every step; the result is
+ *   bitwise the same as without the flag.  The graph is kept in the model and
+ *   reused by later calls whose pointers, shapes, guidance and n_steps are
+ *   the same; otherwise it is captured again.  Cannot be combined with
+ *   per-launch timing (dit_profile_start with timing on): DIT_ERR_INVALID_ARG. */
 dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, const int32_t latent_thw[3],
                             const float* cond, const float* uncond, int cond_len,
                             const float* sigmas, int n_steps, float guidance, uint32_t flags,
@@ -235,8 +274,9 @@ enum {
   DIT_KERNEL_ATTN_SELF = 7,
   DIT_KERNEL_ATTN_CROSS = 8,
   DIT_KERNEL_LN = 9,          /* LayerNorm + adaLN modulation                     */
-  DIT_KERNEL_SMALL = 10,      /* timestep MLP, tables, packing, CFG + Euler, casts */
-  DIT_KERNEL_KINDS = 11
+  DIT_KERNEL_SMALL = 10,      /* timestep MLP, tables, packing, casts             */
+  DIT_KERNEL_CFG_EULER = 11,  /* guidance + Euler update of the loop              */
+  DIT_KERNEL_KINDS = 12
 };
 dit_status dit_profile_start(dit_model* m, int timing);
 dit_status dit_profile_stop(dit_model* m, int64_t* counts, double* ms);

@@ -1,5 +1,8 @@
 """Helpers shared by the GPU tests: device upload, model construction from
 seeded weights, and the tolerance checks against the oracle."""
+import json
+import os
+
 import numpy as np
 
 from diffusion_transformer_denoising_gb300 import dit, synth
@@ -59,12 +62,42 @@ TOL_F32 = 1e-4
 TOL_BF16_BLOCK = 2e-2
 TOL_BF16_MAX = 5e-2
 COS_BF16_LOOP = 0.999
+# Regression bounds, about three times the largest errors the bf16 kernels
+# reached over every parity case (block outputs: RMS error 1.9e-3, largest
+# element 2.0e-2 of the output RMS, on the 3072-wide image block; block
+# updates, the output minus the input: RMS 2.6e-3, largest element 2.3e-2 of
+# the update's RMS).  Three times the largest element error of a block output
+# lies above the stated 5e-2, so there the stated bound is the tighter one.
+REG_BF16_RMS = 6e-3
+REG_BF16_MAX = TOL_BF16_MAX
+REG_UPDATE_RMS = 8e-3
+REG_UPDATE_MAX = 7e-2
 
 
-def assert_block_close(got, ref, scale=1.0):
-    """bf16 per-block criterion (RMS error and element bound), both scaled by `scale`."""
+def log_errors(case: str, **vals):
+    """Append measured errors to the file named by DIT_PARITY_LOG (if set), one
+    JSON object per line, so the regression bounds below can be checked
+    against what the kernels actually reach."""
+    path = os.environ.get("DIT_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+            f.write(json.dumps(dict(test=test, case=case, **{k: float(v) for k, v in vals.items()})) + "\n")
+
+
+def assert_block_close(got, ref, scale=1.0, case="", regress=True):
+    """bf16 per-block criterion (RMS error and element bound), both scaled by
+    `scale` (5 for a block's update); with `regress`, also the regression
+    bounds near three times the errors the kernels measured.  The measured
+    errors are in every message."""
     rms, mx = rel_rms_err(got, ref), rel_max_err(got, ref)
-    assert rms < scale * TOL_BF16_BLOCK and mx < scale * TOL_BF16_MAX, (rms, mx)
+    log_errors(case or "block", rms=rms, max=mx, scale=scale)
+    msg = f"{case}: RMS error {rms:.3e}, max error {mx:.3e} (of the reference RMS)"
+    assert rms < scale * TOL_BF16_BLOCK and mx < scale * TOL_BF16_MAX, "stated bound: " + msg
+    if regress:
+        # scale > 1 marks a check of the block's update (output minus input)
+        rr, rm = (REG_UPDATE_RMS, REG_UPDATE_MAX) if scale > 1 else (REG_BF16_RMS, REG_BF16_MAX)
+        assert rms < rr and mx < rm, f"regression bound (RMS {rr:.0e}, max {rm:.0e}): " + msg
 
 
 def small_bf16_cfg(mode=synth.COND_CROSS, **kw):

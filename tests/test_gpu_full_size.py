@@ -193,3 +193,24 @@ def test_video_embed_head_and_cfg_euler_full_size(video_block):
     dit.flow_euler_step(xl, out, 0.7, 0.65, n)
     ref = O.euler_step(lat[0], O.cfg_combine(gv[0], gv[1], 5.0), 0.7, 0.65)
     np.testing.assert_allclose(host(xl).reshape(ref.shape), ref, rtol=0, atol=1e-4)
+
+
+def test_image_block_sweep_batch8(image_model):
+    """Sweep point: batch 8 (four requests' CFG pairs) at 4096 + 512 tokens;
+    first and last batch items checked."""
+    cfg, W, m = image_model
+    _image_block_case(cfg, W, m, cfg["latent"], 8, (0, 7), seed=23)
+
+
+def test_image_block_sweep_1024_tokens(image_model):
+    """Sweep point: 1024 image tokens (32 x 32 grid) + 512 condition tokens."""
+    cfg, W, m = image_model
+    _image_block_case(cfg, W, m, (1, 64, 64), 2, (0, 1), seed=24)
+
+
+def test_image_block_sweep_65536_tokens(image_model):
+    """Sweep point: 65536 image tokens (256 x 256 grid) + 512 condition tokens,
+    batch 2: 516 key tiles, so the attention runs one CTA per item rather than
+    the persistent walk used for short key ranges."""
+    cfg, W, m = image_model
+    _image_block_case(cfg, W, m, (1, 512, 512), 2, (0,), seed=25)

@@ -294,3 +294,133 @@ def test_device_wait_timeout_is_reported_and_model_stays_usable(tiny):
     m.dit_timestep_modulation(t, out)
     m.dit_synchronize()
     assert rel_max_err(host(out)[0], O.timestep_modulation(500.0, W, cfg)) < TOL_F32
+
+
+# ------------------------------------------------------------------ more shapes and paths
+def test_bf16_k_and_n_tails():
+    """MLP width 648 and condition width 200 (multiples of 8, not of 64): the
+    GEMMs' last K block and the FFN1 output's last column tile are partial
+    (the tensor-map loads fill the missing K columns with zeros)."""
+    cfg = small_bf16_cfg(synth.COND_CROSS, mlp=648, cond_dim=200, depth=1)
+    W = synth.make_weights(cfg, seed=13)
+    m = make_model(cfg, W)
+    grid, L = (2, 9, 7), 37
+    N = int(np.prod(grid))
+    rng = np.random.default_rng(14)
+    x0 = (rng.standard_normal((2, N, cfg["hidden"])) * 0.5).astype(np.float32)
+    ctx = synth.make_cond(cfg, batch=2, seed=15, length=L)
+    mods = np.stack([O.timestep_modulation(t, W, cfg) for t in (250.0, 650.0)])
+    x = dev(x0)
+    m.dit_block_forward(0, x, None, dev(mods), dev(ctx), 2, grid, L)
+    m.dit_synchronize()
+    got = host(x)
+    for b in range(2):
+        ref = O.block_cross(x0[b], mods[b], ctx[b], W, 0, cfg, grid)
+        assert_block_close(got[b], ref, case=f"k_tails b{b}")
+        assert_block_close(got[b] - x0[b], ref - x0[b], 5, case=f"k_tails update b{b}")
+    m.close()
+
+
+def test_bf16_attention_rescale_paths():
+    """Peaked attention whose scores grow along the token order: the query and
+    key projections are equal and scaled by 8 (exact in bf16), and the tokens
+    lean more and more on one direction, so scores span ~180 log2 units and
+    most rows' maxima grow by far more than 2^8 after the first key tile.
+    This runs the attention kernel's slow paths (tile row max, rescale of O
+    and l, redone rows; large tile sums) on most tiles."""
+    cfg = small_bf16_cfg(synth.COND_CROSS, depth=1, rope_axes=(0, 0, 0))
+    W = synth.make_weights(cfg, seed=51)
+    D = cfg["hidden"]
+    wqkv = W["blocks.0.attn.qkv.weight"].copy()
+    wqkv[:D] *= 8.0
+    wqkv[D:2 * D] = wqkv[:D]
+    W["blocks.0.attn.qkv.weight"] = wqkv
+    m = make_model(cfg, W)
+    grid, L = (1, 20, 26), 64     # 520 tokens: 5 key tiles, the last one partial
+    N = int(np.prod(grid))
+    rng = np.random.default_rng(52)
+    u = rng.standard_normal(D)
+    x0 = (np.linspace(0.0, 4.0, N)[:, None] * u[None] + rng.standard_normal((N, D))).astype(np.float32)
+    mod = O.timestep_modulation(600.0, W, cfg)
+    # the case does what it claims: score span and growth along the key tiles
+    sh1, sc1 = O.block_modulation(mod, W["blocks.0.mod_table"], D)[:2]
+    h = O.modulate(O.layer_norm(x0, cfg["ln_eps"]), sh1, sc1)
+    q = O.linear(h, wqkv[:D], W["blocks.0.attn.qkv.bias"][:D])
+    k = O.linear(h, wqkv[D:2 * D], W["blocks.0.attn.qkv.bias"][D:2 * D])
+    s = q[:, :128] @ k[:, :128].T * (np.log2(np.e) / np.sqrt(128))
+    assert s.max() - s.min() > 20
+    assert np.mean(s[:, 384:512].max(1) - s[:, :128].max(1) > 8) > 0.5
+    ctx = synth.make_cond(cfg, batch=1, seed=53, length=L)
+    x = dev(x0[None])
+    m.dit_block_forward(0, x, None, dev(mod[None]), dev(ctx), 1, grid, L)
+    m.dit_synchronize()
+    got = host(x)[0]
+    ref = O.block_cross(x0, mod, ctx[0], W, 0, cfg, grid)
+    assert_block_close(got, ref, case="rescale")
+    assert_block_close(got - x0, ref - x0, 5, case="rescale update")
+    m.close()
+
+
+@pytest.mark.parametrize("which", ["tiny_fp32", "bf16_cross", "bf16_joint"])
+def test_loop_two_requests(which, tiny, small_cross, small_joint):
+    """dit_denoise_loop with batch = 2 requests, each with its own latent,
+    positive and (non-zero) negative condition: the CFG batch runs as
+    [cond(2); uncond(2)] and every request must match its own oracle loop."""
+    if which == "tiny_fp32":
+        cfg, W, m = tiny
+        thw, L, g = cfg["latent"], cfg["cond_len"], cfg["guidance"]
+    else:
+        cfg, W, m = small_cross if which == "bf16_cross" else small_joint
+        thw, L, g = ((2, 12, 16) if which == "bf16_cross" else (1, 16, 20)), 24, 4.0
+    lat = synth.make_latent(cfg, batch=2, seed=61, latent=thw)
+    cond = synth.make_cond(cfg, batch=2, seed=62, length=L)
+    unc = synth.make_cond(cfg, batch=2, seed=63, length=L) * np.float32(0.5)
+    sig = O.shift_sigma(O.sigma_schedule(3), 3.0).astype(np.float32)
+    x = dev(lat)
+    m.dit_denoise_loop(x, 2, thw, dev(cond), dev(unc), L, sig, g)
+    m.dit_synchronize()
+    got = host(x)
+    for r in range(2):
+        ref = O.denoise_loop(lat[r], cond[r], unc[r], W, cfg, sig.astype(np.float64), g)
+        if which == "tiny_fp32":
+            assert rel_max_err(got[r], ref) < TOL_F32
+            assert rel_max_err(got[r] - lat[r], ref - lat[r]) < 10 * TOL_F32
+        else:
+            assert cosine(got[r], ref) >= COS_BF16_LOOP
+            assert cosine(got[r] - lat[r], ref - lat[r]) >= 0.99
+
+
+@pytest.mark.parametrize("which", ["tiny_fp32", "bf16_cross", "bf16_joint"])
+def test_loop_cuda_graph_is_bitwise_eager(which, tiny, small_cross, small_joint):
+    """DIT_LOOP_CUDA_GRAPH replays one captured step: the final latents are
+    bitwise those of the eager launches, a second call reuses the capture,
+    a changed guidance scale is captured again, and the launch counts of the
+    replayed steps equal the eager ones."""
+    if which == "tiny_fp32":
+        cfg, W, m = tiny
+        thw, L = cfg["latent"], cfg["cond_len"]
+    else:
+        cfg, W, m = small_cross if which == "bf16_cross" else small_joint
+        thw, L = ((2, 12, 16) if which == "bf16_cross" else (1, 16, 20)), 24
+    lat = synth.make_latent(cfg, batch=1, seed=91, latent=thw)
+    cond = dev(synth.make_cond(cfg, batch=1, seed=92, length=L))
+    unc = dev(np.zeros((1, L, cfg["cond_dim"]), np.float32))
+    sig = O.shift_sigma(O.sigma_schedule(4), 3.0).astype(np.float32)
+    x, x0 = dev(lat), dev(lat)
+
+    def run(flags, g):
+        x.copy_(x0)
+        m.dit_profile_start(timing=False)
+        m.dit_denoise_loop(x, 1, thw, cond, unc, L, sig, g, flags=flags)
+        counts = m.dit_profile_stop()
+        m.dit_synchronize()
+        return host(x), counts
+
+    eager, c_eager = run(0, 4.0)
+    graph1, c_graph = run(dit.LOOP_CUDA_GRAPH, 4.0)
+    graph2, _ = run(dit.LOOP_CUDA_GRAPH, 4.0)          # the capture is reused
+    assert np.array_equal(eager, graph1) and np.array_equal(eager, graph2)
+    assert {k: v[0] for k, v in c_eager.items()} == {k: v[0] for k, v in c_graph.items()}
+    eager3, _ = run(0, 2.5)
+    graph3, _ = run(dit.LOOP_CUDA_GRAPH, 2.5)          # new scalar: captured again
+    assert np.array_equal(eager3, graph3) and not np.array_equal(eager3, eager)
