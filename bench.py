@@ -16,9 +16,9 @@ The headline loop is timed with one CUDA event pair around the whole call
 (launches are counted, nothing else is recorded on the stream); the
 per-kernel breakdown and the roofline figure come from a second, separately
 timed pass with an event pair around every launch.  On one GPU the default
-line also carries the 30-block image loop (`image_loop`), the seven points of
-the image block batch/sequence sweep (`sweep`) and the CPU oracle timings
-(`cpu_baseline`).
+line also carries the 30-block image loop (`image_loop`), the video workload
+in fp8 precision (`fp8_loop`), the seven points of the image block
+batch/sequence sweep (`sweep`) and the CPU oracle timings (`cpu_baseline`).
 
 With N > 1 (torchrun), each rank denoises its own request on its own GPU
 (independent replicas, no collective on the data path); the timing is the
@@ -338,6 +338,69 @@ def run_image_loop(args, clocks_gpu: str) -> dict:
     return out
 
 
+def run_fp8_loop(args, clocks_gpu: str) -> dict:
+    """Steps/s of the video workload in fp8 precision (the LayerNorm-fed GEMMs
+    -- Q/K/V, cross-attention Q, MLP up-projection -- in e4m3), timed like the
+    headline; then a separate per-launch pass for the fp8 GEMMs' rate, given
+    against the fp8 peak taken as twice the measured bf16 peak (the nominal
+    dense fp8 : bf16 ratio, 4.5 : 2.25 PFLOP/s)."""
+    import torch
+    from diffusion_transformer_denoising_gb300 import dit
+    cfg = synth.config("video", precision=synth.PREC_FP8)
+    L, C, D, F = cfg["cond_len"], cfg["in_channels"], cfg["hidden"], cfg["mlp"]
+    N = int(np.prod(synth.grid(cfg)))
+    m = dit.DiT(cfg)
+    W = synth.make_weights_torch(cfg, seed=0, device="cuda")
+    m.load_weights(W)
+    del W
+    torch.cuda.empty_cache()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3000)
+    lat0 = torch.randn((1, C) + cfg["latent"], generator=g, device="cuda")
+    cond = torch.randn((1, L, cfg["cond_dim"]), generator=g, device="cuda").to(torch.bfloat16).float()
+    unc = torch.zeros_like(cond)
+    flags = dit.LOOP_PARTIAL_SCHEDULE
+    lat = lat0.clone()
+    m.dit_denoise_loop(lat, 1, cfg["latent"], cond, unc, L, _schedule(cfg, args.warmup), cfg["guidance"], flags)
+    m.dit_synchronize()
+    lat = lat0.clone()
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(clocks_gpu)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    m.dit_denoise_loop(lat, 1, cfg["latent"], cond, unc, L, _schedule(cfg, args.steps), cfg["guidance"], flags)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    m.dit_synchronize()
+    t_step = e0.elapsed_time(e1) / 1e3 / args.steps
+    k_prof = max(1, min(args.steps, 3))
+    lat_p = lat0.clone()
+    m.dit_profile_start(timing=True)
+    m.dit_denoise_loop(lat_p, 1, cfg["latent"], cond, unc, L, _schedule(cfg, k_prof), cfg["guidance"], flags)
+    prof = m.dit_profile_stop()
+    m.dit_synchronize()
+    fl = step_flops(cfg, 2, N, L)
+    peaks = measured_peaks()
+    f8_flops = 2 * 2 * N * D * (3 * D + D + F) * cfg["depth"]          # Q/K/V, cross Q, FFN1 per step
+    f8_ms = sum(prof[k][1] for k in ("gemm_qkv", "gemm_cross_q", "gemm_ffn1")) / k_prof
+    f8_tflops = f8_flops / (f8_ms / 1e3) / 1e12
+    out = {"what": "video workload with the LayerNorm-fed GEMMs in e4m3 (per-row / per-output-channel scales), "
+                   f"first {args.steps} of {cfg['steps']} steps",
+           "steps_per_s": 1.0 / t_step, "ms_per_step": t_step * 1e3, "steps": args.steps,
+           "attn_gemm_tflops": fl["total"] / t_step / 1e12,
+           "fp8_gemm_tflops": f8_tflops, "fp8_peak_tflops": 2 * peaks["bf16_sustained"],
+           "fp8_gemm_frac": f8_tflops / (2 * peaks["bf16_sustained"]),
+           "fp8_peak_kind": f"2 x measured bf16 sustained ({peaks['source']}), nominal fp8:bf16 ratio",
+           "kernel_ms_per_step": {k: v[1] / k_prof for k, v in prof.items()},
+           "finite": bool(torch.isfinite(lat).all().item()), "clocks": clk}
+    m.close()
+    del lat, lat0, lat_p, cond, unc
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     import torch
     from diffusion_transformer_denoising_gb300 import dit
@@ -493,6 +556,7 @@ def run_gpu(args):
         del lat, lat0, cond, unc, d_lat, d_cond, d_unc
         torch.cuda.empty_cache()
         line["image_loop"] = run_image_loop(args, gpu_id)
+        line["fp8_loop"] = run_fp8_loop(args, gpu_id)
         line["sweep"] = sweep_points(args, steps=3, warmup=1)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_leg(args.workload)
@@ -508,7 +572,8 @@ def run_block_case(args):
     import torch
     from diffusion_transformer_denoising_gb300 import dit
     torch.cuda.set_device(0)
-    cfg = synth.config(WORKLOADS[args.workload]["cfg"], depth=1)
+    prec = {"bf16": synth.PREC_BF16, "fp8": synth.PREC_FP8}[args.precision]
+    cfg = synth.config(WORKLOADS[args.workload]["cfg"], depth=1, precision=prec)
     grid = synth.grid(cfg)
     N, L, D = int(np.prod(grid)), cfg["cond_len"], cfg["hidden"]
     m = dit.DiT(cfg)
@@ -534,7 +599,7 @@ def run_block_case(args):
     m.dit_synchronize()
     fl = step_flops(cfg, B, N, L)
     n, ms = prof["attn_self"]
-    out = {"case": f"one {args.workload} block, batch {B}", "per_kernel_ms": {k: v[1] / args.steps for k, v in prof.items()},
+    out = {"case": f"one {args.workload} block, batch {B}, {args.precision}", "per_kernel_ms": {k: v[1] / args.steps for k, v in prof.items()},
            "attn_self_tflops": fl["attn_self_per_launch"] / (ms / max(n, 1) / 1e3) / 1e12,
            "block_tflops": fl["total"] / (sum(v[1] for v in prof.values()) / args.steps / 1e3) / 1e12}
     print(json.dumps(out), flush=True)
@@ -618,6 +683,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the image loop and the sweep points that the default video line also carries")
     ap.add_argument("--batch", type=int, default=2, help="batch of the block case")
+    ap.add_argument("--precision", default="bf16", choices=["bf16", "fp8"], help="precision of the block case")
     ap.add_argument("--case", default="step", choices=["step", "block", "sweep"],
                     help="block: one DiT block repeatedly (small case for kernel profiling); "
                          "sweep: image block batch/sequence sweep")

@@ -109,7 +109,7 @@ static dit_status validate_config(const dit_config* c) {
   if (c->freq_dim % 2) return fail(DIT_ERR_INVALID_ARG, "freq_dim must be even");
   if (c->cond_mode != DIT_COND_CROSS && c->cond_mode != DIT_COND_JOINT)
     return fail(DIT_ERR_INVALID_ARG, "unknown cond_mode %d", c->cond_mode);
-  if (c->precision != DIT_PREC_BF16 && c->precision != DIT_PREC_F32)
+  if (c->precision != DIT_PREC_BF16 && c->precision != DIT_PREC_F32 && c->precision != DIT_PREC_FP8)
     return fail(DIT_ERR_INVALID_ARG, "unknown precision %d", c->precision);
   const int ra = c->rope_axes[0] + c->rope_axes[1] + c->rope_axes[2];
   for (int i = 0; i < 3; ++i)
@@ -123,7 +123,9 @@ static dit_status validate_config(const dit_config* c) {
   if (!(c->ln_eps >= 0.f) || !(c->rope_theta > 0.f) || !(c->timestep_scale > 0.f))
     return fail(DIT_ERR_INVALID_ARG, "ln_eps >= 0, rope_theta > 0 and timestep_scale > 0 required");
   if (c->hidden % 4) return fail(DIT_ERR_SHAPE, "hidden must be a multiple of 4");
-  if (c->precision == DIT_PREC_BF16) {
+  if (c->precision == DIT_PREC_FP8 && c->hidden % 16)
+    return fail(DIT_ERR_SHAPE, "fp8 precision requires hidden to be a multiple of 16");
+  if (c->precision == DIT_PREC_BF16 || c->precision == DIT_PREC_FP8) {
     if (c->head_dim != 128) return fail(DIT_ERR_SHAPE, "bf16 precision requires head_dim 128");
     if (c->mlp % 8 || c->cond_dim % 8)
       return fail(DIT_ERR_SHAPE, "bf16 precision requires mlp and cond_dim multiples of 8");
@@ -148,10 +150,25 @@ static __device__ __align__(256) float g_noalloc_scratch[DIT_NOALLOC_MAX_BATCH +
 struct Param {
   ParamSpec spec;
   bool matrix;  // linear weight: stored in the activation dtype
+  bool fp8;     // stored as e4m3 bytes with one fp32 scale per output row (fp8 precision)
   size_t offset;
+  size_t scale_offset;
   int64_t numel;
   bool loaded;
 };
+
+// In fp8 precision the weights of the GEMMs whose input comes from a
+// LayerNorm (self-attention Q/K/V of both streams, cross-attention Q, MLP
+// up-projection of both streams) are kept in e4m3; the LayerNorm writes their
+// input in e4m3 with one scale per row.
+static bool fp8_weight(const std::string& n) {
+  auto ends = [&](const char* suf) {
+    const size_t l = strlen(suf);
+    return n.size() >= l && n.compare(n.size() - l, l, suf) == 0;
+  };
+  return n.rfind("blocks.", 0) == 0 &&
+         (ends(".attn.qkv.weight") || ends(".cross.q.weight") || ends(".mlp.fc1.weight"));
+}
 
 struct Workspace {
   void* base = nullptr;
@@ -170,6 +187,7 @@ struct dit_model {
   int device = 0;
   int num_sms = 0;
   bool bf16 = true;
+  bool fp8 = false;  // e4m3 GEMMs after the LayerNorms (DIT_PREC_FP8)
   size_t act = 2;  // bytes per activation element
   std::vector<Param> params;
   std::unordered_map<std::string, int> index;
@@ -206,6 +224,11 @@ struct dit_model {
   size_t prof_next = 0;
 
   const void* W(const std::string& n) const { return arena + params[index.at(n)].offset; }
+  // per-output-row scales of an e4m3 weight (nullptr for the others)
+  const float* S(const std::string& n) const {
+    const Param& p = params[index.at(n)];
+    return p.fp8 ? reinterpret_cast<const float*>(arena + p.scale_offset) : nullptr;
+  }
   const float* V(const std::string& n) const {
     return reinterpret_cast<const float*>(arena + params[index.at(n)].offset);
   }
@@ -275,7 +298,8 @@ extern "C" dit_status dit_create(const dit_config* cfg, int device, dit_model** 
   dit_model* m = new dit_model();
   m->cfg = *cfg;
   m->device = device;
-  m->bf16 = cfg->precision == DIT_PREC_BF16;
+  m->bf16 = cfg->precision != DIT_PREC_F32;
+  m->fp8 = cfg->precision == DIT_PREC_FP8;
   m->act = m->bf16 ? 2 : 4;
   // arena layout: block modulation tables first, contiguous per stream
   const int64_t D = cfg->hidden;
@@ -291,6 +315,8 @@ extern "C" dit_status dit_create(const dit_config* cfg, int device, dit_model** 
     Param p;
     p.spec = sp;
     p.matrix = is_matrix(sp.name);
+    p.fp8 = m->fp8 && p.matrix && fp8_weight(sp.name);
+    p.scale_offset = 0;
     p.numel = 1;
     for (auto d : sp.shape) p.numel *= d;
     p.loaded = false;
@@ -302,8 +328,12 @@ extern "C" dit_status dit_create(const dit_config* cfg, int device, dit_model** 
       p.offset = (ctx ? m->ctx_tables_off : m->tables_off) + (size_t)b * 6 * D * sizeof(float);
     } else {
       p.offset = off;
-      const size_t bytes = (size_t)p.numel * (p.matrix ? m->act : sizeof(float));
+      const size_t bytes = (size_t)p.numel * (p.fp8 ? 1 : (p.matrix ? m->act : sizeof(float)));
       off += (bytes + 255) & ~size_t(255);
+      if (p.fp8) {
+        p.scale_offset = off;
+        off += ((size_t)sp.shape[0] * sizeof(float) + 255) & ~size_t(255);
+      }
     }
     m->index[n] = (int)m->params.size();
     m->params.push_back(p);
@@ -394,7 +424,7 @@ extern "C" dit_status dit_load_weights(dit_model* m, const dit_tensor* t, int n)
     const Param& p = m->params[idx[i]];
     const bool want_bf16 = p.matrix && m->bf16;
     const bool have_bf16 = t[i].dtype == DIT_DTYPE_BF16;
-    if (want_bf16 != have_bf16) stage_bytes = std::max(stage_bytes, (size_t)p.numel * (have_bf16 ? 2 : 4));
+    if (want_bf16 != have_bf16 || p.fp8) stage_bytes = std::max(stage_bytes, (size_t)p.numel * (have_bf16 ? 2 : 4));
   }
   void* stage = nullptr;
   DIT_TRY(dev_alloc(&stage, stage_bytes));
@@ -406,7 +436,14 @@ extern "C" dit_status dit_load_weights(dit_model* m, const dit_tensor* t, int n)
     const bool have_bf16 = t[i].dtype == DIT_DTYPE_BF16;
     const size_t src_bytes = (size_t)p.numel * (have_bf16 ? 2 : 4);
     cudaError_t e;
-    if (want_bf16 == have_bf16) {
+    if (p.fp8) {
+      // e4m3 with one scale per output row, quantized on the device
+      e = cudaMemcpy(stage, t[i].data, src_bytes, cudaMemcpyDefault);
+      if (e == cudaSuccess)
+        e = quantize_rows_e4m3(stage, have_bf16, p.spec.shape[0], (int)p.spec.shape[1], reinterpret_cast<uint8_t*>(dst),
+                               reinterpret_cast<float*>(m->arena + p.scale_offset), 0);
+      if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    } else if (want_bf16 == have_bf16) {
       e = cudaMemcpy(dst, t[i].data, src_bytes, cudaMemcpyDefault);
     } else {
       e = cudaMemcpy(stage, t[i].data, src_bytes, cudaMemcpyDefault);
@@ -558,7 +595,9 @@ static dit_status do_gemm(dit_model* m, int kind, const void* A, int64_t M, int 
   g.epi.M = (int)M;
   g.epi.N = N;
   Launch l_(m, kind, 1, s);
-  cudaError_t e = m->bf16 ? gemm_bf16_tc(g, m->d_err, m->num_sms, s) : gemm_f32(g, s);
+  cudaError_t e = ep.a_scale ? gemm_e4m3_tc(g, m->d_err, m->num_sms, s)
+                  : m->bf16  ? gemm_bf16_tc(g, m->d_err, m->num_sms, s)
+                             : gemm_f32(g, s);
   if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "GEMM launch (M=%lld N=%d K=%d) failed: %s", (long long)M, N, K,
                                     cudaGetErrorString(e));
   return DIT_OK;
@@ -588,7 +627,8 @@ static dit_status do_gemm_pair(dit_model* m, int kind, const void* A0, int64_t M
   cudaError_t e = cudaSuccess;
   if (m->bf16) {
     Launch l_(m, kind, 1, s);
-    e = gemm_bf16_tc_pair(g[0], g[1], m->d_err, m->num_sms, s);
+    e = ep0.a_scale ? gemm_e4m3_tc_pair(g[0], g[1], m->d_err, m->num_sms, s)
+                    : gemm_bf16_tc_pair(g[0], g[1], m->d_err, m->num_sms, s);
   } else {
     Launch l_(m, kind, 2, s);
     e = gemm_f32(g[0], s);
@@ -605,7 +645,8 @@ static dit_status do_gemm_pair(dit_model* m, int kind, const void* A0, int64_t M
 static dit_status ln_pair(dit_model* m, const LnArgs& a, const LnArgs& b, cudaStream_t s) {
   Launch l_(m, DIT_KERNEL_LN, 0, s);
   int n = 0;
-  cudaError_t e = ln_modulate_pair(a, b, m->cfg.hidden, m->cfg.ln_eps, m->bf16, m->d_err, m->num_sms, s, &n);
+  const int kind = a.row_scale ? LN_E4M3 : (m->bf16 ? LN_BF16 : LN_F32);
+  cudaError_t e = ln_modulate_pair(a, b, m->cfg.hidden, m->cfg.ln_eps, kind, m->d_err, m->num_sms, s, &n);
   l_.n = n;
   if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "LayerNorm pair launch failed: %s", cudaGetErrorString(e));
   return DIT_OK;
@@ -697,6 +738,8 @@ struct BlockBufs {
   void* vc;
   void* hc;        // [B, L, D] act (joint: condition-stream LN output)
   void* gc;        // [B, L, F] act (joint: condition-stream MLP hidden)
+  float* hs;       // [B, max(N, L)] row scales of h when it holds e4m3 (fp8 precision)
+  float* hcs;      // [B, L] row scales of hc (joint, fp8 precision)
 };
 
 static size_t block_ws_bytes(const dit_model* m, int B, int N, int L) {
@@ -717,6 +760,10 @@ static size_t block_ws_bytes(const dit_model* m, int B, int N, int L) {
   if (c.cond_mode == DIT_COND_JOINT) {
     add((int64_t)B * L * c.hidden, a);     // hc
     add((int64_t)B * L * c.mlp, a);        // gc
+  }
+  if (m->fp8) {
+    add((int64_t)B * NL, 4);               // hs
+    add((int64_t)B * L, 4);                // hcs
   }
   return t;
 }
@@ -742,7 +789,25 @@ static BlockBufs carve_block(const dit_model* m, Workspace& w, int B, int N, int
     b.hc = w.take((size_t)B * L * c.hidden * a);
     b.gc = w.take((size_t)B * L * c.mlp * a);
   }
+  b.hs = b.hcs = nullptr;
+  if (m->fp8) {
+    b.hs = static_cast<float*>(w.take((size_t)B * NL * 4));
+    b.hcs = static_cast<float*>(w.take((size_t)B * L * 4));
+  }
   return b;
+}
+
+// LayerNorm feeding a GEMM: e4m3 + row scales in fp8 precision, else the
+// activation dtype.
+static int ln_out_kind(const dit_model* m) { return m->fp8 ? LN_E4M3 : (m->bf16 ? LN_BF16 : LN_F32); }
+// The same epilogue with the operand scales of an e4m3 GEMM (no change when
+// the weight is not e4m3).
+static EpiParams scaled(EpiParams e, const float* a_scale, const float* w_scale) {
+  if (w_scale) {
+    e.a_scale = a_scale;
+    e.w_scale = w_scale;
+  }
+  return e;
 }
 
 // Cross-attention keys/values of the condition tokens for one block:
@@ -764,28 +829,34 @@ static dit_status run_block(dit_model* m, int blk, float* x, float* xc, const fl
   const dit_config& c = m->cfg;
   const int D = c.hidden, F = c.mlp;
   const float eps = c.ln_eps;
-  const bool bf = m->bf16;
+  const int lk = ln_out_kind(m);  // LayerNorm outputs that feed a GEMM directly
+  float* hs = bb.hs;              // their row scales (fp8 precision), else unused
+  auto Wt = [&](const char* n) { return m->W(m->blk(blk, n)); };
+  auto Sc = [&](const char* n) { return m->S(m->blk(blk, n)); };
   if (c.cond_mode == DIT_COND_CROSS) {
     const int64_t R = (int64_t)B * N;
     // self-attention half
-    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, bf, m->d_err, m->num_sms, s));
-    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_QKV, bb.h, R, D, D, m->W(m->blk(blk, "attn.qkv.weight")), 3 * D,
-                    epi_heads(m, m->V(m->blk(blk, "attn.qkv.bias")), bb.q, bb.k, bb.v, N, N, 0, 0x3), s));
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 0 * D, mod + 1 * D, mod_bstride, eps, bb.h, lk, m->d_err, m->num_sms, s, hs));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_QKV, bb.h, R, D, D, Wt("attn.qkv.weight"), 3 * D,
+                    scaled(epi_heads(m, m->V(m->blk(blk, "attn.qkv.bias")), bb.q, bb.k, bb.v, N, N, 0, 0x3), hs,
+                           Sc("attn.qkv.weight")), s));
     DIT_TRY(do_attn(m, DIT_KERNEL_ATTN_SELF, bb.q, bb.k, bb.v, B, N, N, bb.a, nullptr, N, s));
-    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, m->W(m->blk(blk, "attn.out.weight")), D,
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, Wt("attn.out.weight"), D,
                     epi_resid(m->V(m->blk(blk, "attn.out.bias")), x, mod + 2 * D, mod_bstride, N), s));
     // cross-attention half: plain LN, no rotation, ungated residual
-    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, nullptr, nullptr, 0, eps, bb.h, bf, m->d_err, m->num_sms, s));
-    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_CROSS_Q, bb.h, R, D, D, m->W(m->blk(blk, "cross.q.weight")), D,
-                    epi_heads(m, m->V(m->blk(blk, "cross.q.bias")), bb.q, nullptr, nullptr, N, N, 0, 0), s));
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, nullptr, nullptr, 0, eps, bb.h, lk, m->d_err, m->num_sms, s, hs));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_CROSS_Q, bb.h, R, D, D, Wt("cross.q.weight"), D,
+                    scaled(epi_heads(m, m->V(m->blk(blk, "cross.q.bias")), bb.q, nullptr, nullptr, N, N, 0, 0), hs,
+                           Sc("cross.q.weight")), s));
     DIT_TRY(do_attn(m, DIT_KERNEL_ATTN_CROSS, bb.q, kc, vc, B, N, L, bb.a, nullptr, N, s));
-    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, m->W(m->blk(blk, "cross.out.weight")), D,
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, Wt("cross.out.weight"), D,
                     epi_resid(m->V(m->blk(blk, "cross.out.bias")), x, nullptr, 0, N), s));
     // MLP half
-    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, m->d_err, m->num_sms, s));
-    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN1, bb.h, R, D, D, m->W(m->blk(blk, "mlp.fc1.weight")), F,
-                    epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F), s));
-    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN2, bb.g, R, F, F, m->W(m->blk(blk, "mlp.fc2.weight")), D,
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, lk, m->d_err, m->num_sms, s, hs));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN1, bb.h, R, D, D, Wt("mlp.fc1.weight"), F,
+                    scaled(epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F), hs, Sc("mlp.fc1.weight")),
+                    s));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN2, bb.g, R, F, F, Wt("mlp.fc2.weight"), D,
                     epi_resid(m->V(m->blk(blk, "mlp.fc2.bias")), x, mod + 5 * D, mod_bstride, N), s));
     return DIT_OK;
   }
@@ -794,44 +865,55 @@ static dit_status run_block(dit_model* m, int blk, float* x, float* xc, const fl
   // after), so the condition stream's 1024 rows fill the image GEMM's last wave.
   const int S = L + N;
   const int64_t R = (int64_t)B * N, Rc = (int64_t)B * L;
-  DIT_TRY(ln_pair(m, LnArgs{x, R, N, mod + 0 * D, mod + 1 * D, mod_bstride, bb.h},
-                  LnArgs{xc, Rc, L, modc + 0 * D, modc + 1 * D, mod_bstride, bb.hc}, s));
+  float* hcs = bb.hcs;
+  auto ln_args = [&](const float* xx, int64_t rows, int rpb, const float* sh, const float* sc, void* out,
+                     float* rs) {
+    LnArgs a{xx, rows, rpb, sh, sc, mod_bstride, out};
+    a.row_scale = m->fp8 ? rs : nullptr;
+    return a;
+  };
+  DIT_TRY(ln_pair(m, ln_args(x, R, N, mod + 0 * D, mod + 1 * D, bb.h, hs),
+                  ln_args(xc, Rc, L, modc + 0 * D, modc + 1 * D, bb.hc, hcs), s));
   DIT_TRY(do_gemm_pair(m, DIT_KERNEL_GEMM_QKV,
-                       bb.h, R, m->W(m->blk(blk, "attn.qkv.weight")),
-                       epi_heads(m, m->V(m->blk(blk, "attn.qkv.bias")), bb.q, bb.k, bb.v, N, S, L, 0x3),
-                       bb.hc, Rc, m->W(m->blk(blk, "ctx.attn.qkv.weight")),
-                       epi_heads(m, m->V(m->blk(blk, "ctx.attn.qkv.bias")), bb.q, bb.k, bb.v, L, S, 0, 0),
+                       bb.h, R, Wt("attn.qkv.weight"),
+                       scaled(epi_heads(m, m->V(m->blk(blk, "attn.qkv.bias")), bb.q, bb.k, bb.v, N, S, L, 0x3), hs,
+                              Sc("attn.qkv.weight")),
+                       bb.hc, Rc, Wt("ctx.attn.qkv.weight"),
+                       scaled(epi_heads(m, m->V(m->blk(blk, "ctx.attn.qkv.bias")), bb.q, bb.k, bb.v, L, S, 0, 0), hcs,
+                              Sc("ctx.attn.qkv.weight")),
                        D, 3 * D, s));
   DIT_TRY(do_attn(m, DIT_KERNEL_ATTN_SELF, bb.q, bb.k, bb.v, B, S, S, bb.ac, bb.a, L, s));
   if (!ctx_out_needed) {
     // last block: the condition stream's output is never read
-    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, m->W(m->blk(blk, "attn.out.weight")), D,
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_OUT, bb.a, R, D, D, Wt("attn.out.weight"), D,
                     epi_resid(m->V(m->blk(blk, "attn.out.bias")), x, mod + 2 * D, mod_bstride, N), s));
-    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, bf, m->d_err, m->num_sms, s));
-    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN1, bb.h, R, D, D, m->W(m->blk(blk, "mlp.fc1.weight")), F,
-                    epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F), s));
-    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN2, bb.g, R, F, F, m->W(m->blk(blk, "mlp.fc2.weight")), D,
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, R, D, N, mod + 3 * D, mod + 4 * D, mod_bstride, eps, bb.h, lk, m->d_err, m->num_sms, s, hs));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN1, bb.h, R, D, D, Wt("mlp.fc1.weight"), F,
+                    scaled(epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F), hs, Sc("mlp.fc1.weight")),
+                    s));
+    DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_FFN2, bb.g, R, F, F, Wt("mlp.fc2.weight"), D,
                     epi_resid(m->V(m->blk(blk, "mlp.fc2.bias")), x, mod + 5 * D, mod_bstride, N), s));
     return DIT_OK;
   }
   DIT_TRY(do_gemm_pair(m, DIT_KERNEL_GEMM_OUT,
-                       bb.a, R, m->W(m->blk(blk, "attn.out.weight")),
+                       bb.a, R, Wt("attn.out.weight"),
                        epi_resid(m->V(m->blk(blk, "attn.out.bias")), x, mod + 2 * D, mod_bstride, N),
-                       bb.ac, Rc, m->W(m->blk(blk, "ctx.attn.out.weight")),
+                       bb.ac, Rc, Wt("ctx.attn.out.weight"),
                        epi_resid(m->V(m->blk(blk, "ctx.attn.out.bias")), xc, modc + 2 * D, mod_bstride, L),
                        D, D, s));
-  DIT_TRY(ln_pair(m, LnArgs{x, R, N, mod + 3 * D, mod + 4 * D, mod_bstride, bb.h},
-                  LnArgs{xc, Rc, L, modc + 3 * D, modc + 4 * D, mod_bstride, bb.hc}, s));
+  DIT_TRY(ln_pair(m, ln_args(x, R, N, mod + 3 * D, mod + 4 * D, bb.h, hs),
+                  ln_args(xc, Rc, L, modc + 3 * D, modc + 4 * D, bb.hc, hcs), s));
   DIT_TRY(do_gemm_pair(m, DIT_KERNEL_GEMM_FFN1,
-                       bb.h, R, m->W(m->blk(blk, "mlp.fc1.weight")),
-                       epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F),
-                       bb.hc, Rc, m->W(m->blk(blk, "ctx.mlp.fc1.weight")),
-                       epi_store(EPI_GELU, m->V(m->blk(blk, "ctx.mlp.fc1.bias")), bb.gc, F),
+                       bb.h, R, Wt("mlp.fc1.weight"),
+                       scaled(epi_store(EPI_GELU, m->V(m->blk(blk, "mlp.fc1.bias")), bb.g, F), hs, Sc("mlp.fc1.weight")),
+                       bb.hc, Rc, Wt("ctx.mlp.fc1.weight"),
+                       scaled(epi_store(EPI_GELU, m->V(m->blk(blk, "ctx.mlp.fc1.bias")), bb.gc, F), hcs,
+                              Sc("ctx.mlp.fc1.weight")),
                        D, F, s));
   DIT_TRY(do_gemm_pair(m, DIT_KERNEL_GEMM_FFN2,
-                       bb.g, R, m->W(m->blk(blk, "mlp.fc2.weight")),
+                       bb.g, R, Wt("mlp.fc2.weight"),
                        epi_resid(m->V(m->blk(blk, "mlp.fc2.bias")), x, mod + 5 * D, mod_bstride, N),
-                       bb.gc, Rc, m->W(m->blk(blk, "ctx.mlp.fc2.weight")),
+                       bb.gc, Rc, Wt("ctx.mlp.fc2.weight"),
                        epi_resid(m->V(m->blk(blk, "ctx.mlp.fc2.bias")), xc, modc + 5 * D, mod_bstride, L),
                        F, D, s));
   return DIT_OK;
@@ -986,7 +1068,7 @@ extern "C" dit_status dit_final_layer(dit_model* m, const float* x, const float*
   void* h = w.take((size_t)batch * N * D * m->act);
   float* vt = static_cast<float*>(w.take((size_t)batch * N * P * 4));
   LAUNCH(DIT_KERNEL_SMALL, 1, add_tables(mod, batch, D, 2, m->V("head.mod_table"), 1, headtab, s));
-  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, batch * N, D, (int)N, headtab, headtab + D, 2 * D, c.ln_eps, h, m->bf16, m->d_err, m->num_sms, s));
+  LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, batch * N, D, (int)N, headtab, headtab + D, 2 * D, c.ln_eps, h, m->bf16 ? LN_BF16 : LN_F32, m->d_err, m->num_sms, s));
   DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_EMBED, h, batch * N, D, D, m->W("head.weight"), P, epi_store(EPI_F32, m->V("head.bias"), vt, P), s));
   LAUNCH(DIT_KERNEL_SMALL, 1, unpatchify(vt, batch, c.in_channels, thw[0], thw[1], thw[2], c.patch[0], c.patch[1], c.patch[2], v, s));
   return DIT_OK;
@@ -1128,7 +1210,7 @@ extern "C" dit_status dit_denoise_loop(dit_model* m, float* latents, int batch, 
                         tabs_c ? tabs_c + (size_t)blk * 6 * D : nullptr, 0, kc, vc, B, N, L, blk + 1 < c.depth, bb,
                         s));
     }
-    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, (int64_t)B * N, D, N, headtab, headtab + D, 0, c.ln_eps, bb.h, m->bf16, m->d_err, m->num_sms, s));
+    LAUNCH(DIT_KERNEL_LN, 1, ln_modulate(x, (int64_t)B * N, D, N, headtab, headtab + D, 0, c.ln_eps, bb.h, m->bf16 ? LN_BF16 : LN_F32, m->d_err, m->num_sms, s));
     DIT_TRY(do_gemm(m, DIT_KERNEL_GEMM_EMBED, bb.h, (int64_t)B * N, D, D, m->W("head.weight"), P,
                     epi_store(EPI_F32, m->V("head.bias"), vt, P), s));
     LAUNCH(DIT_KERNEL_CFG_EULER, 1, cfg_euler_tokens(vt, Bq, cfg, guidance, sig_dev, step_dev, c.in_channels, thw[0], thw[1],

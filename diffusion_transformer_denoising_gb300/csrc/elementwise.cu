@@ -15,6 +15,34 @@ DIT_DEV float warp_sum(float v) {
   return v;
 }
 
+DIT_DEV float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Quantize a warp's row held as y[NCH] float4 (lane owns float4 c = lane + 32 i
+// while c < n4) to e4m3 bytes at dst (row of n4 * 4 bytes) with its scale
+// max|row| / 448 written by lane 0 to *row_scale.
+template <int NCH>
+DIT_DEV void store_row_e4m3(const float4 (&y)[NCH], int n4, uint8_t* dst, float* row_scale) {
+  const int lane = threadIdx.x & 31;
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < NCH; ++i)
+    if (lane + 32 * i < n4)
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(y[i].x), fabsf(y[i].y)), fmaxf(fabsf(y[i].z), fabsf(y[i].w))));
+  amax = warp_max(amax);
+  const float sc = amax > 0.f ? amax / kE4M3Max : 1.f;
+  const float inv = amax > 0.f ? kE4M3Max / amax : 1.f;
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    const int c = lane + 32 * i;
+    if (c < n4) reinterpret_cast<uint32_t*>(dst)[c] = pack_e4m3x4(y[i].x * inv, y[i].y * inv, y[i].z * inv, y[i].w * inv);
+  }
+  if (lane == 0) *row_scale = sc;
+}
+
 static inline unsigned blocks_for(int64_t n, int per_block, int cap = 152 * 32) {
   int64_t b = (n + per_block - 1) / per_block;
   if (b < 1) b = 1;
@@ -24,11 +52,11 @@ static inline unsigned blocks_for(int64_t n, int per_block, int cap = 152 * 32) 
 // ---------------------------------------------------------------- LayerNorm + adaLN
 // One warp per row; the row stays in registers (NCH float4 per lane) so x is
 // read once.  Statistics in fp32: mean, then the centred second moment.
-template <int NCH, bool kBf16>
+template <int NCH, int OUT>
 __global__ void __launch_bounds__(256) ln_mod_kernel(const float* __restrict__ x, int64_t rows, int D, int rpb,
                                                      const float* __restrict__ shift,
                                                      const float* __restrict__ scale, int64_t mbs, float eps,
-                                                     void* __restrict__ out) {
+                                                     void* __restrict__ out, float* __restrict__ row_scale) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -73,15 +101,18 @@ __global__ void __launch_bounds__(256) ln_mod_kernel(const float* __restrict__ x
       y.z = fmaf(y.z, 1.f + a.z, b.z);
       y.w = fmaf(y.w, 1.f + a.w, b.w);
     }
-    if constexpr (kBf16) {
+    if constexpr (OUT == LN_BF16) {
       uint2 u;
       u.x = pack_bf16x2(y.x, y.y);
       u.y = pack_bf16x2(y.z, y.w);
       reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + row * D)[c] = u;
-    } else {
+    } else if constexpr (OUT == LN_F32) {
       reinterpret_cast<float4*>(static_cast<float*>(out) + row * D)[c] = y;
+    } else {
+      v[i] = y;  // quantized below, once the row's max is known
     }
   }
+  if constexpr (OUT == LN_E4M3) store_row_e4m3<NCH>(v, n4, static_cast<uint8_t*>(out) + row * D, row_scale + row);
 }
 
 // bf16-output variant with the rows staged in shared memory by bulk copies.
@@ -105,7 +136,8 @@ constexpr int LN_RING_SMEM = 200 * 1024; // ring + modulation
 
 struct LnSeg {
   const float* x = nullptr;        // [rows, D]
-  __nv_bfloat16* out = nullptr;    // [rows, D]
+  void* out = nullptr;             // [rows, D] bf16, or e4m3 bytes with row_scale[rows]
+  float* row_scale = nullptr;
   const float* shift = nullptr;    // [batch] rows of stride mbs; NULL in both segments = plain LN
   const float* scale = nullptr;
   int64_t mbs = 0;
@@ -117,7 +149,7 @@ struct LnSegs {
   int nmod = 0;                    // modulation entries (batch elements of both segments)
 };
 
-template <int NCH>
+template <int NCH, bool F8>
 __global__ void __launch_bounds__(LN_STAGED_THREADS, 1)
     ln_mod_staged_kernel(const __grid_constant__ LnSegs P, int D, float eps, int stages, int* err) {
   extern __shared__ __align__(16) uint8_t ln_smem[];
@@ -227,7 +259,7 @@ __global__ void __launch_bounds__(LN_STAGED_THREADS, 1)
     if (!DIT_BOUNDS(lr >= 0 && lr < g.rows && (!modulate || (e >= 0 && e < P.nmod)), err, 65)) break;
     const float4* sh4 = smod + (size_t)(2 * e) * n4;
     const float4* sc4 = sh4 + n4;
-    uint2* dst = reinterpret_cast<uint2*>(g.out + (int64_t)lr * D);
+    uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(g.out) + (int64_t)lr * D);
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
       const int c = lane + 32 * i;
@@ -241,11 +273,16 @@ __global__ void __launch_bounds__(LN_STAGED_THREADS, 1)
         y.z = fmaf(y.z, a.z, b.z);
         y.w = fmaf(y.w, a.w, b.w);
       }
-      uint2 u;
-      u.x = pack_bf16x2(y.x, y.y);
-      u.y = pack_bf16x2(y.z, y.w);
-      dst[c] = u;
+      if constexpr (F8) {
+        v[i] = y;  // quantized below, once the row's max is known
+      } else {
+        uint2 u;
+        u.x = pack_bf16x2(y.x, y.y);
+        u.y = pack_bf16x2(y.z, y.w);
+        dst[c] = u;
+      }
     }
+    if constexpr (F8) store_row_e4m3<NCH>(v, n4, static_cast<uint8_t*>(g.out) + (int64_t)lr * D, g.row_scale + lr);
   }
 }
 
@@ -255,7 +292,7 @@ __global__ void __launch_bounds__(LN_STAGED_THREADS, 1)
 // more than one SM needs in flight to cover DRAM latency at its share of the
 // bandwidth), a multiple of LN_CONSUMERS; one CTA per SM (fewer when there
 // are fewer rows).
-template <int NCH>
+template <int NCH, bool F8>
 static bool ln_staged_launch(LnSegs P, int D, float eps, int* err, int num_sms, cudaStream_t s, cudaError_t* status) {
   const int row_bytes = D * 4;
   int nmod = 0;
@@ -278,14 +315,14 @@ static bool ln_staged_launch(LnSegs P, int D, float eps, int* err, int num_sms, 
   if (stages < LN_CONSUMERS) return false;
   const size_t smem = (size_t)stages * row_bytes + mod_bytes + 2 * sizeof(uint64_t) * stages + 16;
   static SmemAttr attr;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ln_mod_staged_kernel<NCH>), (int)smem, attr);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(ln_mod_staged_kernel<NCH, F8>), (int)smem, attr);
   if (e != cudaSuccess) {
     *status = e;
     return true;
   }
   const int rows = P.s[0].rows + P.s[1].rows;
   const int grid = rows < num_sms ? rows : num_sms;
-  ln_mod_staged_kernel<NCH><<<grid, LN_STAGED_THREADS, smem, s>>>(P, D, eps, stages, err);
+  ln_mod_staged_kernel<NCH, F8><<<grid, LN_STAGED_THREADS, smem, s>>>(P, D, eps, stages, err);
   *status = cudaGetLastError();
   return true;
 }
@@ -296,14 +333,16 @@ static bool staged_ok(const LnArgs& a) {
 }
 
 static bool ln_staged(const LnArgs* a, int nseg, int D, float eps, int* err, int num_sms, cudaStream_t s,
-                      cudaError_t* status) {
+                      cudaError_t* status, bool f8) {
   LnSegs P;
   int64_t rows = 0;
   for (int i = 0; i < nseg; ++i) {
     if (!staged_ok(a[i]) || a[i].rpb <= 0) return false;
     if (i > 0 && (a[i].shift == nullptr) != (a[0].shift == nullptr)) return false;
+    if (f8 && !a[i].row_scale) return false;
     P.s[i].x = a[i].x;
-    P.s[i].out = static_cast<__nv_bfloat16*>(a[i].out);
+    P.s[i].out = a[i].out;
+    P.s[i].row_scale = a[i].row_scale;
     P.s[i].shift = a[i].shift;
     P.s[i].scale = a[i].scale;
     P.s[i].mbs = a[i].mbs;
@@ -313,57 +352,108 @@ static bool ln_staged(const LnArgs* a, int nseg, int D, float eps, int* err, int
   }
   if (rows >= (int64_t)1 << 31) return false;
   const int nch = (D / 4 + 31) / 32;
-  if (nch <= 4) return ln_staged_launch<4>(P, D, eps, err, num_sms, s, status);
-  if (nch <= 12) return ln_staged_launch<12>(P, D, eps, err, num_sms, s, status);
-  if (nch <= 24) return ln_staged_launch<24>(P, D, eps, err, num_sms, s, status);
+  if (f8) {
+    if (nch <= 4) return ln_staged_launch<4, true>(P, D, eps, err, num_sms, s, status);
+    if (nch <= 12) return ln_staged_launch<12, true>(P, D, eps, err, num_sms, s, status);
+    if (nch <= 24) return ln_staged_launch<24, true>(P, D, eps, err, num_sms, s, status);
+    return false;
+  }
+  if (nch <= 4) return ln_staged_launch<4, false>(P, D, eps, err, num_sms, s, status);
+  if (nch <= 12) return ln_staged_launch<12, false>(P, D, eps, err, num_sms, s, status);
+  if (nch <= 24) return ln_staged_launch<24, false>(P, D, eps, err, num_sms, s, status);
   return false;
 }
 
 template <int NCH>
 static cudaError_t ln_launch(const float* x, int64_t rows, int D, int rpb, const float* sh, const float* sc,
-                             int64_t mbs, float eps, void* out, bool bf16, cudaStream_t s) {
+                             int64_t mbs, float eps, void* out, int out_kind, float* row_scale, cudaStream_t s) {
   const unsigned grid = (unsigned)((rows + 7) / 8);
-  if (bf16)
-    ln_mod_kernel<NCH, true><<<grid, 256, 0, s>>>(x, rows, D, rpb, sh, sc, mbs, eps, out);
+  if (out_kind == LN_BF16)
+    ln_mod_kernel<NCH, LN_BF16><<<grid, 256, 0, s>>>(x, rows, D, rpb, sh, sc, mbs, eps, out, row_scale);
+  else if (out_kind == LN_E4M3)
+    ln_mod_kernel<NCH, LN_E4M3><<<grid, 256, 0, s>>>(x, rows, D, rpb, sh, sc, mbs, eps, out, row_scale);
   else
-    ln_mod_kernel<NCH, false><<<grid, 256, 0, s>>>(x, rows, D, rpb, sh, sc, mbs, eps, out);
+    ln_mod_kernel<NCH, LN_F32><<<grid, 256, 0, s>>>(x, rows, D, rpb, sh, sc, mbs, eps, out, row_scale);
   return cudaGetLastError();
 }
 
 cudaError_t ln_modulate(const float* x, int64_t rows, int D, int rpb, const float* shift, const float* scale,
-                        int64_t mbs, float eps, void* out, bool out_bf16, int* err, int num_sms, cudaStream_t s) {
+                        int64_t mbs, float eps, void* out, int out_kind, int* err, int num_sms, cudaStream_t s,
+                        float* row_scale) {
   if (rows == 0) return cudaSuccess;
   if (D % 4) return cudaErrorInvalidValue;
-  if (out_bf16) {
-    const LnArgs a{x, rows, rpb, shift, scale, mbs, out};
+  if (out_kind == LN_E4M3 && (!row_scale || (reinterpret_cast<uintptr_t>(out) & 3))) return cudaErrorInvalidValue;
+  if (out_kind != LN_F32) {
+    LnArgs a{x, rows, rpb, shift, scale, mbs, out};
+    a.row_scale = row_scale;
     cudaError_t st = cudaSuccess;
-    if (ln_staged(&a, 1, D, eps, err, num_sms, s, &st)) return st;
+    if (ln_staged(&a, 1, D, eps, err, num_sms, s, &st, out_kind == LN_E4M3)) return st;
   }
   const int nch = (D / 4 + 31) / 32;
-  if (nch <= 1) return ln_launch<1>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
-  if (nch <= 2) return ln_launch<2>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
-  if (nch <= 4) return ln_launch<4>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
-  if (nch <= 8) return ln_launch<8>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
-  if (nch <= 12) return ln_launch<12>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
-  if (nch <= 16) return ln_launch<16>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
-  if (nch <= 24) return ln_launch<24>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
-  if (nch <= 32) return ln_launch<32>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_bf16, s);
+#define DIT_LN_CASE(n) \
+  if (nch <= n) return ln_launch<n>(x, rows, D, rpb, shift, scale, mbs, eps, out, out_kind, row_scale, s);
+  DIT_LN_CASE(1)
+  DIT_LN_CASE(2)
+  DIT_LN_CASE(4)
+  DIT_LN_CASE(8)
+  DIT_LN_CASE(12)
+  DIT_LN_CASE(16)
+  DIT_LN_CASE(24)
+  DIT_LN_CASE(32)
+#undef DIT_LN_CASE
   return cudaErrorInvalidValue;
 }
 
-cudaError_t ln_modulate_pair(const LnArgs& a, const LnArgs& b, int D, float eps, bool out_bf16, int* err,
+cudaError_t ln_modulate_pair(const LnArgs& a, const LnArgs& b, int D, float eps, int out_kind, int* err,
                              int num_sms, cudaStream_t s, int* launches) {
   if (D % 4) return cudaErrorInvalidValue;
   *launches = 1;
-  if (out_bf16 && a.rows > 0 && b.rows > 0) {
+  if (out_kind != LN_F32 && a.rows > 0 && b.rows > 0) {
     const LnArgs ab[2] = {a, b};
     cudaError_t st = cudaSuccess;
-    if (ln_staged(ab, 2, D, eps, err, num_sms, s, &st)) return st;
+    if (ln_staged(ab, 2, D, eps, err, num_sms, s, &st, out_kind == LN_E4M3)) return st;
   }
   *launches = (a.rows > 0) + (b.rows > 0);
-  cudaError_t e = ln_modulate(a.x, a.rows, D, a.rpb, a.shift, a.scale, a.mbs, eps, a.out, out_bf16, err, num_sms, s);
+  cudaError_t e = ln_modulate(a.x, a.rows, D, a.rpb, a.shift, a.scale, a.mbs, eps, a.out, out_kind, err, num_sms, s,
+                              a.row_scale);
   if (e != cudaSuccess) return e;
-  return ln_modulate(b.x, b.rows, D, b.rpb, b.shift, b.scale, b.mbs, eps, b.out, out_bf16, err, num_sms, s);
+  return ln_modulate(b.x, b.rows, D, b.rpb, b.shift, b.scale, b.mbs, eps, b.out, out_kind, err, num_sms, s,
+                     b.row_scale);
+}
+
+// ---------------------------------------------------------------- weight quantization
+// One warp per row: max |w| over the row, then w * 448 / max to e4m3.
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const T* __restrict__ src, int64_t rows, int K,
+                                                            uint8_t* __restrict__ dst, float* __restrict__ scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const T* r = src + row * K;
+  auto ld = [&](int k) -> float {
+    if constexpr (sizeof(T) == 2) return __bfloat162float(r[k]);
+    else return r[k];
+  };
+  float amax = 0.f;
+  for (int k = lane; k < K; k += 32) amax = fmaxf(amax, fabsf(ld(k)));
+  amax = warp_max(amax);
+  const float inv = amax > 0.f ? kE4M3Max / amax : 1.f;
+  for (int k = 4 * lane; k < K; k += 128)  // K is a multiple of 16
+    *reinterpret_cast<uint32_t*>(dst + row * K + k) =
+        pack_e4m3x4(ld(k) * inv, ld(k + 1) * inv, ld(k + 2) * inv, ld(k + 3) * inv);
+  if (lane == 0) scale[row] = amax > 0.f ? amax / kE4M3Max : 1.f;
+}
+
+cudaError_t quantize_rows_e4m3(const void* src, bool src_bf16, int64_t rows, int K, uint8_t* dst, float* scale,
+                               cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  if (K % 16) return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)((rows + 7) / 8);
+  if (src_bf16)
+    quantize_rows_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows, K, dst, scale);
+  else
+    quantize_rows_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(src), rows, K, dst, scale);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- timestep MLP

@@ -67,14 +67,36 @@ template <typename ActT, int NV>
 DIT_DEV void epilogue_values(const EpiParams& p, int64_t row, int col0, float (&v)[NV]) {
   constexpr bool kFast = std::is_same<ActT, __nv_bfloat16>::value;
   const bool full = col0 + NV <= p.N;
-  if (p.bias) {
-    if (full) {
+  // 8-bit operands: the row scale of A and the column scale of W are undone
+  // together with the bias add (v = v * sa * w_scale + bias); whole chunks
+  // read bias and scales as float4 (both are 256-byte aligned arrays and col0
+  // is a multiple of NV)
+  const float sa = p.a_scale ? __ldg(p.a_scale + row) : 1.f;
+  const bool vec = full && NV % 4 == 0 &&
+                   ((reinterpret_cast<uintptr_t>(p.bias) | reinterpret_cast<uintptr_t>(p.w_scale)) & 15) == 0;
+  if (vec) {
 #pragma unroll
-      for (int j = 0; j < NV; ++j) v[j] += __ldg(p.bias + col0 + j);
-    } else {
+    for (int j = 0; j < NV; j += 4) {
+      const float4 b = p.bias ? __ldg(reinterpret_cast<const float4*>(p.bias + col0 + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (p.a_scale) {
+        const float4 w = __ldg(reinterpret_cast<const float4*>(p.w_scale + col0 + j));
+        v[j + 0] = fmaf(v[j + 0], sa * w.x, b.x);
+        v[j + 1] = fmaf(v[j + 1], sa * w.y, b.y);
+        v[j + 2] = fmaf(v[j + 2], sa * w.z, b.z);
+        v[j + 3] = fmaf(v[j + 3], sa * w.w, b.w);
+      } else {
+        v[j + 0] += b.x;
+        v[j + 1] += b.y;
+        v[j + 2] += b.z;
+        v[j + 3] += b.w;
+      }
+    }
+  } else {
 #pragma unroll
-      for (int j = 0; j < NV; ++j)
-        if (col0 + j < p.N) v[j] += __ldg(p.bias + col0 + j);
+    for (int j = 0; j < NV; ++j) {
+      if (!full && col0 + j >= p.N) continue;
+      if (p.a_scale) v[j] *= sa * __ldg(p.w_scale + col0 + j);
+      if (p.bias) v[j] += __ldg(p.bias + col0 + j);
     }
   }
   if (p.kind == EPI_GELU) {

@@ -36,11 +36,15 @@ namespace dit {
 constexpr int EPI_WARPS = 8;
 constexpr int GEMM_THREADS = 32 * (2 + EPI_WARPS);
 
-template <int BN>
+// F8: e4m3 operands (kind::f8f6f4); a K block is then 128 elements, the same
+// 128 bytes per tile row as 64 bf16 elements, so the tiles, swizzle and
+// descriptors are the same and only the MMA kind and K per MMA change.
+template <int BN, bool F8 = false>
 struct TcGemmCfg {
-  static constexpr int BM = 128, BK = 64;
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int BM = 128, BK = F8 ? 128 : 64;
+  static constexpr int ESZ = F8 ? 1 : 2;
+  static constexpr int A_BYTES = BM * BK * ESZ;
+  static constexpr int B_BYTES = BN * BK * ESZ;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
@@ -49,7 +53,8 @@ struct TcGemmCfg {
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = STG_OFF + EPI_WARPS * STG_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + BAR_BYTES + 1024;
-  static constexpr uint32_t IDESC = umma_idesc_bf16(BM, BN, false);
+  static constexpr uint32_t IDESC = F8 ? umma_idesc_e4m3(BM, BN) : umma_idesc_bf16(BM, BN, false);
+  static constexpr int K_PER_MMA = F8 ? 32 : 16;  // 32 bytes of each row per MMA either way
 };
 
 // Output tensor maps of the TMA epilogue: m[0] = output (x for EPI_RESID,
@@ -189,10 +194,10 @@ DIT_DEV void drain_tile_tma(const EpiParams& ep, const EpiMaps& maps, uint32_t t
   }
 }
 
-template <int BN, int NP>
+template <int BN, int NP, bool F8>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ GemmBatch<NP> P, int N, int K, int* err) {
-  using C = TcGemmCfg<BN>;
+  using C = TcGemmCfg<BN, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -308,8 +313,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const uint64_t ad = umma_desc_add(a_desc, stage * C::STAGE_BYTES);
           const uint64_t bd = umma_desc_add(b_desc, stage * C::STAGE_BYTES);
 #pragma unroll
-          for (int k = 0; k < C::BK / 16; ++k)
-            umma_ss(d_tmem, umma_desc_add(ad, k * 32), umma_desc_add(bd, k * 32), C::IDESC, (kb | k) != 0);
+          for (int k = 0; k < C::BK / C::K_PER_MMA; ++k) {
+            if constexpr (F8)
+              umma_ss_f8(d_tmem, umma_desc_add(ad, k * 32), umma_desc_add(bd, k * 32), C::IDESC, (kb | k) != 0);
+            else
+              umma_ss(d_tmem, umma_desc_add(ad, k * 32), umma_desc_add(bd, k * 32), C::IDESC, (kb | k) != 0);
+          }
           umma_commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -427,9 +436,9 @@ static bool make_epi_maps(const EpiParams& e, int64_t M, int N, EpiMaps* maps) {
   return false;
 }
 
-template <int BN, int NP>
+template <int BN, int NP, bool F8>
 static cudaError_t launch_gemm_tc(const GemmArgs* gs, int* err, int num_sms, cudaStream_t s) {
-  using C = TcGemmCfg<BN>;
+  using C = TcGemmCfg<BN, F8>;
   GemmBatch<NP> P{};
   const int n_tiles = (gs[0].N + BN - 1) / BN;
   int tiles = 0;
@@ -438,11 +447,12 @@ static cudaError_t launch_gemm_tc(const GemmArgs* gs, int* err, int num_sms, cud
     P.ep[p] = g.epi;
     P.M[p] = g.M;
     if (g.M > 0) {
-      const uint64_t da[2] = {(uint64_t)g.K, (uint64_t)g.M}, sa[1] = {(uint64_t)g.lda * 2};
-      const uint32_t ba[2] = {64, 128};
-      const uint64_t db[2] = {(uint64_t)g.K, (uint64_t)g.N}, sb[1] = {(uint64_t)g.K * 2};
-      const uint32_t bb[2] = {64, (uint32_t)BN};
-      if (!make_tmap_bf16(&P.tmA[p], g.A, 2, da, sa, ba) || !make_tmap_bf16(&P.tmB[p], g.W, 2, db, sb, bb))
+      const uint64_t da[2] = {(uint64_t)g.K, (uint64_t)g.M}, sa[1] = {(uint64_t)g.lda * C::ESZ};
+      const uint32_t ba[2] = {(uint32_t)C::BK, 128};
+      const uint64_t db[2] = {(uint64_t)g.K, (uint64_t)g.N}, sb[1] = {(uint64_t)g.K * C::ESZ};
+      const uint32_t bb[2] = {(uint32_t)C::BK, (uint32_t)BN};
+      const CUtensorMapDataType dt = F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      if (!make_tmap(&P.tmA[p], dt, g.A, 2, da, sa, ba) || !make_tmap(&P.tmB[p], dt, g.W, 2, db, sb, bb))
         return cudaErrorInvalidValue;
       P.ep[p].tma = make_epi_maps(P.ep[p], g.M, g.N, &P.maps[p]) ? 1 : 0;
     }
@@ -455,47 +465,68 @@ static cudaError_t launch_gemm_tc(const GemmArgs* gs, int* err, int num_sms, cud
   // once more, so groups are used only while A is no larger than W: the
   // image FFN2 (A 226 MB, W 75 MB) read slightly more in two groups (887 MB)
   // than in one (853 MB).
-  const int64_t w_tile_bytes = (int64_t)BN * gs[0].K * 2;
-  const int64_t a_bytes = gs[0].M * gs[0].K * 2, w_bytes = (int64_t)gs[0].N * gs[0].K * 2;
+  const int64_t w_tile_bytes = (int64_t)BN * gs[0].K * C::ESZ;
+  const int64_t a_bytes = gs[0].M * gs[0].K * C::ESZ, w_bytes = (int64_t)gs[0].N * gs[0].K * C::ESZ;
   int64_t gn = ((int64_t)40 << 20) / w_tile_bytes;
   if (gn < 1) gn = 1;
   if (a_bytes > w_bytes) gn = n_tiles;
   P.group_n = (int)(gn < n_tiles ? gn : n_tiles);
   if (tiles == 0) return cudaSuccess;
   static SmemAttr attr;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(gemm_tc_kernel<BN, NP>), C::SMEM_BYTES, attr);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(gemm_tc_kernel<BN, NP, F8>), C::SMEM_BYTES, attr);
   if (e != cudaSuccess) return e;
   const int grid = tiles < num_sms ? tiles : num_sms;
-  gemm_tc_kernel<BN, NP><<<grid, GEMM_THREADS, C::SMEM_BYTES, s>>>(P, gs[0].N, gs[0].K, err);
+  gemm_tc_kernel<BN, NP, F8><<<grid, GEMM_THREADS, C::SMEM_BYTES, s>>>(P, gs[0].N, gs[0].K, err);
   return cudaGetLastError();
 }
 
 // alignment rules of the operand tensor maps: 16-byte rows and bases
-static bool operands_ok(const GemmArgs& g) {
-  return !((g.K % 8) || (g.lda % 8) || (reinterpret_cast<uintptr_t>(g.A) & 15) ||
+static bool operands_ok(const GemmArgs& g, int esz) {
+  const int per16 = 16 / esz;
+  return !((g.K % per16) || (g.lda % per16) || (reinterpret_cast<uintptr_t>(g.A) & 15) ||
            (reinterpret_cast<uintptr_t>(g.W) & 15));
 }
 
-template <int NP>
+template <int NP, bool F8>
 static cudaError_t launch_by_width(const GemmArgs* gs, int* err, int num_sms, cudaStream_t s) {
   const int N = gs[0].N;
-  if (N % 256 == 0) return launch_gemm_tc<256, NP>(gs, err, num_sms, s);
-  if (N % 128 == 0) return launch_gemm_tc<128, NP>(gs, err, num_sms, s);
-  return launch_gemm_tc<64, NP>(gs, err, num_sms, s);
+  if (N % 256 == 0) return launch_gemm_tc<256, NP, F8>(gs, err, num_sms, s);
+  if (N % 128 == 0) return launch_gemm_tc<128, NP, F8>(gs, err, num_sms, s);
+  return launch_gemm_tc<64, NP, F8>(gs, err, num_sms, s);
+}
+
+template <bool F8>
+static cudaError_t gemm_single(const GemmArgs& g, int* err, int num_sms, cudaStream_t s) {
+  if (g.M == 0 || g.N == 0) return cudaSuccess;
+  if (!operands_ok(g, F8 ? 1 : 2)) return cudaErrorInvalidValue;
+  if (F8 && (!g.epi.a_scale || !g.epi.w_scale)) return cudaErrorInvalidValue;
+  return launch_by_width<1, F8>(&g, err, num_sms, s);
+}
+
+template <bool F8>
+static cudaError_t gemm_pair(const GemmArgs& g0, const GemmArgs& g1, int* err, int num_sms, cudaStream_t s) {
+  if (g0.N != g1.N || g0.K != g1.K) return cudaErrorInvalidValue;
+  if (g0.N == 0 || (g0.M == 0 && g1.M == 0)) return cudaSuccess;
+  for (const GemmArgs* g : {&g0, &g1}) {
+    if (g->M == 0) continue;
+    if (!operands_ok(*g, F8 ? 1 : 2)) return cudaErrorInvalidValue;
+    if (F8 && (!g->epi.a_scale || !g->epi.w_scale)) return cudaErrorInvalidValue;
+  }
+  const GemmArgs gs[2] = {g0, g1};
+  return launch_by_width<2, F8>(gs, err, num_sms, s);
 }
 
 cudaError_t gemm_bf16_tc(const GemmArgs& g, int* err, int num_sms, cudaStream_t s) {
-  if (g.M == 0 || g.N == 0) return cudaSuccess;
-  if (!operands_ok(g)) return cudaErrorInvalidValue;
-  return launch_by_width<1>(&g, err, num_sms, s);
+  return gemm_single<false>(g, err, num_sms, s);
 }
-
 cudaError_t gemm_bf16_tc_pair(const GemmArgs& g0, const GemmArgs& g1, int* err, int num_sms, cudaStream_t s) {
-  if (g0.N != g1.N || g0.K != g1.K) return cudaErrorInvalidValue;
-  if (g0.N == 0 || (g0.M == 0 && g1.M == 0)) return cudaSuccess;
-  if ((g0.M > 0 && !operands_ok(g0)) || (g1.M > 0 && !operands_ok(g1))) return cudaErrorInvalidValue;
-  const GemmArgs gs[2] = {g0, g1};
-  return launch_by_width<2>(gs, err, num_sms, s);
+  return gemm_pair<false>(g0, g1, err, num_sms, s);
+}
+cudaError_t gemm_e4m3_tc(const GemmArgs& g, int* err, int num_sms, cudaStream_t s) {
+  return gemm_single<true>(g, err, num_sms, s);
+}
+cudaError_t gemm_e4m3_tc_pair(const GemmArgs& g0, const GemmArgs& g1, int* err, int num_sms, cudaStream_t s) {
+  return gemm_pair<true>(g0, g1, err, num_sms, s);
 }
 
 }  // namespace dit

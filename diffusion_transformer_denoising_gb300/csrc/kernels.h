@@ -46,6 +46,11 @@ struct EpiParams {
   // set by the tensor-core GEMM launcher when its output tensor maps are valid
   // (the epilogue then stores through shared memory with TMA)
   int tma = 0;
+  // 8-bit GEMM: the accumulator of row r, column n is multiplied by
+  // a_scale[r] * w_scale[n] (the scales the two operands were quantized with)
+  // before the bias and the rest of the epilogue
+  const float* a_scale = nullptr;
+  const float* w_scale = nullptr;
 };
 
 struct GemmArgs {
@@ -66,6 +71,16 @@ cudaError_t gemm_bf16_tc(const GemmArgs& g, int* err, int num_sms, cudaStream_t 
 // Two bf16 GEMMs with the same N and K in one persistent launch (g0's tiles
 // first, then g1's); either may have M = 0.
 cudaError_t gemm_bf16_tc_pair(const GemmArgs& g0, const GemmArgs& g1, int* err, int num_sms, cudaStream_t s);
+// e4m3 tcgen05 GEMM (kind::f8f6f4): A [M, K] and W [N, K] bytes (row strides
+// lda and K bytes, multiples of 16), fp32 accumulation; the epilogue applies
+// epi.a_scale / epi.w_scale.  Single and paired forms as above.
+cudaError_t gemm_e4m3_tc(const GemmArgs& g, int* err, int num_sms, cudaStream_t s);
+cudaError_t gemm_e4m3_tc_pair(const GemmArgs& g0, const GemmArgs& g1, int* err, int num_sms, cudaStream_t s);
+// Row-wise e4m3 quantization of a weight matrix: src [rows, K] (fp32 or bf16)
+// -> dst [rows, K] e4m3 bytes and scale[rows] = max|row| / 448 (1 for a zero
+// row), dst = src / scale rounded to nearest.
+cudaError_t quantize_rows_e4m3(const void* src, bool src_bf16, int64_t rows, int K, uint8_t* dst, float* scale,
+                               cudaStream_t s);
 
 // ------------------------------------------------------------------ attention
 // Q [B, H, Lq, hd], K/V [B, H, Lk, hd] head-major; output token-major rows of
@@ -87,9 +102,12 @@ cudaError_t attention_bf16_tc(const AttnArgs& a, int* err, cudaStream_t s);
 // shift/scale NULL = plain LN.  Output bf16 (out_bf16) or fp32.  The bf16
 // path stages rows through shared memory on a grid of at most num_sms CTAs;
 // err = device error word for its bounded waits.
+// Output kinds: LN_F32, LN_BF16, or LN_E4M3 (e4m3 bytes, each row divided by
+// its scale max|row| / 448, written to row_scale[row]).
+enum LnOut : int { LN_F32 = 0, LN_BF16 = 1, LN_E4M3 = 2 };
 cudaError_t ln_modulate(const float* x, int64_t rows, int D, int rows_per_batch, const float* shift,
-                        const float* scale, int64_t mod_bstride, float eps, void* out, bool out_bf16, int* err,
-                        int num_sms, cudaStream_t s);
+                        const float* scale, int64_t mod_bstride, float eps, void* out, int out_kind, int* err,
+                        int num_sms, cudaStream_t s, float* row_scale = nullptr);
 // One LayerNorm of a pair: x [rows, D] -> out, modulation of batch element
 // r / rpb at shift/scale + (r / rpb) * mbs (both NULL = plain LN).
 struct LnArgs {
@@ -100,11 +118,12 @@ struct LnArgs {
   const float* scale;
   int64_t mbs;
   void* out;
+  float* row_scale = nullptr;  // LN_E4M3 output: per-row scale
 };
 // Two LayerNorms of the same width in one launch where the staged bf16 path
 // takes them (both modulated or both plain), else one launch each;
 // *launches = the number of kernels launched.
-cudaError_t ln_modulate_pair(const LnArgs& a, const LnArgs& b, int D, float eps, bool out_bf16, int* err,
+cudaError_t ln_modulate_pair(const LnArgs& a, const LnArgs& b, int D, float eps, int out_kind, int* err,
                              int num_sms, cudaStream_t s, int* launches);
 // Sinusoidal timestep embedding + 2-layer MLP: mod[b, 6D] for each t[b].
 // hidden_scratch: float[batch * D].

@@ -19,7 +19,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.environ.get("DIT_LIB") or os.path.join(_PKG, "libdit.so")
 
 DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_SHAPE, DIT_ERR_NOT_LOADED, DIT_ERR_OOM, DIT_ERR_CUDA, DIT_ERR_TIMEOUT = range(7)
-PREC_BF16, PREC_F32 = 0, 1
+PREC_BF16, PREC_F32, PREC_FP8 = 0, 1, 2
 COND_CROSS, COND_JOINT = 0, 1
 DTYPE_F32, DTYPE_BF16 = 0, 1
 LOOP_PARTIAL_SCHEDULE = 1

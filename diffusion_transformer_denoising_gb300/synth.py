@@ -24,6 +24,7 @@ import numpy as np
 
 PREC_BF16 = 0
 PREC_F32 = 1
+PREC_FP8 = 2   # bf16 activations; the LayerNorm-fed GEMMs in e4m3
 COND_CROSS = 0
 COND_JOINT = 1
 
@@ -126,7 +127,8 @@ def make_weights(cfg: dict, seed: int = 0, std: float = 0.02,
 
     blocks: optional iterable of block indices to draw (others are skipped;
     non-block tensors are always drawn).  With precision bf16 the values are
-    rounded to bf16, the precision both sides then read.
+    rounded to bf16 (also for fp8 precision, whose weights are quantized
+    from these values on the device), the precision both sides then read.
     """
     keep = None if blocks is None else {f"blocks.{b}." for b in blocks}
     out = {}
@@ -135,7 +137,7 @@ def make_weights(cfg: dict, seed: int = 0, std: float = 0.02,
                 not any(name.startswith(k) for k in keep):
             continue
         w = _rng(seed, i).standard_normal(shape, dtype=np.float32) * np.float32(std)
-        if cfg["precision"] == PREC_BF16:
+        if cfg["precision"] in (PREC_BF16, PREC_FP8):
             w = round_bf16(w)
         out[name] = w
     return out
@@ -155,7 +157,7 @@ def make_cond(cfg: dict, batch: int = 1, seed: int = 2, length=None) -> np.ndarr
     L = length if length is not None else cfg["cond_len"]
     c = _rng(seed, 10**6 + 1).standard_normal((batch, L, cfg["cond_dim"]),
                                               dtype=np.float32)
-    if cfg["precision"] == PREC_BF16:
+    if cfg["precision"] in (PREC_BF16, PREC_FP8):
         c = round_bf16(c)
     return c
 

@@ -58,7 +58,7 @@ typedef enum {
   DIT_ERR_TIMEOUT = 6      /* a kernel gave up a bounded wait (see dit_synchronize) */
 } dit_status;
 
-enum { DIT_PREC_BF16 = 0, DIT_PREC_F32 = 1 };
+enum { DIT_PREC_BF16 = 0, DIT_PREC_F32 = 1, DIT_PREC_FP8 = 2 };
 enum { DIT_COND_CROSS = 0, DIT_COND_JOINT = 1 };
 enum { DIT_DTYPE_F32 = 0, DIT_DTYPE_BF16 = 1 };
 /* dit_denoise_loop flags */
@@ -84,6 +84,11 @@ enum {
  *                 DIT_COND_JOINT: dual-stream joint attention with them
  *   precision     DIT_PREC_BF16: bf16 weights/activations, fp32 accumulate
  *                 (tcgen05 tensor cores; requires head_dim == 128);
+ *                 DIT_PREC_FP8: as bf16, except that the GEMMs fed by a
+ *                 LayerNorm (self-attention Q/K/V, cross-attention Q, MLP
+ *                 up-projection) take e4m3 operands: weights quantized at
+ *                 load with one scale per output row, the LayerNorm output
+ *                 with one scale per token row (requires hidden % 16 == 0);
  *                 DIT_PREC_F32: fp32 everywhere (test mode, CUDA cores)
  *   ln_eps, rope_theta, timestep_scale (t = timestep_scale * sigma)
  */

@@ -214,3 +214,55 @@ def test_image_block_sweep_65536_tokens(image_model):
     the persistent walk used for short key ranges."""
     cfg, W, m = image_model
     _image_block_case(cfg, W, m, (1, 512, 512), 2, (0,), seed=25)
+
+
+def test_fp8_video_block_full_size():
+    """DIT_PREC_FP8 at the video block's full size (32760 tokens, batch 2),
+    sampled rows against the oracle."""
+    from tests.gpu_util import assert_fp8_block_close
+    cfg = synth.config("video", depth=1, precision=synth.PREC_FP8)
+    W = synth.make_weights(cfg, seed=0)
+    m = make_model(cfg, W)
+    grid = synth.grid(cfg)
+    N, L = int(np.prod(grid)), cfg["cond_len"]
+    lat = synth.make_latent(cfg, batch=1, seed=1)
+    ctx = np.concatenate([synth.make_cond(cfg, batch=1, seed=2), np.zeros((1, L, cfg["cond_dim"]), np.float32)])
+    x0 = np.stack([O.patch_embed(lat[0], W, cfg)] * 2).astype(np.float32)
+    mod = O.timestep_modulation(700.0, W, cfg)
+    mods = np.stack([mod, mod]).astype(np.float32)
+    x = dev(x0)
+    m.dit_block_forward(0, x, None, dev(mods), dev(ctx), 2, grid, L)
+    m.dit_synchronize()
+    got = host(x)
+    rows = _rows(N, extra=range(N - 120, N - 110))
+    angles = O.rope_angles(O.token_positions(grid), cfg["rope_axes"], cfg["rope_theta"])
+    for b in range(2):
+        ref = O.block_cross(x0[b], mods[b], ctx[b], W, 0, cfg, grid, rows=rows, angles=angles)
+        assert_fp8_block_close(got[b][rows], ref, x0[b][rows], case=f"fp8 video block b{b}")
+    m.close()
+
+
+def test_fp8_video_loop_tracks_fp32_path_full_tokens():
+    """The fp8 video loop at the full token count (depth 4, two CFG + Euler
+    steps) against the fp32 test path with the same bf16-valued weights."""
+    from tests.gpu_util import COS_FP8_LOOP, log_errors
+    cfg_8 = synth.config("video", depth=4, precision=synth.PREC_FP8)
+    cfg_f = dict(cfg_8, precision=synth.PREC_F32)
+    W = synth.make_weights(cfg_8, seed=41)
+    L = cfg_8["cond_len"]
+    lat = synth.make_latent(cfg_8, batch=1, seed=42)
+    cond = synth.make_cond(cfg_8, batch=1, seed=43)
+    unc = np.zeros_like(cond)
+    sig = O.shift_sigma(O.sigma_schedule(cfg_8["steps"]), cfg_8["shift"])[:3].astype(np.float32)
+    out = {}
+    for name, cfg in (("fp8", cfg_8), ("fp32", cfg_f)):
+        m = make_model(cfg, W)
+        x = dev(lat)
+        m.dit_denoise_loop(x, 1, cfg["latent"], dev(cond), dev(unc), L, sig, cfg["guidance"],
+                           flags=dit.LOOP_PARTIAL_SCHEDULE)
+        m.dit_synchronize()
+        out[name] = host(x)[0]
+        m.close()
+    c_all, c_upd = cosine(out["fp8"], out["fp32"]), cosine(out["fp8"] - lat[0], out["fp32"] - lat[0])
+    log_errors("fp8 video loop depth 4", cos=c_all, cos_update=c_upd)
+    assert c_all >= COS_FP8_LOOP and c_upd >= COS_FP8_LOOP - 0.01, (c_all, c_upd)

@@ -424,3 +424,59 @@ def test_loop_cuda_graph_is_bitwise_eager(which, tiny, small_cross, small_joint)
     eager3, _ = run(0, 2.5)
     graph3, _ = run(dit.LOOP_CUDA_GRAPH, 2.5)          # new scalar: captured again
     assert np.array_equal(eager3, graph3) and not np.array_equal(eager3, eager)
+
+
+# ------------------------------------------------------------------ fp8 precision
+@pytest.mark.parametrize("mode,grid,L", [(synth.COND_CROSS, (3, 10, 13), 77), (synth.COND_CROSS, (2, 9, 7), 5),
+                                         (synth.COND_JOINT, (1, 12, 20), 64), (synth.COND_JOINT, (1, 7, 9), 33)])
+def test_fp8_block(mode, grid, L):
+    """DIT_PREC_FP8: the same block as the bf16 tests with the LayerNorm-fed
+    GEMMs in e4m3 (weights quantized at load, activations per row), against
+    the oracle on the same bf16-valued weights."""
+    from tests.gpu_util import assert_fp8_block_close
+    cfg = small_bf16_cfg(mode, precision=synth.PREC_FP8, depth=1)
+    W = synth.make_weights(cfg, seed=17)
+    m = make_model(cfg, W)
+    N = int(np.prod(grid))
+    rng = np.random.default_rng(N + 7 * L)
+    x0 = (rng.standard_normal((2, N, cfg["hidden"])) * 0.5).astype(np.float32)
+    ctx = synth.make_cond(cfg, batch=2, seed=L + 1, length=L)
+    mods = np.stack([O.timestep_modulation(t, W, cfg) for t in (300.0, 800.0)])
+    x = dev(x0)
+    if mode == synth.COND_CROSS:
+        m.dit_block_forward(0, x, None, dev(mods), dev(ctx), 2, grid, L)
+    else:
+        xc = dev(ctx)
+        m.dit_block_forward(0, x, xc, dev(mods), None, 2, grid, L)
+    m.dit_synchronize()
+    got = host(x)
+    for b in range(2):
+        if mode == synth.COND_CROSS:
+            ref = O.block_cross(x0[b], mods[b], ctx[b], W, 0, cfg, grid)
+        else:
+            ref = O.block_joint(x0[b], ctx[b], mods[b], W, 0, cfg, grid)[0]
+        assert_fp8_block_close(got[b], ref, x0[b], case=f"fp8 block mode {mode} grid {grid} L {L} b{b}")
+    m.close()
+
+
+@pytest.mark.parametrize("mode", [synth.COND_CROSS, synth.COND_JOINT])
+def test_fp8_denoise_loop(mode):
+    from tests.gpu_util import COS_FP8_LOOP, log_errors
+    cfg = small_bf16_cfg(mode, precision=synth.PREC_FP8)
+    W = synth.make_weights(cfg, seed=18)
+    m = make_model(cfg, W)
+    thw = (2, 12, 18) if mode == synth.COND_CROSS else (1, 24, 20)
+    L = 40
+    lat = synth.make_latent(cfg, batch=1, seed=23, latent=thw)
+    cond = synth.make_cond(cfg, batch=1, seed=24, length=L)
+    unc = np.zeros_like(cond)
+    sig = O.shift_sigma(O.sigma_schedule(3), 3.0).astype(np.float32)
+    x = dev(lat)
+    m.dit_denoise_loop(x, 1, thw, dev(cond), dev(unc), L, sig, 4.0)
+    m.dit_synchronize()
+    got = host(x)[0]
+    ref = O.denoise_loop(lat[0], cond[0], unc[0], W, cfg, sig.astype(np.float64), 4.0)
+    c_all, c_upd = cosine(got, ref), cosine(got - lat[0], ref - lat[0])
+    log_errors(f"fp8 loop mode {mode}", cos=c_all, cos_update=c_upd)
+    assert c_all >= COS_FP8_LOOP and c_upd >= COS_FP8_LOOP - 0.01, (c_all, c_upd)
+    m.close()
