@@ -58,13 +58,10 @@ WORKLOADS = {
 # valid only for the exact kernel source it was captured on.
 TRAFFIC = {
     # kernel source file -> (sha256 prefix of the source, workload, bytes per launch).
-    # attn_tc.cu: dram__bytes_read.sum + dram__bytes_write.sum = 387.9 MB for one
-    # batch-1 video self-attention launch (ncu capture of the block case),
-    # scaled x2 to the batch-2 launch the step runs (traffic grows with the
-    # number of query rows).  The source hash was moved on by a change to the
-    # host-side launcher only (per-device shared-memory attribute); the
-    # kernel's device code is the one captured.
-    "attn_tc.cu": ("cfef0bdc32671c41", "video", 2 * 387.9e6),
+    # attn_tc.cu: dram__bytes_read.sum + dram__bytes_write.sum = 605.4 + 186.2 MB
+    # for one batch-2 video self-attention launch (the launch the step runs),
+    # from an ncu capture of the block case (one launch, --clock-control none).
+    "attn_tc.cu": ("aad0b5cb920dd3a0", "video", 605447680 + 186185984),
 }
 
 
@@ -325,13 +322,32 @@ def run_image_loop(args, clocks_gpu: str) -> dict:
     clk = clocks.stop()
     m.dit_synchronize()
     t_step = e0.elapsed_time(e1) / 1e3 / args.steps
+    # the same steps replayed from one captured step (DIT_LOOP_CUDA_GRAPH); the
+    # capture is made by an untimed call with the same buffers and step count
+    sched = _schedule(cfg, args.steps)
+    gflags = flags | dit.LOOP_CUDA_GRAPH
+    lat_g = lat0.clone()
+    m.dit_denoise_loop(lat_g, 1, cfg["latent"], cond, unc, L, sched, cfg["guidance"], gflags)
+    m.dit_synchronize()
+    lat_g.copy_(lat0)
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    m.dit_denoise_loop(lat_g, 1, cfg["latent"], cond, unc, L, sched, cfg["guidance"], gflags)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    m.dit_synchronize()
+    t_graph = g0.elapsed_time(g1) / 1e3 / args.steps
     fl = step_flops(cfg, 2, N, L)
     peaks = measured_peaks()
     out = {"what": WORKLOADS["image"]["desc"] + f", first {args.steps} of {cfg['steps']} steps, shift {cfg['shift']}",
            "steps_per_s": 1.0 / t_step, "ms_per_step": t_step * 1e3, "steps": args.steps,
            "attn_gemm_tflops": fl["total"] / t_step / 1e12,
            "pct_bf16_peak": 100 * fl["total"] / t_step / 1e12 / peaks["bf16"],
+           "graph_steps_per_s": 1.0 / t_graph, "graph_ms_per_step": t_graph * 1e3,
+           "graph_bitwise_equal": bool(torch.equal(lat_g, lat)),
            "finite": bool(torch.isfinite(lat).all().item()), "clocks": clk}
+    del lat_g
     m.close()
     del lat, lat0, cond, unc
     torch.cuda.empty_cache()

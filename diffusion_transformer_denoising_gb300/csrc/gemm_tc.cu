@@ -131,7 +131,10 @@ DIT_DEV void drain_tile_tma(const EpiParams& ep, const EpiMaps& maps, uint32_t t
       uint32_t r[UW];
       tmem_ld32(tacc + u * UW, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
       if constexpr (UW == 64) tmem_ld32(tacc + u * UW + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-      tmem_ld_wait();
+      // no memory clobber: the epilogue's bias and scale loads may issue
+      // while the tensor-memory load is in flight
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+      if constexpr (UW == 64) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
 #pragma unroll
       for (int j = 0; j < UW; ++j) v[j] = __uint_as_float(r[j]);
     }
