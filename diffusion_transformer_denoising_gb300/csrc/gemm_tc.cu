@@ -533,3 +533,7 @@ cudaError_t gemm_e4m3_tc_pair(const GemmArgs& g0, const GemmArgs& g1, int* err, 
 }
 
 }  // namespace dit
+
+static_assert(dit::TcGemmCfg<256>::SMEM_BYTES <= 232448 && dit::TcGemmCfg<128>::SMEM_BYTES <= 232448 &&
+                  dit::TcGemmCfg<64>::SMEM_BYTES <= 232448,
+              "GEMM tile set exceeds 227 KB of shared memory");
