@@ -3,9 +3,9 @@ tile coordinates and indices on the device (GEMM tiles and head-major store
 boxes, attention items and key tiles, LayerNorm rows and modulation entries)
 and records the first failure in the model's error word instead of touching
 memory; dit_synchronize then reports it.  Run over the small odd shapes of
-the CPU comparisons (ragged token counts, short condition lengths, K and N
-tails, both conditioning modes, complete loops), every check must pass and
-every result must still match the oracle.  Runs in a child process because
+the CPU comparisons (ragged token counts, a single token, short and
+single-token conditions, K and N tails, both conditioning modes, complete
+loops), every check must pass and every result must still match the oracle.  Runs in a child process because
 the library a process loads is fixed at its first use."""
 import os
 import subprocess
@@ -39,7 +39,8 @@ def model(cfg, W):
 # blocks: ragged grids, short conditions, K/N tails, both modes
 for mode, grid, L, kw in ((synth.COND_CROSS, (2, 9, 7), 5, {}), (synth.COND_CROSS, (3, 10, 13), 77, {}),
                           (synth.COND_CROSS, (1, 6, 11), 37, dict(mlp=648, cond_dim=200)),
-                          (synth.COND_JOINT, (1, 7, 9), 33, {}), (synth.COND_JOINT, (1, 12, 20), 64, {})):
+                          (synth.COND_JOINT, (1, 7, 9), 33, {}), (synth.COND_JOINT, (1, 12, 20), 64, {}),
+                          (synth.COND_CROSS, (1, 1, 1), 1, {}), (synth.COND_JOINT, (1, 1, 1), 1, {})):
     cfg = small_bf16_cfg(mode, depth=1, **kw)
     W = synth.make_weights(cfg, seed=101)
     m = model(cfg, W)
@@ -103,4 +104,4 @@ def test_debug_bounds_build_on_odd_shapes():
     r = subprocess.run([sys.executable, "-c", _CHILD, ROOT], cwd=ROOT, env=env, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
-    assert "debug build checked 13" in r.stdout, r.stdout[-2000:]
+    assert "debug build checked 17" in r.stdout, r.stdout[-2000:]

@@ -480,3 +480,48 @@ def test_fp8_denoise_loop(mode):
     log_errors(f"fp8 loop mode {mode}", cos=c_all, cos_update=c_upd)
     assert c_all >= COS_FP8_LOOP and c_upd >= COS_FP8_LOOP - 0.01, (c_all, c_upd)
     m.close()
+
+
+# ------------------------------------------------------------------ degenerate shapes
+@pytest.mark.parametrize("prec", [synth.PREC_F32, synth.PREC_BF16])
+@pytest.mark.parametrize("mode", [synth.COND_CROSS, synth.COND_JOINT])
+@pytest.mark.parametrize("grid,L", [((1, 1, 1), 1), ((1, 1, 1), 3), ((1, 2, 1), 1)])
+def test_degenerate_single_token_and_single_condition(prec, mode, grid, L):
+    """One image/video token and/or one condition token: every GEMM has one
+    partial row tile, the attention one partial key tile with a single valid
+    key (cross mode, L = 1: the output row is that key's value row)."""
+    if prec == synth.PREC_F32:
+        cfg = synth.config("tiny", cond_mode=mode, depth=1, rope_axes=(0, 16, 16))
+        if mode == synth.COND_JOINT:
+            cfg["cond_dim"] = cfg["hidden"]
+        tol = lambda got, ref, case: assert_f32_close(got, ref, case)
+    else:
+        cfg = small_bf16_cfg(mode, depth=1)
+        tol = lambda got, ref, case: assert_block_close(got, ref, case=case)
+    W = synth.make_weights(cfg, seed=29)
+    m = make_model(cfg, W)
+    N = int(np.prod(grid))
+    rng = np.random.default_rng(77 + N + L)
+    x0 = (rng.standard_normal((2, N, cfg["hidden"])) * 0.5).astype(np.float32)
+    ctx = synth.make_cond(cfg, batch=2, seed=31 + L, length=L)
+    mods = np.stack([O.timestep_modulation(t, W, cfg) for t in (150.0, 650.0)])
+    x = dev(x0)
+    if mode == synth.COND_CROSS:
+        m.dit_block_forward(0, x, None, dev(mods), dev(ctx), 2, grid, L)
+    else:
+        xc = dev(ctx)
+        m.dit_block_forward(0, x, xc, dev(mods), None, 2, grid, L)
+    m.dit_synchronize()
+    got = host(x)
+    for b in range(2):
+        if mode == synth.COND_CROSS:
+            ref = O.block_cross(x0[b], mods[b], ctx[b], W, 0, cfg, grid)
+        else:
+            ref = O.block_joint(x0[b], ctx[b], mods[b], W, 0, cfg, grid)[0]
+        tol(got[b], ref, f"degenerate {grid} L {L} mode {mode} prec {prec} b{b}")
+    m.close()
+
+
+def assert_f32_close(got, ref, case):
+    e = rel_max_err(got, ref)
+    assert e < TOL_F32, f"{case}: max error {e:.3e} of the reference RMS"
