@@ -56,3 +56,29 @@ def test_aggregate_max_over_ranks_gloo():
 def test_single_rank_aggregate_is_identity():
     t, v = bench.aggregate(2.5, 5, 1, None)
     assert t == 2.5 and v == pytest.approx(2.0)
+
+
+def test_reference_line_states_its_extrapolation(monkeypatch, capsys):
+    """The reference arm's line: `config` is the GPU arm's object, the value
+    is labelled extrapolated, `steps` counts the samples that ran and
+    `ms_per_step` is their measured wall time (so steps x ms_per_step is the
+    time the arm actually spent), with the extrapolated full step beside it."""
+    import argparse
+    import json
+    calls = []
+
+    def fake_sample(workload):
+        calls.append(workload)
+        return dict(t_block=1.0, t_step=60.0, sample_s=0.001, sample="s", cores=4)
+
+    monkeypatch.setattr(bench, "cpu_oracle_sample", fake_sample)
+    monkeypatch.setattr(bench, "_oracle_block_weights", lambda w: None)
+    bench.run_reference(argparse.Namespace(gpus=1, steps=3, warmup=1, workload="video"))
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["extrapolated"] is True
+    assert line["config"] == bench.workload_config("video", 3, 1)
+    assert line["steps"] == 3 and len(calls) == 4            # warm-up + timed samples
+    assert line["ms_per_step"] * line["steps"] < 1e3         # the time that ran, not the extrapolation
+    assert line["ms_per_full_step_extrapolated"] == pytest.approx(60.0e3)
+    assert line["value"] == pytest.approx(1 / 60.0)
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["extrapolated"] is True
