@@ -16,8 +16,8 @@ The headline loop is timed with one CUDA event pair around the whole call
 (launches are counted, nothing else is recorded on the stream); the
 per-kernel breakdown and the roofline figure come from a second, separately
 timed pass with an event pair around every launch.  On one GPU the default
-line also carries the 30-block image loop (`image_loop`), the video workload
-in fp8 precision (`fp8_loop`), the seven points of the image block
+line also carries the 30-block image loop (`image_loop`), the video and image
+workloads in fp8 precision (`fp8_loop`, `fp8_image_loop`), the seven points of the image block
 batch/sequence sweep (`sweep`) and the CPU oracle timings (`cpu_baseline`).
 
 With N > 1 (torchrun), each rank denoises its own request on its own GPU
@@ -354,15 +354,15 @@ def run_image_loop(args, clocks_gpu: str) -> dict:
     return out
 
 
-def run_fp8_loop(args, clocks_gpu: str) -> dict:
-    """Steps/s of the video workload in fp8 precision (the LayerNorm-fed GEMMs
-    -- Q/K/V, cross-attention Q, MLP up-projection -- in e4m3), timed like the
-    headline; then a separate per-launch pass for the fp8 GEMMs' rate, given
-    against the fp8 peak taken as twice the measured bf16 peak (the nominal
-    dense fp8 : bf16 ratio, 4.5 : 2.25 PFLOP/s)."""
+def run_fp8_loop(args, clocks_gpu: str, workload: str = "video") -> dict:
+    """Steps/s of a workload in fp8 precision (the LayerNorm-fed GEMMs -- Q/K/V,
+    cross-attention Q, MLP up-projection -- in e4m3), timed like the headline;
+    then a separate per-launch pass for the fp8 GEMMs' rate, given against the
+    fp8 peak taken as twice the measured bf16 peak (the nominal dense fp8 :
+    bf16 ratio, 4.5 : 2.25 PFLOP/s)."""
     import torch
     from diffusion_transformer_denoising_gb300 import dit
-    cfg = synth.config("video", precision=synth.PREC_FP8)
+    cfg = synth.config(WORKLOADS[workload]["cfg"], precision=synth.PREC_FP8)
     L, C, D, F = cfg["cond_len"], cfg["in_channels"], cfg["hidden"], cfg["mlp"]
     N = int(np.prod(synth.grid(cfg)))
     m = dit.DiT(cfg)
@@ -399,11 +399,16 @@ def run_fp8_loop(args, clocks_gpu: str) -> dict:
     m.dit_synchronize()
     fl = step_flops(cfg, 2, N, L)
     peaks = measured_peaks()
-    f8_flops = 2 * 2 * N * D * (3 * D + D + F) * cfg["depth"]          # Q/K/V, cross Q, FFN1 per step
+    if cfg["cond_mode"] == synth.COND_CROSS:
+        f8_flops = 2 * 2 * N * D * (3 * D + D + F) * cfg["depth"]      # Q/K/V, cross Q, FFN1 per step
+    else:
+        # Q/K/V and FFN1 of both streams; the last block's condition stream
+        # skips its MLP (its output is never read)
+        f8_flops = 2 * 2 * (N + L) * D * (3 * D + F) * cfg["depth"] - 2 * 2 * L * D * F
     f8_ms = sum(prof[k][1] for k in ("gemm_qkv", "gemm_cross_q", "gemm_ffn1")) / k_prof
     f8_tflops = f8_flops / (f8_ms / 1e3) / 1e12
-    out = {"what": "video workload with the LayerNorm-fed GEMMs in e4m3 (per-row / per-output-channel scales), "
-                   f"first {args.steps} of {cfg['steps']} steps",
+    out = {"what": f"{workload} workload with the LayerNorm-fed GEMMs in e4m3 (per-row / per-output-channel "
+                   f"scales), first {args.steps} of {cfg['steps']} steps",
            "steps_per_s": 1.0 / t_step, "ms_per_step": t_step * 1e3, "steps": args.steps,
            "attn_gemm_tflops": fl["total"] / t_step / 1e12,
            "fp8_gemm_tflops": f8_tflops, "fp8_peak_tflops": 2 * peaks["bf16_sustained"],
@@ -573,6 +578,7 @@ def run_gpu(args):
         torch.cuda.empty_cache()
         line["image_loop"] = run_image_loop(args, gpu_id)
         line["fp8_loop"] = run_fp8_loop(args, gpu_id)
+        line["fp8_image_loop"] = run_fp8_loop(args, gpu_id, "image")
         line["sweep"] = sweep_points(args, steps=3, warmup=1)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_leg(args.workload)
