@@ -79,8 +79,13 @@ def step_flops(cfg: dict, B: int, N: int, L: int) -> dict:
         gemm = 2 * B * S * D * (3 * D + D + 2 * F)
         attn_self = 4 * B * H * S * S * hd
         attn_cross = 0
-    return dict(gemm=depth * gemm, attn_self=depth * attn_self, attn_cross=depth * attn_cross,
-                total=depth * (gemm + attn_self + attn_cross), attn_self_per_launch=attn_self)
+    total_gemm = depth * gemm
+    if cfg["cond_mode"] != synth.COND_CROSS:
+        # the last block's condition stream skips its out-projection and MLP
+        # (their output is never read), so they are not counted
+        total_gemm -= 2 * B * L * D * (D + 2 * F)
+    return dict(gemm=total_gemm, attn_self=depth * attn_self, attn_cross=depth * attn_cross,
+                total=total_gemm + depth * (attn_self + attn_cross), attn_self_per_launch=attn_self)
 
 
 def workload_config(workload: str, steps: int, world: int) -> dict:
