@@ -65,10 +65,11 @@ TRAFFIC = {
 }
 
 
-def step_flops(cfg: dict, B: int, N: int, L: int) -> dict:
+def step_flops(cfg: dict, B: int, N: int, L: int, loop: bool = True) -> dict:
     """Algorithmic FLOPs of one step: 2*MACs of every block GEMM plus QK^T and
     PV of attention, split by kind.  Cross-attention keys/values are computed
-    once per loop call and are not part of a step."""
+    once per loop call and are not part of a step.  loop=False counts a
+    stand-alone block forward (every output of both streams computed)."""
     D, F, H, hd, depth = cfg["hidden"], cfg["mlp"], cfg["heads"], cfg["head_dim"], cfg["depth"]
     if cfg["cond_mode"] == synth.COND_CROSS:
         gemm = 2 * B * N * D * (3 * D + D + D + D + 2 * F)
@@ -80,9 +81,9 @@ def step_flops(cfg: dict, B: int, N: int, L: int) -> dict:
         attn_self = 4 * B * H * S * S * hd
         attn_cross = 0
     total_gemm = depth * gemm
-    if cfg["cond_mode"] != synth.COND_CROSS:
-        # the last block's condition stream skips its out-projection and MLP
-        # (their output is never read), so they are not counted
+    if loop and cfg["cond_mode"] != synth.COND_CROSS:
+        # in the loop the last block's condition stream skips its
+        # out-projection and MLP (their output is never read): not counted
         total_gemm -= 2 * B * L * D * (D + 2 * F)
     return dict(gemm=total_gemm, attn_self=depth * attn_self, attn_cross=depth * attn_cross,
                 total=total_gemm + depth * (attn_self + attn_cross), attn_self_per_launch=attn_self)
@@ -624,7 +625,7 @@ def run_block_case(args):
         m.dit_block_forward(0, x, xc, mod, None if joint else cond, B, grid, L)
     prof = m.dit_profile_stop()
     m.dit_synchronize()
-    fl = step_flops(cfg, B, N, L)
+    fl = step_flops(cfg, B, N, L, loop=False)   # dit_block_forward computes both streams' outputs
     n, ms = prof["attn_self"]
     out = {"case": f"one {args.workload} block, batch {B}, {args.precision}", "per_kernel_ms": {k: v[1] / args.steps for k, v in prof.items()},
            "attn_self_tflops": fl["attn_self_per_launch"] / (ms / max(n, 1) / 1e3) / 1e12,
