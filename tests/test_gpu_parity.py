@@ -525,3 +525,26 @@ def test_degenerate_single_token_and_single_condition(prec, mode, grid, L):
 def assert_f32_close(got, ref, case):
     e = rel_max_err(got, ref)
     assert e < TOL_F32, f"{case}: max error {e:.3e} of the reference RMS"
+
+
+@pytest.mark.parametrize("which", ["tiny_fp32", "bf16_cross", "bf16_joint"])
+def test_loop_resumed_from_a_sub_schedule_is_bitwise_the_same(which, tiny, small_cross, small_joint):
+    """Resume: four steps in one call equal two calls over the sub-schedules
+    sigmas[0:3] and sigmas[2:5] (DIT_LOOP_PARTIAL_SCHEDULE), bit for bit."""
+    if which == "tiny_fp32":
+        cfg, W, m = tiny
+        thw, L = cfg["latent"], cfg["cond_len"]
+    else:
+        cfg, W, m = small_cross if which == "bf16_cross" else small_joint
+        thw, L = ((2, 12, 16) if which == "bf16_cross" else (1, 16, 20)), 24
+    lat = synth.make_latent(cfg, batch=1, seed=95, latent=thw)
+    cond = dev(synth.make_cond(cfg, batch=1, seed=96, length=L))
+    unc = dev(np.zeros((1, L, cfg["cond_dim"]), np.float32))
+    sig = O.shift_sigma(O.sigma_schedule(4), 3.0).astype(np.float32)
+    x_all = dev(lat)
+    m.dit_denoise_loop(x_all, 1, thw, cond, unc, L, sig, 4.0)
+    x_two = dev(lat)
+    m.dit_denoise_loop(x_two, 1, thw, cond, unc, L, sig[0:3].copy(), 4.0, flags=dit.LOOP_PARTIAL_SCHEDULE)
+    m.dit_denoise_loop(x_two, 1, thw, cond, unc, L, sig[2:5].copy(), 4.0, flags=dit.LOOP_PARTIAL_SCHEDULE)
+    m.dit_synchronize()
+    assert np.array_equal(host(x_all), host(x_two))
