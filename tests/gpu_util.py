@@ -119,7 +119,11 @@ def small_bf16_cfg(mode=synth.COND_CROSS, **kw):
 # at the video block's full size, outputs 1.9e-2 RMS).  Bounds, per block, as
 # multiples of the reference RMS: (RMS error, largest element) of the output
 # and of the update (output minus input); final latents of a loop by cosine.
-TOL_FP8_OUT = (3e-2, 3e-1)
+# Where a block's input is zero -- the condition stream of the unconditional
+# pass enters the first joint block as all-zero tokens -- its output is its
+# update, so the output bound sits at the update's measured error plus
+# margin (measured there: output RMS 3.1e-2, element 0.33).
+TOL_FP8_OUT = (5e-2, 5e-1)
 TOL_FP8_UPDATE = (1e-1, 6e-1)
 COS_FP8_LOOP = 0.99
 

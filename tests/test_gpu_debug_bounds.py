@@ -24,8 +24,8 @@ import torch
 sys.path.insert(0, sys.argv[1])
 from diffusion_transformer_denoising_gb300 import dit, synth
 from oracle import dit_oracle as O
-from tests.gpu_util import (COS_BF16_LOOP, TOL_F32, assert_block_close, cosine, dev, host, rel_max_err,
-                            small_bf16_cfg)
+from tests.gpu_util import (COS_BF16_LOOP, TOL_F32, assert_block_close, assert_fp8_block_close, cosine, dev, host,
+                            rel_max_err, small_bf16_cfg)
 
 assert dit.LIB_PATH.endswith("libdit_debug.so"), dit.LIB_PATH
 torch.cuda.set_device(0)
@@ -40,7 +40,9 @@ def model(cfg, W):
 for mode, grid, L, kw in ((synth.COND_CROSS, (2, 9, 7), 5, {}), (synth.COND_CROSS, (3, 10, 13), 77, {}),
                           (synth.COND_CROSS, (1, 6, 11), 37, dict(mlp=648, cond_dim=200)),
                           (synth.COND_JOINT, (1, 7, 9), 33, {}), (synth.COND_JOINT, (1, 12, 20), 64, {}),
-                          (synth.COND_CROSS, (1, 1, 1), 1, {}), (synth.COND_JOINT, (1, 1, 1), 1, {})):
+                          (synth.COND_CROSS, (1, 1, 1), 1, {}), (synth.COND_JOINT, (1, 1, 1), 1, {}),
+                          (synth.COND_CROSS, (3, 10, 13), 77, dict(precision=synth.PREC_FP8)),
+                          (synth.COND_JOINT, (1, 7, 9), 33, dict(precision=synth.PREC_FP8))):
     cfg = small_bf16_cfg(mode, depth=1, **kw)
     W = synth.make_weights(cfg, seed=101)
     m = model(cfg, W)
@@ -62,7 +64,10 @@ for mode, grid, L, kw in ((synth.COND_CROSS, (2, 9, 7), 5, {}), (synth.COND_CROS
             ref = O.block_cross(x0[b], mods[b], ctx[b], W, 0, cfg, grid)
         else:
             ref = O.block_joint(x0[b], ctx[b], mods[b], W, 0, cfg, grid)[0]
-        assert_block_close(got[b], ref, case=f"debug build block {mode} {grid} {L}")
+        if cfg["precision"] == synth.PREC_FP8:
+            assert_fp8_block_close(got[b], ref, x0[b], case=f"debug build fp8 block {mode} {grid} {L}")
+        else:
+            assert_block_close(got[b], ref, case=f"debug build block {mode} {grid} {L}")
         n_checked += 1
     m.close()
 
@@ -104,4 +109,4 @@ def test_debug_bounds_build_on_odd_shapes():
     r = subprocess.run([sys.executable, "-c", _CHILD, ROOT], cwd=ROOT, env=env, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
-    assert "debug build checked 17" in r.stdout, r.stdout[-2000:]
+    assert "debug build checked 21" in r.stdout, r.stdout[-2000:]

@@ -266,3 +266,32 @@ def test_fp8_video_loop_tracks_fp32_path_full_tokens():
     c_all, c_upd = cosine(out["fp8"], out["fp32"]), cosine(out["fp8"] - lat[0], out["fp32"] - lat[0])
     log_errors("fp8 video loop depth 4", cos=c_all, cos_update=c_upd)
     assert c_all >= COS_FP8_LOOP and c_upd >= COS_FP8_LOOP - 0.01, (c_all, c_upd)
+
+
+def test_fp8_image_block_full_size():
+    """DIT_PREC_FP8 on the dual-stream image block at full size (4096 image +
+    512 condition tokens, batch 2): the paired e4m3 GEMMs carry their own row
+    scales per stream; sampled rows of both streams against the oracle."""
+    from tests.gpu_util import assert_fp8_block_close
+    cfg = synth.config("image", depth=1, precision=synth.PREC_FP8)
+    W = synth.make_weights(cfg, seed=0)
+    m = make_model(cfg, W)
+    grid = synth.grid(cfg)
+    N, L, D = int(np.prod(grid)), cfg["cond_len"], cfg["hidden"]
+    rng = np.random.default_rng(33)
+    x0 = (rng.standard_normal((2, N, D)) * 0.2).astype(np.float32)
+    xc0 = np.concatenate([synth.make_cond(cfg, batch=1, seed=34), np.zeros((1, L, D), np.float32)])
+    mod = O.timestep_modulation(400.0, W, cfg)
+    mods = np.stack([mod, mod]).astype(np.float32)
+    x, xc = dev(x0), dev(xc0)
+    m.dit_block_forward(0, x, xc, dev(mods), None, 2, grid, L)
+    m.dit_synchronize()
+    gx, gc = host(x), host(xc)
+    rows = _rows(L + N, extra=range(L - 3, L + 3))
+    angles = O.rope_angles(O.token_positions(grid), cfg["rope_axes"], cfg["rope_theta"])
+    for b in range(2):
+        ref = O.block_joint(x0[b], xc0[b], mods[b], W, 0, cfg, grid, rows=rows, angles=angles)
+        got = np.concatenate([gc[b], gx[b]])[rows]
+        inp = np.concatenate([xc0[b], x0[b]])[rows]
+        assert_fp8_block_close(got, ref, inp, case=f"fp8 image block b{b}")
+    m.close()
