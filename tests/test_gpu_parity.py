@@ -548,3 +548,37 @@ def test_loop_resumed_from_a_sub_schedule_is_bitwise_the_same(which, tiny, small
     m.dit_denoise_loop(x_two, 1, thw, cond, unc, L, sig[2:5].copy(), 4.0, flags=dit.LOOP_PARTIAL_SCHEDULE)
     m.dit_synchronize()
     assert np.array_equal(host(x_all), host(x_two))
+
+
+def test_two_models_on_unordered_streams_are_isolated():
+    """Separate models share nothing: two models' loops enqueued on two
+    streams with no ordering between them give, bit for bit, what each gives
+    alone (tiny fp32 and small bf16 models, different weights and inputs)."""
+    import torch
+    cases = []
+    for cfg, seed in ((synth.config("tiny"), 201), (small_bf16_cfg(synth.COND_CROSS), 202)):
+        W = synth.make_weights(cfg, seed=seed)
+        thw = cfg["latent"] if cfg["precision"] == synth.PREC_F32 else (2, 12, 16)
+        L = 16
+        lat = synth.make_latent(cfg, batch=1, seed=seed + 1, latent=thw)
+        cond = dev(synth.make_cond(cfg, batch=1, seed=seed + 2, length=L))
+        unc = dev(np.zeros((1, L, cfg["cond_dim"]), np.float32))
+        cases.append((make_model(cfg, W), thw, L, lat, cond, unc))
+    sig = O.shift_sigma(O.sigma_schedule(4), 3.0).astype(np.float32)
+    alone = []
+    for m, thw, L, lat, cond, unc in cases:
+        x = dev(lat)
+        m.dit_denoise_loop(x, 1, thw, cond, unc, L, sig, 5.0)
+        m.dit_synchronize()
+        alone.append(host(x))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    xs = [dev(c[3]) for c in cases]
+    torch.cuda.synchronize()
+    for (m, thw, L, lat, cond, unc), x, st in zip(cases, xs, streams):
+        m.dit_denoise_loop(x, 1, thw, cond, unc, L, sig, 5.0, stream=st)
+    for (m, *_), st in zip(cases, streams):
+        m.dit_synchronize(stream=st)
+    for a, x in zip(alone, xs):
+        assert np.array_equal(a, host(x))
+    for m, *_ in cases:
+        m.close()
