@@ -9,9 +9,9 @@ GPU's block input (all tokens, for the keys and values) and computes the
 block output for 64 sampled rows.  Between the checked steps the latent
 advances through dit_denoise_loop itself.
 
-The 30-block image loop (4096 + 512 joint tokens) runs complete against the
-fp32 test-precision path (pinned to the oracle at 1e-4 on complete loops),
-with the same bf16-valued weights.
+The 30-block image loop (4096 + 512 joint tokens) runs complete, in bf16 and
+in fp8 precision, against the fp32 test-precision path (pinned to the oracle
+at 1e-4 on complete loops), with the same bf16-valued weights.
 """
 import time
 
@@ -84,10 +84,13 @@ def test_video_loop_teacher_forced_every_block():
 def test_image_loop_full_depth_all_steps_tracks_fp32_path():
     """The complete image loop: 30 dual-stream blocks, 30 steps of the shift-3
     schedule, CFG scale 4, 4096 + 512 tokens; bf16 production path against
-    the fp32 test-precision path, final latents cosine >= 0.999."""
+    the fp32 test-precision path, final latents cosine >= 0.999; the fp8
+    precision against the same fp32 result, cosine >= 0.99."""
     import torch
+    from tests.gpu_util import COS_FP8_LOOP
     cfg_b = synth.config("image")
     cfg_f = dict(cfg_b, precision=synth.PREC_F32)
+    cfg_8 = dict(cfg_b, precision=synth.PREC_FP8)
     Wt = synth.make_weights_torch(cfg_b, seed=81, device="cuda")   # bf16 values; the fp32 model widens them
     L = cfg_b["cond_len"]
     lat = synth.make_latent(cfg_b, batch=1, seed=82)
@@ -95,7 +98,7 @@ def test_image_loop_full_depth_all_steps_tracks_fp32_path():
     unc = np.zeros_like(cond)
     sig = O.shift_sigma(O.sigma_schedule(cfg_b["steps"]), cfg_b["shift"]).astype(np.float32)
     out, secs = {}, {}
-    for name, cfg in (("bf16", cfg_b), ("fp32", cfg_f)):
+    for name, cfg in (("bf16", cfg_b), ("fp8", cfg_8), ("fp32", cfg_f)):
         m = dit.DiT(cfg)
         m.load_weights(Wt)
         x = dev(lat)
@@ -108,7 +111,11 @@ def test_image_loop_full_depth_all_steps_tracks_fp32_path():
         torch.cuda.empty_cache()
     del Wt
     c_all, c_upd = cosine(out["bf16"], out["fp32"]), cosine(out["bf16"] - lat[0], out["fp32"] - lat[0])
-    log_errors("image full loop", cos=c_all, cos_update=c_upd, bf16_s=secs["bf16"], fp32_s=secs["fp32"])
-    assert np.isfinite(out["bf16"]).all()
+    f_all, f_upd = cosine(out["fp8"], out["fp32"]), cosine(out["fp8"] - lat[0], out["fp32"] - lat[0])
+    log_errors("image full loop", cos=c_all, cos_update=c_upd, fp8_cos=f_all, fp8_cos_update=f_upd,
+               bf16_s=secs["bf16"], fp8_s=secs["fp8"], fp32_s=secs["fp32"])
+    assert np.isfinite(out["bf16"]).all() and np.isfinite(out["fp8"]).all()
     assert c_all >= COS_BF16_LOOP, (c_all, c_upd)
     assert c_upd >= 0.99, (c_all, c_upd)
+    # fp8 precision over the complete loop (reading R16's loop bound)
+    assert f_all >= COS_FP8_LOOP and f_upd >= COS_FP8_LOOP - 0.01, (f_all, f_upd)
