@@ -133,7 +133,10 @@ dit_status dit_create(const dit_config* cfg, int device, dit_model** out);
  * DIT_ERR_SHAPE and nothing of this call is kept (SGLang-Diffusion "Support
  * New Diffusion Models", "Reuse component loaders": strict key and shape
  * checks, fail instead of falling back).  The forward calls return
- * DIT_ERR_NOT_LOADED until every parameter has been loaded.  Synchronous. */
+ * DIT_ERR_NOT_LOADED until every parameter has been loaded.  Synchronous.
+ * With DIT_PREC_FP8 the weights of the self-attention Q/K/V, cross-attention
+ * Q and MLP up-projection are quantized here on the device to e4m3 with one
+ * scale per output row (max |row| / 448); the others are stored as bf16. */
 dit_status dit_load_weights(dit_model* m, const dit_tensor* tensors, int n);
 
 /* Host-only queries on a configuration (no GPU needed): the number of
