@@ -22,6 +22,14 @@
 // SM walks the tile list with stride gridDim.x; tiles are ordered N-fastest so
 // CTAs running together share the same A rows through L2.
 //
+// Widths that are multiples of 256 run on CTA pairs (clusters of two): a
+// 256 x 256 tile per pair, one tcgen05.mma.cta_group::2 (M = 256) per K step
+// issued by the leader CTA, each CTA loading its own 128 rows of A and 128 of
+// the tile's 256 W rows.  The L2 then serves 32 KB per CTA and K block
+// instead of 48 KB; operand delivery from L2 is what limits the 128 x 256
+// single-CTA main loop once the epilogue's stores compete with it.  The
+// epilogue is unchanged: each CTA drains its own 128 x 256 accumulator.
+//
 // Every mbarrier wait is bounded (common.cuh); on a timeout the CTA records
 // the failure in *err, winds down, waits for its own copies and MMAs in
 // flight, frees its TMEM and exits.
@@ -39,21 +47,29 @@ constexpr int GEMM_THREADS = 32 * (2 + EPI_WARPS);
 // F8: e4m3 operands (kind::f8f6f4); a K block is then 128 elements, the same
 // 128 bytes per tile row as 64 bf16 elements, so the tiles, swizzle and
 // descriptors are the same and only the MMA kind and K per MMA change.
-template <int BN, bool F8 = false>
+//
+// PAIR: the tile is 256 x BN and runs on a cluster of two CTAs (one
+// tcgen05.mma.cta_group::2 of M = 256 per K step, issued by the leader).  Each
+// CTA loads its own 128 rows of A and half of the tile's BN rows of W, so a
+// CTA reads 32 KB per K block instead of 48 KB, and holds its 128 x BN part
+// of the accumulator.
+template <int BN, bool F8 = false, bool PAIR = false>
 struct TcGemmCfg {
   static constexpr int BM = 128, BK = F8 ? 128 : 64;
   static constexpr int ESZ = F8 ? 1 : 2;
+  static constexpr int BN_CTA = PAIR ? BN / 2 : BN;  // W rows one CTA loads per tile
   static constexpr int A_BYTES = BM * BK * ESZ;
-  static constexpr int B_BYTES = BN * BK * ESZ;
+  static constexpr int B_BYTES = BN_CTA * BK * ESZ;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int STAGES = PAIR ? 6 : (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int BAR_BYTES = 256;
   static constexpr int STG_BYTES = 32 * 128;  // one epilogue warp's staging unit
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = STG_OFF + EPI_WARPS * STG_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + BAR_BYTES + 1024;
-  static constexpr uint32_t IDESC = F8 ? umma_idesc_e4m3(BM, BN) : umma_idesc_bf16(BM, BN, false);
+  static constexpr int MMA_M = PAIR ? 2 * BM : BM;
+  static constexpr uint32_t IDESC = F8 ? umma_idesc_e4m3(MMA_M, BN) : umma_idesc_bf16(MMA_M, BN, false);
   static constexpr int K_PER_MMA = F8 ? 32 : 16;  // 32 bytes of each row per MMA either way
 };
 
@@ -109,11 +125,12 @@ DIT_DEV int locate_tile(const GemmBatch<NP>& P, int tile, int* t) {
 
 // Drain one accumulator tile through shared memory and TMA.  UW = columns per
 // 128-byte unit (64 bf16 or 32 fp32).  The warp owns rows row0..row0+31 and
-// units u = half, half+2, ...; it releases the accumulator (tempty) as soon
-// as its last tcgen05.ld has completed.
-template <int BN, int UW>
+// units u = half, half+2, ...; it releases the accumulator (lane 0 calls
+// release(), an arrival on the accumulator's tempty barrier) as soon as its
+// last tcgen05.ld has completed.
+template <int BN, int UW, class Release>
 DIT_DEV void drain_tile_tma(const EpiParams& ep, const EpiMaps& maps, uint32_t tacc, int64_t row0, int64_t M, int N,
-                            int nb, int half, uint8_t* stg, uint64_t* tempty_bar, int* err) {
+                            int nb, int half, uint8_t* stg, Release release, int* err) {
   constexpr int NU = BN / UW;
   const int lane = threadIdx.x & 31;
   const int64_t row = row0 + lane;
@@ -121,7 +138,7 @@ DIT_DEV void drain_tile_tma(const EpiParams& ep, const EpiMaps& maps, uint32_t t
   const int64_t vrow = row < M ? row : M - 1;
   if (half >= NU) {
     __syncwarp();
-    if (lane == 0) mbar_arrive(tempty_bar);
+    if (lane == 0) release();
     return;
   }
 #pragma unroll 1
@@ -141,7 +158,7 @@ DIT_DEV void drain_tile_tma(const EpiParams& ep, const EpiMaps& maps, uint32_t t
     if (u + 2 >= NU) {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar);
+      if (lane == 0) release();
     }
     const int col0 = nb * BN + u * UW;
     if (col0 >= N || row0 >= M) continue;
@@ -197,10 +214,10 @@ DIT_DEV void drain_tile_tma(const EpiParams& ep, const EpiMaps& maps, uint32_t t
   }
 }
 
-template <int BN, int NP, bool F8>
+template <int BN, int NP, bool F8, bool PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ GemmBatch<NP> P, int N, int K, int* err) {
-  using C = TcGemmCfg<BN, F8>;
+  using C = TcGemmCfg<BN, F8, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -212,6 +229,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA pair: rank 0 (the leader) issues the MMAs of both CTAs.  Its full[s]
+  // counts the operand bytes of both CTAs (the peer's loads complete on it),
+  // its tempty[a] the epilogue warps of both; the leader's commits arrive on
+  // empty[s] and tfull[a] of both CTAs.  The peer's own full and tempty stay
+  // unused.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+  const bool leader = rank == 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -219,7 +243,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], EPI_WARPS);
+      mbar_init(&tempty[a], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -233,15 +257,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tma_prefetch_desc(&P.tmB[p]);
     }
   }
-  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR)
+      tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+    else
+      tmem_alloc(tmem_slot, C::TMEM_COLS);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // both CTAs' barriers are initialised before any remote arrival or copy
+  if constexpr (PAIR) cluster_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // a role that gives up also stops the other CTA's waits
+  auto abort_pair = [&]() {
+    if constexpr (PAIR) st_cluster_u32(cluster_map((const void*)abort_flag, rank ^ 1u), 1u);
+  };
 
   const int n_tiles = (N + BN - 1) / BN;
   const int k_blocks = (K + C::BK - 1) / C::BK;
   const int num_tiles = P.tile_end[NP - 1];
+  // Both CTAs of a pair walk the same tile list; tile (mb, nb) of a pair
+  // launch is 256 rows, of which CTA `rank` holds 128-row block 2 mb + rank.
+  const int first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int stride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (one thread)
@@ -254,43 +293,64 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // W tiles are reused by every row tile: keep them in L2 ahead of the
       // streamed A rows (FFN2, whose A is the 1.2 GB MLP hidden, 3 % faster)
       const uint64_t w_policy = l2_policy_evict_last();
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      const uint32_t full_leader = PAIR ? cluster_map(full, 0) : 0;
+      for (int tile = first; ok && tile < num_tiles; tile += stride) {
         int t, mb, nb;
         const int p = locate_tile(P, tile, &t);
         tile_coords(t, P.m_tiles[p], n_tiles, P.group_n, &mb, &nb);
         if (!DIT_BOUNDS(p >= 0 && p < NP && mb >= 0 && mb < P.m_tiles[p] && nb >= 0 && nb < n_tiles, err, 60)) {
           *abort_flag = 1;  // the other roles' waits return at once: the CTA winds down
+          abort_pair();
           ok = false;
           break;
         }
         const CUtensorMap* tmA = &P.tmA[p];
         const CUtensorMap* tmB = &P.tmB[p];
+        const int a_row = PAIR ? (2 * mb + (int)rank) * C::BM : mb * C::BM;
+        const int b_row = nb * BN + (int)rank * C::BN_CTA;
         // Short main loops (K <= 2048): the residual rows this tile adds into
         // go to L2 now, so the epilogue's reduce-add a tile later does not
         // wait for DRAM (0.54 -> 0.51 ms for a video block's two
         // out-projections).  With long main loops the reduce has time to
         // spare and the prefetch only slowed the GEMM (FFN2 +3 %).
         if (P.ep[p].kind == EPI_RESID && P.ep[p].tma && k_blocks <= 32)
-          tma_prefetch_l2_2d(&P.maps[p].m[1], nb * BN, mb * C::BM);
+          tma_prefetch_l2_2d(&P.maps[p].m[1], nb * BN, a_row);
         for (int kb = 0; kb < k_blocks; ++kb) {
           ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, err, 11);
           if (!ok) break;
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(sa, tmA, &full[stage], kb * C::BK, mb * C::BM);
-          tma_load_2d_hint(sa + C::A_BYTES, tmB, &full[stage], kb * C::BK, nb * BN, w_policy);
+          if constexpr (PAIR) {
+            // the leader's arrival brings the bytes of both CTAs' loads
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+            const uint32_t fb = full_leader + stage * (uint32_t)sizeof(uint64_t);
+            tma_load_2d_pair(sa, tmA, fb, kb * C::BK, a_row);
+            tma_load_2d_pair_hint(sa + C::A_BYTES, tmB, fb, kb * C::BK, b_row, w_policy);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+            tma_load_2d(sa, tmA, &full[stage], kb * C::BK, a_row);
+            tma_load_2d_hint(sa + C::A_BYTES, tmB, &full[stage], kb * C::BK, b_row, w_policy);
+          }
           ++issued[stage];
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
+        if (!ok) abort_pair();
       }
       if (!ok) {
         // wind down: let every copy this thread started land before the CTA exits
         volatile int no_abort = 0;
-        for (int s = 0; s < C::STAGES; ++s)
-          if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1), &no_abort, nullptr, 0);
+        if (leader) {
+          for (int s = 0; s < C::STAGES; ++s)
+            if (issued[s] > 0) mbar_wait(&full[s], (uint32_t)((issued[s] - 1) & 1), &no_abort, nullptr, 0);
+        } else {
+          // the peer's loads complete on the leader's barriers, whose phases
+          // need the leader's arrivals as well: give them a fixed time to land
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 200000ull) {
+          }
+        }
       }
     }
     __syncwarp();
@@ -298,12 +358,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ------------------------------------------------ MMA issuer (one thread)
     // The whole role runs on lane 0: a warp that diverges and reconverges
     // around every MMA burst costs the tensor pipe a large share of its rate.
-    if (lane == 0) {
+    // In a pair only the leader's issues.
+    if (lane == 0 && leader) {
       uint32_t stage = 0, phase = 0, local = 0;
       bool ok = true;
       const uint64_t a_desc = umma_desc_sw128(smem_u32(smem), 16, 1024);
       const uint64_t b_desc = umma_desc_sw128(smem_u32(smem) + C::A_BYTES, 16, 1024);
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+      for (int tile = first; ok && tile < num_tiles; tile += stride, ++local) {
         const uint32_t acc = local & 1, aphase = (local >> 1) & 1;
         ok = mbar_wait(&tempty[acc], aphase ^ 1, abort_flag, err, 12);
         if (!ok) break;
@@ -317,22 +378,38 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const uint64_t bd = umma_desc_add(b_desc, stage * C::STAGE_BYTES);
 #pragma unroll
           for (int k = 0; k < C::BK / C::K_PER_MMA; ++k) {
-            if constexpr (F8)
-              umma_ss_f8(d_tmem, umma_desc_add(ad, k * 32), umma_desc_add(bd, k * 32), C::IDESC, (kb | k) != 0);
+            const uint64_t ak = umma_desc_add(ad, k * 32), bk = umma_desc_add(bd, k * 32);
+            const uint32_t accum = (kb | k) != 0;
+            if constexpr (PAIR && F8)
+              umma_ss_f8_pair(d_tmem, ak, bk, C::IDESC, accum);
+            else if constexpr (PAIR)
+              umma_ss_pair(d_tmem, ak, bk, C::IDESC, accum);
+            else if constexpr (F8)
+              umma_ss_f8(d_tmem, ak, bk, C::IDESC, accum);
             else
-              umma_ss(d_tmem, umma_desc_add(ad, k * 32), umma_desc_add(bd, k * 32), C::IDESC, (kb | k) != 0);
+              umma_ss(d_tmem, ak, bk, C::IDESC, accum);
           }
-          umma_commit(&empty[stage]);
+          if constexpr (PAIR)
+            umma_commit_pair(&empty[stage], 0x3);
+          else
+            umma_commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
+        if constexpr (PAIR)
+          umma_commit_pair(&tfull[acc], 0x3);
+        else
+          umma_commit(&tfull[acc]);
       }
+      if (!ok) abort_pair();
       // all MMAs issued by this thread complete before TMEM is released
-      umma_commit(drain);
+      if constexpr (PAIR)
+        umma_commit_pair(drain, 0x1);
+      else
+        umma_commit(drain);
       volatile int no_abort = 0;
       mbar_wait(drain, 0, &no_abort, nullptr, 0);
     }
@@ -343,9 +420,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int half = (warp - 2) / 4;
     const int row_in_tile = q * 32 + lane;
     uint8_t* stg = smem + C::STG_OFF + (warp - 2) * C::STG_BYTES;
+    const uint32_t tempty_leader = PAIR ? cluster_map(tempty, 0) : 0;
     uint32_t local = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    for (int tile = first; tile < num_tiles; tile += stride, ++local) {
       const uint32_t acc = local & 1, aphase = (local >> 1) & 1;
       ok = mbar_wait_warp(&tfull[acc], aphase, abort_flag, err, 14);
       if (!ok) break;
@@ -355,16 +433,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tile_coords(t, P.m_tiles[p], n_tiles, P.group_n, &mb, &nb);
       const EpiParams& ep = P.ep[p];
       const int64_t M = P.M[p];
+      const int64_t tile_row0 = PAIR ? (int64_t)(2 * mb + (int)rank) * C::BM : (int64_t)mb * C::BM;
       const uint32_t tacc = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
-      if (ep.tma) {
-        const int64_t row0 = (int64_t)mb * C::BM + q * 32;
-        if (ep.kind == EPI_F32 || ep.kind == EPI_RESID)
-          drain_tile_tma<BN, 32>(ep, P.maps[p], tacc, row0, M, N, nb, half, stg, &tempty[acc], err);
+      // this warp is done with accumulator `acc` (tensor-memory reads complete)
+      auto release = [&]() {
+        if constexpr (PAIR)
+          mbar_arrive_cluster(tempty_leader + acc * (uint32_t)sizeof(uint64_t));
         else
-          drain_tile_tma<BN, 64>(ep, P.maps[p], tacc, row0, M, N, nb, half, stg, &tempty[acc], err);
+          mbar_arrive(&tempty[acc]);
+      };
+      if (ep.tma) {
+        const int64_t row0 = tile_row0 + q * 32;
+        if (ep.kind == EPI_F32 || ep.kind == EPI_RESID)
+          drain_tile_tma<BN, 32>(ep, P.maps[p], tacc, row0, M, N, nb, half, stg, release, err);
+        else
+          drain_tile_tma<BN, 64>(ep, P.maps[p], tacc, row0, M, N, nb, half, stg, release, err);
         continue;
       }
-      const int64_t row = (int64_t)mb * C::BM + row_in_tile;
+      const int64_t row = tile_row0 + row_in_tile;
 #pragma unroll 1
       for (int c = half; c < BN / 32; c += 2) {
         uint32_t r[32];
@@ -380,17 +466,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) release();
     }
+    if (!ok && lane == 0) abort_pair();
     // every TMA store of this warp has read its staging buffer and landed
     if (lane == 0) bulk_wait0();
     __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
+  // A pair frees its tensor memory together, once the leader's MMAs have all
+  // completed (its MMA thread waited on `drain`) and neither CTA has remote
+  // arrivals or copies left to make into the other.
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -439,9 +533,27 @@ static bool make_epi_maps(const EpiParams& e, int64_t M, int N, EpiMaps* maps) {
   return false;
 }
 
-template <int BN, int NP, bool F8>
+// Clusters of two GEMM CTAs that fit on the device at once (per device,
+// queried at the first pair launch).  A persistent pair launch never asks for
+// more: a cluster that had to wait for a slot would run its whole tile list
+// after the others.
+static int pair_clusters(const void* kernel, cudaLaunchConfig_t cfg, int num_sms) {
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
+    cached[dev] = n < num_sms / 2 ? n : num_sms / 2;
+  }
+  return cached[dev];
+}
+
+template <int BN, int NP, bool F8, bool PAIR>
 static cudaError_t launch_gemm_tc(const GemmArgs* gs, int* err, int num_sms, cudaStream_t s) {
-  using C = TcGemmCfg<BN, F8>;
+  using C = TcGemmCfg<BN, F8, PAIR>;
+  constexpr int TILE_M = PAIR ? 2 * C::BM : C::BM;
   GemmBatch<NP> P{};
   const int n_tiles = (gs[0].N + BN - 1) / BN;
   int tiles = 0;
@@ -453,13 +565,13 @@ static cudaError_t launch_gemm_tc(const GemmArgs* gs, int* err, int num_sms, cud
       const uint64_t da[2] = {(uint64_t)g.K, (uint64_t)g.M}, sa[1] = {(uint64_t)g.lda * C::ESZ};
       const uint32_t ba[2] = {(uint32_t)C::BK, 128};
       const uint64_t db[2] = {(uint64_t)g.K, (uint64_t)g.N}, sb[1] = {(uint64_t)g.K * C::ESZ};
-      const uint32_t bb[2] = {(uint32_t)C::BK, (uint32_t)BN};
+      const uint32_t bb[2] = {(uint32_t)C::BK, (uint32_t)C::BN_CTA};
       const CUtensorMapDataType dt = F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
       if (!make_tmap(&P.tmA[p], dt, g.A, 2, da, sa, ba) || !make_tmap(&P.tmB[p], dt, g.W, 2, db, sb, bb))
         return cudaErrorInvalidValue;
       P.ep[p].tma = make_epi_maps(P.ep[p], g.M, g.N, &P.maps[p]) ? 1 : 0;
     }
-    P.m_tiles[p] = (int)((g.M + C::BM - 1) / C::BM);
+    P.m_tiles[p] = (int)((g.M + TILE_M - 1) / TILE_M);
     tiles += P.m_tiles[p] * n_tiles;
     P.tile_end[p] = tiles;
   }
@@ -476,11 +588,32 @@ static cudaError_t launch_gemm_tc(const GemmArgs* gs, int* err, int num_sms, cud
   P.group_n = (int)(gn < n_tiles ? gn : n_tiles);
   if (tiles == 0) return cudaSuccess;
   static SmemAttr attr;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(gemm_tc_kernel<BN, NP, F8>), C::SMEM_BYTES, attr);
+  const void* kernel = reinterpret_cast<const void*>(gemm_tc_kernel<BN, NP, F8, PAIR>);
+  cudaError_t e = ensure_smem_attr(kernel, C::SMEM_BYTES, attr);
   if (e != cudaSuccess) return e;
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  gemm_tc_kernel<BN, NP, F8><<<grid, GEMM_THREADS, C::SMEM_BYTES, s>>>(P, gs[0].N, gs[0].K, err);
-  return cudaGetLastError();
+  if constexpr (PAIR) {
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    const int max_clusters = pair_clusters(kernel, cfg, num_sms);
+    if (max_clusters <= 0) return cudaErrorInvalidConfiguration;
+    const int clusters = tiles < max_clusters ? tiles : max_clusters;
+    cfg.gridDim = dim3(2 * clusters);
+    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, NP, F8, true>, P, gs[0].N, gs[0].K, err);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  } else {
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    gemm_tc_kernel<BN, NP, F8, false><<<grid, GEMM_THREADS, C::SMEM_BYTES, s>>>(P, gs[0].N, gs[0].K, err);
+    return cudaGetLastError();
+  }
 }
 
 // alignment rules of the operand tensor maps: 16-byte rows and bases
@@ -490,12 +623,21 @@ static bool operands_ok(const GemmArgs& g, int esz) {
            (reinterpret_cast<uintptr_t>(g.W) & 15));
 }
 
+// Widths that are multiples of 256 run on CTA pairs (256 x 256 tiles) unless
+// pairs are switched off (dit_debug_gemm_cta_pairs); the others on single
+// CTAs with 128 x 128 or 128 x 64 tiles.
+static int g_cta_pairs = 1;
+void set_gemm_cta_pairs(int on) { g_cta_pairs = on ? 1 : 0; }
+
 template <int NP, bool F8>
 static cudaError_t launch_by_width(const GemmArgs* gs, int* err, int num_sms, cudaStream_t s) {
   const int N = gs[0].N;
-  if (N % 256 == 0) return launch_gemm_tc<256, NP, F8>(gs, err, num_sms, s);
-  if (N % 128 == 0) return launch_gemm_tc<128, NP, F8>(gs, err, num_sms, s);
-  return launch_gemm_tc<64, NP, F8>(gs, err, num_sms, s);
+  if (N % 256 == 0) {
+    if (g_cta_pairs && num_sms >= 2) return launch_gemm_tc<256, NP, F8, true>(gs, err, num_sms, s);
+    return launch_gemm_tc<256, NP, F8, false>(gs, err, num_sms, s);
+  }
+  if (N % 128 == 0) return launch_gemm_tc<128, NP, F8, false>(gs, err, num_sms, s);
+  return launch_gemm_tc<64, NP, F8, false>(gs, err, num_sms, s);
 }
 
 template <bool F8>
@@ -535,5 +677,6 @@ cudaError_t gemm_e4m3_tc_pair(const GemmArgs& g0, const GemmArgs& g1, int* err, 
 }  // namespace dit
 
 static_assert(dit::TcGemmCfg<256>::SMEM_BYTES <= 232448 && dit::TcGemmCfg<128>::SMEM_BYTES <= 232448 &&
-                  dit::TcGemmCfg<64>::SMEM_BYTES <= 232448,
+                  dit::TcGemmCfg<64>::SMEM_BYTES <= 232448 && dit::TcGemmCfg<256, false, true>::SMEM_BYTES <= 232448 &&
+                  dit::TcGemmCfg<256, true, true>::SMEM_BYTES <= 232448,
               "GEMM tile set exceeds 227 KB of shared memory");

@@ -29,7 +29,7 @@ LOOP_CUDA_GRAPH = 2
 EXPORTS = ["dit_create", "dit_load_weights", "dit_num_params", "dit_param_info", "dit_timestep_modulation",
            "dit_patch_embed", "dit_block_forward", "dit_final_layer", "cfg_combine", "flow_euler_step",
            "dit_denoise_loop", "dit_synchronize", "dit_device_bytes", "dit_destroy", "dit_status_string",
-           "dit_last_error", "dit_debug_fail_alloc_after", "dit_debug_stall", "dit_profile_start", "dit_profile_stop",
+           "dit_last_error", "dit_debug_fail_alloc_after", "dit_debug_gemm_cta_pairs", "dit_debug_stall", "dit_profile_start", "dit_profile_stop",
            "dit_timestep_modulation_noalloc"]
 NOALLOC_MAX_BATCH, NOALLOC_MAX_HIDDEN = 64, 262144
 
@@ -90,6 +90,7 @@ def lib():
         "dit_status_string": ([C.c_int], C.c_char_p),
         "dit_last_error": ([], C.c_char_p),
         "dit_debug_fail_alloc_after": ([C.c_int], None),
+        "dit_debug_gemm_cta_pairs": ([C.c_int], None),
         "dit_debug_stall": ([vp, vp], C.c_int),
         "dit_profile_start": ([vp, C.c_int], C.c_int),
         "dit_profile_stop": ([vp, C.POINTER(i64), C.POINTER(C.c_double)], C.c_int),
@@ -166,6 +167,10 @@ def flow_euler_step(x, v, sigma: float, sigma_next: float, n: int, stream=None):
 
 def dit_debug_fail_alloc_after(n: int):
     lib().dit_debug_fail_alloc_after(n)
+
+
+def dit_debug_gemm_cta_pairs(enable: bool):
+    lib().dit_debug_gemm_cta_pairs(1 if enable else 0)
 
 
 class DiT:

@@ -301,6 +301,14 @@ const char* dit_last_error(void);
  * DIT_ERR_OOM (0 disables).  Host-side only; used to test failure paths. */
 void dit_debug_fail_alloc_after(int n);
 
+/* Test hook: 1 (the default) runs every GEMM whose output width is a
+ * multiple of 256 on clusters of two CTAs that share one tcgen05.mma of
+ * 256 x 256 (cta_group::2); 0 runs those GEMMs on single CTAs with
+ * 128 x 256 tiles.  Process-wide; takes effect at the next launch (a CUDA
+ * graph captured before keeps the kernels it captured).  Used to compare
+ * the two paths. */
+void dit_debug_gemm_cta_pairs(int enable);
+
 /* Test hook for the device-side failure path.  Enqueues on `stream` a kernel
  * whose bounded wait on a barrier that nothing ever arrives on gives up after
  * the library's wait limit (1.5 s) and records DIT_DEBUG_STALL_SITE in the

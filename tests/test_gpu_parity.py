@@ -582,3 +582,37 @@ def test_two_models_on_unordered_streams_are_isolated():
         assert np.array_equal(a, host(x))
     for m, *_ in cases:
         m.close()
+
+
+# ------------------------------------------------------------------ GEMM CTA pairs
+@pytest.mark.parametrize("prec", [synth.PREC_BF16, synth.PREC_FP8])
+def test_gemm_cta_pairs_match_single_ctas(prec):
+    """GEMMs of width a multiple of 256 run on CTA pairs (one cta_group::2 MMA
+    of 256 x 256 per K step, each CTA holding half of the W tile); with pairs
+    switched off they run on single CTAs (128 x 256).  Each output element is
+    the same fp32 sum over the same K steps either way, so a block (QKV,
+    out-projections, cross-K/V, FFN2 on pairs; 390 tokens x 2 = 7 row blocks,
+    so the last pair's second CTA reads rows past M) gives the same bits."""
+    cfg = small_bf16_cfg(synth.COND_CROSS, precision=prec, depth=1)
+    W = synth.make_weights(cfg, seed=19)
+    grid, L = (3, 10, 13), 5
+    N = int(np.prod(grid))
+    rng = np.random.default_rng(5)
+    x0 = (rng.standard_normal((2, N, cfg["hidden"])) * 0.5).astype(np.float32)
+    ctx = synth.make_cond(cfg, batch=2, seed=6, length=L)
+    mods = np.stack([O.timestep_modulation(t, W, cfg) for t in (250.0, 850.0)])
+    out = {}
+    try:
+        for pairs in (True, False):
+            dit.dit_debug_gemm_cta_pairs(pairs)
+            m = make_model(cfg, W)
+            x = dev(x0)
+            m.dit_block_forward(0, x, None, dev(mods), dev(ctx), 2, grid, L)
+            m.dit_synchronize()
+            out[pairs] = host(x)
+            m.close()
+    finally:
+        dit.dit_debug_gemm_cta_pairs(True)
+    diff = float(np.max(np.abs(out[True] - out[False])))
+    print(f"[gpu] cta pairs vs single, precision {prec}: max |diff| {diff:.3e}")
+    assert np.array_equal(out[True], out[False]), diff
