@@ -715,13 +715,13 @@ def main():
     ap.add_argument("--case", default="step", choices=["step", "block", "sweep"],
                     help="block: one DiT block repeatedly (small case for kernel profiling); "
                          "sweep: image block batch/sequence sweep")
-    ap.add_argument("--gemm-cta-pairs", type=int, default=1, choices=[0, 1],
-                    help="1: GEMMs of width a multiple of 256 on CTA pairs (cta_group::2, 256 x 256 tiles); "
-                         "0: on single CTAs (128 x 256)")
+    ap.add_argument("--gemm-cta-pairs", type=int, default=1, choices=[0, 1, 2],
+                    help="GEMMs of width a multiple of 256 on CTA pairs (cta_group::2, 256 x 256 tiles): "
+                         "0 never (single CTAs, 128 x 256), 1 when the main loop has >= 16 K blocks, 2 always")
     args = ap.parse_args()
-    if args.impl != "reference" and args.gemm_cta_pairs == 0:
+    if args.impl != "reference" and args.gemm_cta_pairs != 1:
         from diffusion_transformer_denoising_gb300 import dit
-        dit.dit_debug_gemm_cta_pairs(False)
+        dit.dit_debug_gemm_cta_pairs(args.gemm_cta_pairs)
     if args.case == "block":
         run_block_case(args)
     elif args.case == "sweep":

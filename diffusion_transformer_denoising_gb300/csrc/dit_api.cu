@@ -258,7 +258,7 @@ extern "C" dit_status dit_param_info(const dit_config* cfg, int i, char* name_bu
 }
 
 extern "C" void dit_debug_fail_alloc_after(int n) { g_fail_alloc_after = n; }
-extern "C" void dit_debug_gemm_cta_pairs(int enable) { dit::set_gemm_cta_pairs(enable); }
+extern "C" void dit_debug_gemm_cta_pairs(int mode) { dit::set_gemm_cta_pairs(mode); }
 
 extern "C" const char* dit_status_string(dit_status s) {
   switch (s) {

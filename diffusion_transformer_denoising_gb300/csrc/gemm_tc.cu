@@ -22,7 +22,8 @@
 // SM walks the tile list with stride gridDim.x; tiles are ordered N-fastest so
 // CTAs running together share the same A rows through L2.
 //
-// Widths that are multiples of 256 run on CTA pairs (clusters of two): a
+// Widths that are multiples of 256 with main loops of 16 K blocks or more
+// run on CTA pairs (clusters of two): a
 // 256 x 256 tile per pair, one tcgen05.mma.cta_group::2 (M = 256) per K step
 // issued by the leader CTA, each CTA loading its own 128 rows of A and 128 of
 // the tile's 256 W rows.  The L2 then serves 32 KB per CTA and K block
@@ -623,17 +624,25 @@ static bool operands_ok(const GemmArgs& g, int esz) {
            (reinterpret_cast<uintptr_t>(g.W) & 15));
 }
 
-// Widths that are multiples of 256 run on CTA pairs (256 x 256 tiles) unless
-// pairs are switched off (dit_debug_gemm_cta_pairs); the others on single
-// CTAs with 128 x 128 or 128 x 64 tiles.
-static int g_cta_pairs = 1;
-void set_gemm_cta_pairs(int on) { g_cta_pairs = on ? 1 : 0; }
+// Widths that are multiples of 256 run on CTA pairs (256 x 256 tiles) when a
+// tile's main loop has at least kPairMinKBlocks K blocks; the others on single
+// CTAs with 128 x 256, 128 x 128 or 128 x 64 tiles.  A pair's MMA waits until
+// both CTAs' epilogues have drained the accumulator, so where the epilogue of
+// a tile outlasts the main loop of the next the pair runs at the pace of the
+// slower CTA: the video e4m3 projections (K = 1536: 12 K blocks) were 7-12 %
+// slower on pairs, every GEMM with 24 K blocks or more (bf16 video and image,
+// e4m3 image) 4-15 % faster.
+constexpr int kPairMinKBlocks = 16;
+static int g_cta_pairs = 1;  // 0 never, 1 by main-loop length, 2 always
+void set_gemm_cta_pairs(int mode) { g_cta_pairs = mode < 0 ? 0 : (mode > 2 ? 2 : mode); }
 
 template <int NP, bool F8>
 static cudaError_t launch_by_width(const GemmArgs* gs, int* err, int num_sms, cudaStream_t s) {
   const int N = gs[0].N;
   if (N % 256 == 0) {
-    if (g_cta_pairs && num_sms >= 2) return launch_gemm_tc<256, NP, F8, true>(gs, err, num_sms, s);
+    const int k_blocks = (gs[0].K + TcGemmCfg<256, F8>::BK - 1) / TcGemmCfg<256, F8>::BK;
+    const bool pair = g_cta_pairs == 2 || (g_cta_pairs == 1 && k_blocks >= kPairMinKBlocks);
+    if (pair && num_sms >= 2) return launch_gemm_tc<256, NP, F8, true>(gs, err, num_sms, s);
     return launch_gemm_tc<256, NP, F8, false>(gs, err, num_sms, s);
   }
   if (N % 128 == 0) return launch_gemm_tc<128, NP, F8, false>(gs, err, num_sms, s);

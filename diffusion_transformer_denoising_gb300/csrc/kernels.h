@@ -76,9 +76,10 @@ cudaError_t gemm_bf16_tc_pair(const GemmArgs& g0, const GemmArgs& g1, int* err, 
 // epi.a_scale / epi.w_scale.  Single and paired forms as above.
 cudaError_t gemm_e4m3_tc(const GemmArgs& g, int* err, int num_sms, cudaStream_t s);
 cudaError_t gemm_e4m3_tc_pair(const GemmArgs& g0, const GemmArgs& g1, int* err, int num_sms, cudaStream_t s);
-// 1 (default): GEMMs whose N is a multiple of 256 run on clusters of two CTAs
-// sharing cta_group::2 MMAs of 256 x 256 tiles; 0: on single CTAs (128 x 256).
-void set_gemm_cta_pairs(int on);
+// GEMMs whose N is a multiple of 256 on clusters of two CTAs sharing
+// cta_group::2 MMAs of 256 x 256 tiles: 0 never (single CTAs, 128 x 256),
+// 1 (default) when the main loop has at least 16 K blocks, 2 always.
+void set_gemm_cta_pairs(int mode);
 // Row-wise e4m3 quantization of a weight matrix: src [rows, K] (fp32 or bf16)
 // -> dst [rows, K] e4m3 bytes and scale[rows] = max|row| / 448 (1 for a zero
 // row), dst = src / scale rounded to nearest.

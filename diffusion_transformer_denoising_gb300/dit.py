@@ -169,8 +169,10 @@ def dit_debug_fail_alloc_after(n: int):
     lib().dit_debug_fail_alloc_after(n)
 
 
-def dit_debug_gemm_cta_pairs(enable: bool):
-    lib().dit_debug_gemm_cta_pairs(1 if enable else 0)
+def dit_debug_gemm_cta_pairs(mode: int):
+    """0: GEMMs never on CTA pairs, 1 (default): when the main loop has >= 16
+    K blocks, 2: always (widths that are multiples of 256)."""
+    lib().dit_debug_gemm_cta_pairs(int(mode))
 
 
 class DiT:

@@ -301,13 +301,15 @@ const char* dit_last_error(void);
  * DIT_ERR_OOM (0 disables).  Host-side only; used to test failure paths. */
 void dit_debug_fail_alloc_after(int n);
 
-/* Test hook: 1 (the default) runs every GEMM whose output width is a
- * multiple of 256 on clusters of two CTAs that share one tcgen05.mma of
- * 256 x 256 (cta_group::2); 0 runs those GEMMs on single CTAs with
- * 128 x 256 tiles.  Process-wide; takes effect at the next launch (a CUDA
- * graph captured before keeps the kernels it captured).  Used to compare
- * the two paths. */
-void dit_debug_gemm_cta_pairs(int enable);
+/* Test hook: where GEMMs whose output width is a multiple of 256 run on
+ * clusters of two CTAs that share one tcgen05.mma of 256 x 256
+ * (cta_group::2) instead of single CTAs with 128 x 256 tiles.  mode 1 (the
+ * default): when the GEMM's main loop has at least 16 K blocks (K >= 1024 in
+ * bf16, K >= 2048 in e4m3); 0: never; 2: always.  Other values are clamped
+ * to 0..2.  Process-wide; takes effect at the next launch (a CUDA graph
+ * captured before keeps the kernels it captured).  Both paths give the same
+ * bits; the hook exists to compare them. */
+void dit_debug_gemm_cta_pairs(int mode);
 
 /* Test hook for the device-side failure path.  Enqueues on `stream` a kernel
  * whose bounded wait on a barrier that nothing ever arrives on gives up after

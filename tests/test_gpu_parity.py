@@ -585,17 +585,20 @@ def test_two_models_on_unordered_streams_are_isolated():
 
 
 # ------------------------------------------------------------------ GEMM CTA pairs
-@pytest.mark.parametrize("prec", [synth.PREC_BF16, synth.PREC_FP8])
-def test_gemm_cta_pairs_match_single_ctas(prec):
-    """GEMMs of width a multiple of 256 run on CTA pairs (one cta_group::2 MMA
-    of 256 x 256 per K step, each CTA holding half of the W tile); with pairs
-    switched off they run on single CTAs (128 x 256).  Each output element is
-    the same fp32 sum over the same K steps either way, so a block (QKV,
-    out-projections, cross-K/V, FFN2 on pairs; 390 tokens x 2 = 7 row blocks,
-    so the last pair's second CTA reads rows past M) gives the same bits."""
-    cfg = small_bf16_cfg(synth.COND_CROSS, precision=prec, depth=1)
+@pytest.mark.parametrize("prec,mode", [(synth.PREC_BF16, synth.COND_CROSS), (synth.PREC_FP8, synth.COND_CROSS),
+                                       (synth.PREC_BF16, synth.COND_JOINT)])
+def test_gemm_cta_pairs_match_single_ctas(prec, mode):
+    """GEMMs of width a multiple of 256 can run on CTA pairs (one cta_group::2
+    MMA of 256 x 256 per K step, each CTA holding half of the W tile) or on
+    single CTAs (128 x 256).  Each output element is the same fp32 sum over
+    the same K steps either way, so a block with pairs forced on (QKV,
+    out-projections, cross-K/V, FFN2; in the joint block the two streams'
+    problems share each launch) gives the same bits as with pairs off.  390
+    (or 400) tokens x 2 = 7 row blocks: the last pair's second CTA reads rows
+    past M; 5 condition rows: the whole second CTA does."""
+    cfg = small_bf16_cfg(mode, precision=prec, depth=1)
     W = synth.make_weights(cfg, seed=19)
-    grid, L = (3, 10, 13), 5
+    grid, L = ((3, 10, 13) if mode == synth.COND_CROSS else (1, 20, 20)), 5
     N = int(np.prod(grid))
     rng = np.random.default_rng(5)
     x0 = (rng.standard_normal((2, N, cfg["hidden"])) * 0.5).astype(np.float32)
@@ -603,16 +606,23 @@ def test_gemm_cta_pairs_match_single_ctas(prec):
     mods = np.stack([O.timestep_modulation(t, W, cfg) for t in (250.0, 850.0)])
     out = {}
     try:
-        for pairs in (True, False):
+        for pairs in (2, 0):
             dit.dit_debug_gemm_cta_pairs(pairs)
             m = make_model(cfg, W)
             x = dev(x0)
-            m.dit_block_forward(0, x, None, dev(mods), dev(ctx), 2, grid, L)
-            m.dit_synchronize()
-            out[pairs] = host(x)
+            if mode == synth.COND_CROSS:
+                m.dit_block_forward(0, x, None, dev(mods), dev(ctx), 2, grid, L)
+                m.dit_synchronize()
+                out[pairs] = host(x)
+            else:
+                xc = dev(ctx)
+                m.dit_block_forward(0, x, xc, dev(mods), None, 2, grid, L)
+                m.dit_synchronize()
+                out[pairs] = np.concatenate([host(x).ravel(), host(xc).ravel()])
             m.close()
     finally:
-        dit.dit_debug_gemm_cta_pairs(True)
-    diff = float(np.max(np.abs(out[True] - out[False])))
-    print(f"[gpu] cta pairs vs single, precision {prec}: max |diff| {diff:.3e}")
-    assert np.array_equal(out[True], out[False]), diff
+        dit.dit_debug_gemm_cta_pairs(1)
+    diff = float(np.max(np.abs(out[2] - out[0])))
+    print(f"[gpu] cta pairs vs single, precision {prec} mode {mode}: max |diff| {diff:.3e}")
+    assert np.isfinite(out[2]).all()
+    assert np.array_equal(out[2], out[0]), diff
