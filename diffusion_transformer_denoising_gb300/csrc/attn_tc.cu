@@ -48,7 +48,9 @@
 // so every ring runs on across item boundaries; the K loader refills the Q
 // buffer once the previous item's last S product has completed, and the
 // first PV product of an item (which overwrites O) waits until the softmax
-// warps have read out the previous item's O (o_free).
+// warps have read out the previous item's O (o_free).  Persistent CTAs write
+// the output through shared memory and TMA tensor stores (three V stages
+// instead of four make the room); one CTA per item stores per lane, once.
 //
 // Per-tile integer work on the softmax path is kept to compares and adds
 // (the ring slots and the rotated key tile advance incrementally): a
@@ -72,20 +74,34 @@ constexpr int KST = 2, VST = 4, SR = 3, PR = 4;
 constexpr int TILE_BYTES = 128 * HD * 2;   // 32 KB: two 16 KB swizzle blocks of 64 channels
 constexpr int Q_OFF = 0;
 constexpr int K_OFF = Q_OFF + TILE_BYTES;
-constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
-constexpr int BAR_OFF = V_OFF + VST * TILE_BYTES;
-// Exchange area: bf16 row maxima [2 parities][NQ][128]; after the loop float
-// row sums [NQ][128] over them.
-constexpr int XCH_OFF = BAR_OFF + 256;
+
+// Exchange areas (after the barriers, see Layout): bf16 row maxima
+// [2 parities][NQ][128] and, apart from them, the float row sums [NQ][128] an
+// item's epilogue combines (a partner warp that has moved on to the next
+// item's first tile may already be writing maxima).
 // The tiles need 1024-byte alignment.  The dynamic shared window of a kernel
 // without static shared memory starts 1024-aligned (checked at entry), so no
 // alignment slack is reserved and the total stays under 227 KB.
 constexpr int SM_WARPS = 8;                       // softmax warps
 constexpr int NQ = SM_WARPS / 4;                  // warps per TMEM lane quadrant
 constexpr int KPW = BKV / NQ;                     // key columns per softmax warp
-constexpr int SMEM_BYTES = XCH_OFF + 2 * NQ * BQ * 2;
+// Persistent CTAs (many short items) write each item's output through
+// shared memory and TMA: every softmax warp stages its 32 rows x 64 channels
+// (4 KB, 128-byte swizzle) and issues one tensor store.  The staging area
+// takes the place of one V stage.  (Per-lane 16-byte stores of 32 different
+// rows cost ~3700 cycles per item, half the time of a 4-tile item.)
+template <bool PERSIST>
+struct Layout {
+  static constexpr int VSTAGES = PERSIST ? 3 : VST;
+  static constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
+  static constexpr int STG_OFF = V_OFF + VSTAGES * TILE_BYTES;  // [SM_WARPS][32 rows][128 B] (persistent)
+  static constexpr int STG_BYTES = PERSIST ? SM_WARPS * 32 * 128 : 0;
+  static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
+  static constexpr int XCH_OFF = BAR_OFF + 256;
+  static constexpr int XSUM_OFF = XCH_OFF + 2 * NQ * BQ * 2;
+  static constexpr int SMEM_BYTES = XSUM_OFF + NQ * BQ * 4;
+};
 static_assert(SR >= KST && PR >= VST && VST <= 4, "completion rings shorter than the stage rings");
-static_assert(NQ * BQ * 4 <= 2 * NQ * BQ * 2, "row sums must fit the exchange area");
 constexpr int NUM_THREADS = 32 * (SM_WARPS + 4);  // + K/Q loader, S-MMA, PV-MMA, V loader warps
 constexpr int TMA_WARP = SM_WARPS, S_WARP = SM_WARPS + 1, PV_WARP = SM_WARPS + 2, VTMA_WARP = SM_WARPS + 3;
 constexpr uint32_t TM_S = 0, TM_P = 256, TM_O = 384;
@@ -140,17 +156,26 @@ DIT_DEV float exp_tile(const float (&s)[NV], uint32_t (&pk)[NV / 2], float scale
 }
 }  // namespace fa
 
+// tmO[0] / tmO[1]: the outputs o1 / o2 as [B][rows][H*128] in boxes of
+// 64 channels x 32 rows, used when bit 0 / bit 1 of o_tma is set (persistent
+// mode only).
+struct AttnOutMaps {
+  CUtensorMap m[2];
+};
+
 template <bool PERSIST>
 __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, AttnArgs a, float scale_log2, int* err) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ AttnOutMaps tmO, int o_tma,
+                   AttnArgs a, float scale_log2, int* err) {
   using namespace fa;
+  using Lay = Layout<PERSIST>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023) {  // uniform across the CTA: nothing has started yet
     if (threadIdx.x == 0) atomicCAS(err, 0, 20);
     return;
   }
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::BAR_OFF);
   uint64_t* q_full = bars;         // Q tile
   uint64_t* kf = bars + 1;              // [KST] K stage loaded
   uint64_t* vf = kf + KST;              // [VST] V stage loaded
@@ -163,8 +188,8 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   uint64_t* o_free = tile_ready + SR;   // O of an item read out (one arrival per softmax warp)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  __nv_bfloat16* xmax = reinterpret_cast<__nv_bfloat16*>(smem + XCH_OFF);
-  float* xsum = reinterpret_cast<float*>(smem + XCH_OFF);
+  __nv_bfloat16* xmax = reinterpret_cast<__nv_bfloat16*>(smem + Lay::XCH_OFF);
+  float* xsum = reinterpret_cast<float*>(smem + Lay::XSUM_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = (a.Lq + BQ - 1) / BQ;
@@ -238,8 +263,8 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       const CUtensorMap* tm = is_k ? &tmK : &tmV;
       uint64_t* full = is_k ? kf : vf;
       uint64_t* consumed = is_k ? s_done : pv_done;
-      const int nst = is_k ? KST : VST, ring = is_k ? SR : PR;
-      uint8_t* stages = smem + (is_k ? K_OFF : V_OFF);
+      const int nst = is_k ? KST : Lay::VSTAGES, ring = is_k ? SR : PR;
+      uint8_t* stages = smem + (is_k ? K_OFF : Lay::V_OFF);
       int issued[4] = {0, 0, 0, 0};
       int q_issued = 0;
       bool ok = true;
@@ -322,19 +347,19 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   } else if (warp == PV_WARP) {
     // ------------------------------------------------ O += P V issuer (one thread)
     if (lane == 0) {
-      const uint64_t v_desc = umma_desc_sw128(smem_u32(smem + V_OFF), 16384, 1024);
+      const uint64_t v_desc = umma_desc_sw128(smem_u32(smem + Lay::V_OFF), 16384, 1024);
       bool ok = true;
       int G = 0;
       for (int k = 0; ok && k < my_items; ++k) {
         for (int j = 0; ok && j < nkv; ++j, ++G) {
           ok = mbar_wait(&p_ready[G & 1], (uint32_t)((G >> 1) & 1), abort_flag, err, 26) &&
-               mbar_wait(&vf[G % VST], (uint32_t)((G / VST) & 1), abort_flag, err, 27);
+               mbar_wait(&vf[G % Lay::VSTAGES], (uint32_t)((G / Lay::VSTAGES) & 1), abort_flag, err, 27);
           // the first product of an item overwrites O: the previous item's O
           // must have been read out
           if (PERSIST && j == 0 && k > 0) ok = ok && mbar_wait(o_free, (uint32_t)((k - 1) & 1), abort_flag, err, 28);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t vd = umma_desc_add(v_desc, (G % VST) * TILE_BYTES);
+          const uint64_t vd = umma_desc_add(v_desc, (G % Lay::VSTAGES) * TILE_BYTES);
           const uint32_t p_tmem = tmem + TM_P + (G & 1) * 64;
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk) {
@@ -478,7 +503,8 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     // O is final once PV_{nkv-1} has completed
     ok = ok && mbar_wait_warp(&pv_done[(G - 1) % PR], (uint32_t)(((G - 1) / PR) & 1), abort_flag, err, 34);
     // the quadrant's partial row sums (same reference max) go through the
-    // exchange buffer once every warp of the quadrant has read its maxima
+    // row-sum area once every warp of the quadrant has read the previous
+    // item's sums from it
     named_bar_sync(1 + q, 32 * NQ);
     xsum[h * BQ + row] = l;
     named_bar_sync(1 + q, 32 * NQ);
@@ -488,26 +514,70 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
 #pragma unroll
       for (int w = 0; w < NQ; ++w) lt += xsum[w * BQ + row];
       const float inv = 1.f / lt;
-      const int tok = item_qt(k) * BQ + row;
+      const int tok0 = item_qt(k) * BQ + q * 32;  // the warp's first row
+      const int tok = tok0 + lane;
       const int bh = item_bh(k), b = bh / a.H, head = bh - b * a.H;
       const int D = a.H * HD;
-      __nv_bfloat16* out = nullptr;
-      if (tok < a.Lq && DIT_BOUNDS(bh < a.B * a.H && tok >= 0, err, 63)) {
-        out = (tok < a.split)
-                  ? static_cast<__nv_bfloat16*>(a.o1) + ((int64_t)b * a.split + tok) * D
-                  : static_cast<__nv_bfloat16*>(a.o2) + ((int64_t)b * (a.Lq - a.split) + (tok - a.split)) * D;
-        out += head * HD + h * KPW;
+      // TMA path: the warp's 32 rows lie in one output (units across the
+      // split between o1 and o2 take the per-lane stores; rows past the last
+      // token are clipped by the tensor map)
+      int map = -1;
+      if constexpr (PERSIST) {
+        if (tok0 + 32 <= a.split || a.split == a.Lq)
+          map = (o_tma & 1) ? 0 : -1;
+        else if (tok0 >= a.split)
+          map = (o_tma & 2) ? 1 : -1;
       }
+      if (map >= 0) {
+        if (tok0 < a.Lq && DIT_BOUNDS(bh < a.B * a.H && tok0 >= 0, err, 63)) {
+          uint8_t* stg = smem + Lay::STG_OFF + warp * (32 * 128);
+          // the staging buffer's previous tensor store has read it
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+          uint8_t* rowp = stg + lane * 128;
 #pragma unroll 1
-      for (int c = 0; c < KPW / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(o_col + c * 32, r);
-        tmem_ld_wait();
-        if (out) {
-          float v[32];
+          for (int c = 0; c < KPW / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(o_col + c * 32, r);
+            tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * inv;
-          store_chunk<__nv_bfloat16, 32>(out + c * 32, v);
+            for (int j = 0; j < 4; ++j) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]) * inv, __uint_as_float(r[8 * j + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]) * inv, __uint_as_float(r[8 * j + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]) * inv, __uint_as_float(r[8 * j + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]) * inv, __uint_as_float(r[8 * j + 7]) * inv);
+              // 128-byte swizzle: 16-byte chunk n of row r sits at chunk n ^ (r % 8)
+              *reinterpret_cast<uint4*>(rowp + (((c * 4 + j) ^ (lane & 7)) << 4)) = w;
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            // rows past the end of the output are clipped by the tensor map
+            tma_store_3d(&tmO.m[map], stg, head * HD + h * KPW, map == 0 ? tok0 : tok0 - a.split, b);
+            bulk_commit();
+          }
+        }
+      } else {
+        __nv_bfloat16* out = nullptr;
+        if (tok < a.Lq && DIT_BOUNDS(bh < a.B * a.H && tok >= 0, err, 63)) {
+          out = (tok < a.split)
+                    ? static_cast<__nv_bfloat16*>(a.o1) + ((int64_t)b * a.split + tok) * D
+                    : static_cast<__nv_bfloat16*>(a.o2) + ((int64_t)b * (a.Lq - a.split) + (tok - a.split)) * D;
+          out += head * HD + h * KPW;
+        }
+#pragma unroll 1
+        for (int c = 0; c < KPW / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_col + c * 32, r);
+          tmem_ld_wait();
+          if (out) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * inv;
+            store_chunk<__nv_bfloat16, 32>(out + c * 32, v);
+          }
         }
       }
     }
@@ -518,6 +588,9 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(o_free);
     }
     }
+    // every tensor store of this warp has landed before the CTA exits
+    if (PERSIST && lane == 0) bulk_wait0();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -541,9 +614,10 @@ cudaError_t attention_bf16_tc(const AttnArgs& a, int* err, cudaStream_t s) {
       !make_tmap_bf16(&tv, a.v, 3, dk, sk, box))
     return cudaErrorInvalidValue;
   static SmemAttr attr_one, attr_persist;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(attn_tc_kernel<false>), SMEM_BYTES, attr_one);
+  cudaError_t e =
+      ensure_smem_attr(reinterpret_cast<const void*>(attn_tc_kernel<false>), Layout<false>::SMEM_BYTES, attr_one);
   if (e == cudaSuccess)
-    e = ensure_smem_attr(reinterpret_cast<const void*>(attn_tc_kernel<true>), SMEM_BYTES, attr_persist);
+    e = ensure_smem_attr(reinterpret_cast<const void*>(attn_tc_kernel<true>), Layout<true>::SMEM_BYTES, attr_persist);
   static int sms_of[kMaxDevices] = {};
   int dev = 0;
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
@@ -558,14 +632,32 @@ cudaError_t attention_bf16_tc(const AttnArgs& a, int* err, cudaStream_t s) {
     const int64_t items = (int64_t)a.B * a.H * nq;
     if (items > INT32_MAX) return cudaErrorInvalidValue;
     const int grid = (int)(items < num_sms ? items : num_sms);
-    attn_tc_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tq, tk, tv, a, scale_log2, err);
+    // output tensor maps [B][rows][H*128]: o1 holds tokens [0, split), o2 the rest
+    AttnOutMaps om{};
+    int o_tma = 0;
+    const uint32_t obox[3] = {64, 32, 1};
+    auto omap = [&](CUtensorMap* t, void* base, int rows) -> bool {
+      if (!base || rows <= 0 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+      const uint64_t d[3] = {(uint64_t)a.H * HD, (uint64_t)rows, (uint64_t)a.B};
+      const uint64_t st[2] = {(uint64_t)a.H * HD * 2, (uint64_t)rows * a.H * HD * 2};
+      return make_tmap_bf16(t, base, 3, d, st, obox);
+    };
+    if (omap(&om.m[0], a.o1, a.split)) o_tma |= 1;
+    if (omap(&om.m[1], a.o2, a.Lq - a.split)) o_tma |= 2;
+    attn_tc_kernel<true><<<grid, NUM_THREADS, Layout<true>::SMEM_BYTES, s>>>(tq, tk, tv, om, o_tma, a, scale_log2,
+                                                                           err);
   } else {
     dim3 grid(nq, a.H, a.B);
-    attn_tc_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tq, tk, tv, a, scale_log2, err);
+    const AttnOutMaps none{};
+    attn_tc_kernel<false><<<grid, NUM_THREADS, Layout<false>::SMEM_BYTES, s>>>(tq, tk, tv, none, 0, a, scale_log2,
+                                                                             err);
   }
   return cudaGetLastError();
 }
 
 }  // namespace dit
 
-static_assert(dit::fa::SMEM_BYTES <= 232448, "attention tile set exceeds 227 KB of shared memory");
+static_assert(dit::fa::Layout<false>::SMEM_BYTES <= 232448 && dit::fa::Layout<true>::SMEM_BYTES <= 232448,
+              "attention tile set exceeds 227 KB of shared memory");
+static_assert(dit::fa::PR >= dit::fa::Layout<true>::VSTAGES, "V completion ring shorter than the V stages");
+static_assert(dit::fa::Layout<true>::STG_OFF % 1024 == 0, "swizzled staging buffers need 1024-byte alignment");

@@ -4,8 +4,8 @@ boxes, attention items and key tiles, LayerNorm rows and modulation entries)
 and records the first failure in the model's error word instead of touching
 memory; dit_synchronize then reports it.  Run over the small odd shapes of
 the CPU comparisons (ragged token counts, a single token, short and
-single-token conditions, K and N tails, both conditioning modes, complete
-loops), every check must pass and every result must still match the oracle.  Runs in a child process because
+single-token conditions, K and N tails, both conditioning modes, GEMMs on
+single CTAs and on CTA pairs, complete loops), every check must pass and every result must still match the oracle.  Runs in a child process because
 the library a process loads is fixed at its first use."""
 import os
 import subprocess
@@ -36,13 +36,18 @@ def model(cfg, W):
     m.load_weights(W)
     return m
 
-# blocks: ragged grids, short conditions, K/N tails, both modes
-for mode, grid, L, kw in ((synth.COND_CROSS, (2, 9, 7), 5, {}), (synth.COND_CROSS, (3, 10, 13), 77, {}),
-                          (synth.COND_CROSS, (1, 6, 11), 37, dict(mlp=648, cond_dim=200)),
-                          (synth.COND_JOINT, (1, 7, 9), 33, {}), (synth.COND_JOINT, (1, 12, 20), 64, {}),
-                          (synth.COND_CROSS, (1, 1, 1), 1, {}), (synth.COND_JOINT, (1, 1, 1), 1, {}),
-                          (synth.COND_CROSS, (3, 10, 13), 77, dict(precision=synth.PREC_FP8)),
-                          (synth.COND_JOINT, (1, 7, 9), 33, dict(precision=synth.PREC_FP8))):
+# blocks: ragged grids, short conditions, K/N tails, both modes; GEMMs of
+# width a multiple of 256 on CTA pairs by main-loop length (these short K
+# give single CTAs) and then with pairs forced on
+import itertools
+for pairs, (mode, grid, L, kw) in itertools.product((1, 2), (
+        (synth.COND_CROSS, (2, 9, 7), 5, {}), (synth.COND_CROSS, (3, 10, 13), 77, {}),
+        (synth.COND_CROSS, (1, 6, 11), 37, dict(mlp=648, cond_dim=200)),
+        (synth.COND_JOINT, (1, 7, 9), 33, {}), (synth.COND_JOINT, (1, 12, 20), 64, {}),
+        (synth.COND_CROSS, (1, 1, 1), 1, {}), (synth.COND_JOINT, (1, 1, 1), 1, {}),
+        (synth.COND_CROSS, (3, 10, 13), 77, dict(precision=synth.PREC_FP8)),
+        (synth.COND_JOINT, (1, 7, 9), 33, dict(precision=synth.PREC_FP8)))):
+    dit.dit_debug_gemm_cta_pairs(pairs)
     cfg = small_bf16_cfg(mode, depth=1, **kw)
     W = synth.make_weights(cfg, seed=101)
     m = model(cfg, W)
@@ -72,6 +77,7 @@ for mode, grid, L, kw in ((synth.COND_CROSS, (2, 9, 7), 5, {}), (synth.COND_CROS
     m.close()
 
 # complete loops: tiny fp32 and bf16 in both modes
+dit.dit_debug_gemm_cta_pairs(1)
 for name, thw, L in (("tiny", None, 16), ("cross", (2, 12, 18), 40), ("joint", (1, 24, 20), 40)):
     if name == "tiny":
         cfg = synth.config("tiny")
@@ -109,4 +115,4 @@ def test_debug_bounds_build_on_odd_shapes():
     r = subprocess.run([sys.executable, "-c", _CHILD, ROOT], cwd=ROOT, env=env, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
-    assert "debug build checked 21" in r.stdout, r.stdout[-2000:]
+    assert "debug build checked 39" in r.stdout, r.stdout[-2000:]
