@@ -539,16 +539,19 @@ static bool make_epi_maps(const EpiParams& e, int64_t M, int N, EpiMaps* maps) {
 // more: a cluster that had to wait for a slot would run its whole tile list
 // after the others.
 static int pair_clusters(const void* kernel, cudaLaunchConfig_t cfg, int num_sms) {
-  static int cached[kMaxDevices] = {};
+  static int cached[kMaxDevices] = {};  // 0: not asked yet, -1: none fit
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   if (cached[dev] == 0) {
     int n = 0;
     cfg.gridDim = dim3(2 * (num_sms / 2));
-    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
-    cached[dev] = n < num_sms / 2 ? n : num_sms / 2;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();  // the query's error is not the launch's
+      n = 0;
+    }
+    cached[dev] = n <= 0 ? -1 : (n < num_sms / 2 ? n : num_sms / 2);
   }
-  return cached[dev];
+  return cached[dev] > 0 ? cached[dev] : 0;
 }
 
 template <int BN, int NP, bool F8, bool PAIR>
@@ -605,7 +608,8 @@ static cudaError_t launch_gemm_tc(const GemmArgs* gs, int* err, int num_sms, cud
     cfg.attrs = at;
     cfg.numAttrs = 1;
     const int max_clusters = pair_clusters(kernel, cfg, num_sms);
-    if (max_clusters <= 0) return cudaErrorInvalidConfiguration;
+    // no two-CTA cluster fits next to this kernel's resources: single CTAs
+    if (max_clusters <= 0) return launch_gemm_tc<BN, NP, F8, false>(gs, err, num_sms, s);
     const int clusters = tiles < max_clusters ? tiles : max_clusters;
     cfg.gridDim = dim3(2 * clusters);
     e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, NP, F8, true>, P, gs[0].N, gs[0].K, err);
