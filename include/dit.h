@@ -1,9 +1,10 @@
 /*
  * dit.h -- C ABI of the GB300 denoiser stage (libdit.so).
  *
- * The denoiser stage is the DiT forward loop together with the scheduler
- * stepping it drives (SGLang-Diffusion "Disaggregated Diffusion Pipeline",
- * Quick Start, role table: "denoiser").  Its inputs are the latents, the
+ * The denoiser stage runs the network's forward passes over the whole step
+ * schedule, with the sampler advancing the latent after each of them
+ * (SGLang-Diffusion "Disaggregated Diffusion Pipeline", Quick Start, role
+ * table: "denoiser").  Its inputs are the latents, the
  * timestep / sigma schedule in the exact order used, the positive prompt
  * embeddings and, when classifier-free guidance is on, the negative ones
  * (SGLang-Diffusion "Support New Diffusion Models", section 4, table of the
