@@ -558,7 +558,7 @@ def run_gpu(args):
         "attn_gemm_tflops": tflops,
         "pct_bf16_peak": 100 * tflops / peaks["bf16"],
         "pct_bf16_peak_sustained": 100 * tflops / peaks["bf16_sustained"],
-        "roofline": {"kernel": "attn_tc_kernel (self-attention)", "bound": "tensor",
+        "roofline": {"kernel": "attn_wide_kernel (self-attention)", "bound": "tensor",
                      "achieved": attn_achieved, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                      "frac": attn_achieved / peaks["bf16_sustained"], "traffic": traffic,
                      "peak_kind": f"bf16 sustained ({peaks['source']}), kernel timed inside a long step",

@@ -1,12 +1,19 @@
 // Bidirectional multi-head attention (no mask), head_dim 128, bf16 in/out,
 // fp32 softmax and accumulation, on the 5th-generation tensor cores.
 //
-// One CTA = 128 query rows of one (batch, head), walking the keys in tiles of
-// 128.  Per key tile j:
-//     S_j = Q K_j^T            (8 tcgen05.mma, A and B from shared memory)
+// Two kernels share the method -- per key tile j
+//     S_j = Q K_j^T            (tcgen05.mma, A and B from shared memory)
 //     P_j = 2^(S_j*c - m)      (softmax warps, bf16, written to tensor memory)
-//     O  += P_j V_j            (8 tcgen05.mma, A = P_j from tensor memory)
-// with the online-softmax running row max m and row sum l (c = log2(e)/sqrt(d)).
+//     O  += P_j V_j            (tcgen05.mma, A = P_j from tensor memory)
+// with the online-softmax running row max m and row sum l (c = log2(e)/sqrt(d))
+// -- and differ in how a CTA is laid out:
+//   attn_tc_kernel    short key ranges (cross-attention over the text tokens,
+//                     the joint image attention): 128-key tiles, persistent
+//                     CTAs that each walk many (query tile, batch*head) items;
+//   attn_wide_kernel  long key ranges (video self-attention): 192-key tiles,
+//                     one CTA per item (further down).
+//
+// attn_tc_kernel: one item = 128 query rows of one (batch, head).
 //
 // The tensor pipe idles whenever its issuing thread stops issuing (a wait, a
 // fence, a commit all leave a gap), and a single chain of MMAs into one
@@ -41,16 +48,15 @@
 // on a barrier needs an action of its own first, so a parity wait never
 // aliases.
 //
-// Persistent mode (short key ranges, e.g. cross-attention over 4 tiles): a
-// CTA per item would spend more on start-up (barrier set-up, tensor memory,
-// the first Q and K loads) than on the item's tiles, so one CTA per SM walks
-// every gridDim-th item.  Tiles are counted over all of a CTA's items,
-// so every ring runs on across item boundaries; the K loader refills the Q
-// buffer once the previous item's last S product has completed, and the
-// first PV product of an item (which overwrites O) waits until the softmax
-// warps have read out the previous item's O (o_free).  Persistent CTAs write
-// the output through shared memory and TMA tensor stores (three V stages
-// instead of four make the room); one CTA per item stores per lane, once.
+// Persistence: a CTA per item would spend more on start-up (barrier set-up,
+// tensor memory, the first Q and K loads) than on the item's few tiles, so
+// one CTA per SM walks every gridDim-th item.  Tiles are counted over all of
+// a CTA's items, so every ring runs on across item boundaries; the K loader
+// refills the Q buffer once the previous item's last S product has
+// completed, and the first PV product of an item (which overwrites O) waits
+// until the softmax warps have read out the previous item's O (o_free).  The
+// output goes through shared memory and TMA tensor stores (three V stages
+// make the room).
 //
 // Per-tile integer work on the softmax path is kept to compares and adds
 // (the ring slots and the rotated key tile advance incrementally): a
@@ -70,7 +76,7 @@ constexpr int BQ = 128, BKV = 128, HD = 128;
 // two tiles ahead of PV, so K needs less lead than V.  A ring must be at least
 // as long as the stage count its loader waits on (SR >= KST, PR >= VST) so that
 // no parity wait can alias.
-constexpr int KST = 2, VST = 4, SR = 3, PR = 4;
+constexpr int KST = 2, VST = 3, SR = 3, PR = 4;
 constexpr int TILE_BYTES = 128 * HD * 2;   // 32 KB: two 16 KB swizzle blocks of 64 channels
 constexpr int Q_OFF = 0;
 constexpr int K_OFF = Q_OFF + TILE_BYTES;
@@ -85,17 +91,14 @@ constexpr int K_OFF = Q_OFF + TILE_BYTES;
 constexpr int SM_WARPS = 8;                       // softmax warps
 constexpr int NQ = SM_WARPS / 4;                  // warps per TMEM lane quadrant
 constexpr int KPW = BKV / NQ;                     // key columns per softmax warp
-// Persistent CTAs (many short items) write each item's output through
-// shared memory and TMA: every softmax warp stages its 32 rows x 64 channels
-// (4 KB, 128-byte swizzle) and issues one tensor store.  The staging area
-// takes the place of one V stage.  (Per-lane 16-byte stores of 32 different
-// rows cost ~3700 cycles per item, half the time of a 4-tile item.)
-template <bool PERSIST>
+// Each item's output goes through shared memory and TMA: every softmax warp
+// stages its 32 rows x 64 channels (4 KB, 128-byte swizzle) and issues one
+// tensor store.  (Per-lane 16-byte stores of 32 different rows cost ~3700
+// cycles per item, half the time of a 4-tile item.)
 struct Layout {
-  static constexpr int VSTAGES = PERSIST ? 3 : VST;
   static constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
-  static constexpr int STG_OFF = V_OFF + VSTAGES * TILE_BYTES;  // [SM_WARPS][32 rows][128 B] (persistent)
-  static constexpr int STG_BYTES = PERSIST ? SM_WARPS * 32 * 128 : 0;
+  static constexpr int STG_OFF = V_OFF + VST * TILE_BYTES;  // [SM_WARPS][32 rows][128 B]
+  static constexpr int STG_BYTES = SM_WARPS * 32 * 128;
   static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
   static constexpr int XCH_OFF = BAR_OFF + 256;
   static constexpr int XSUM_OFF = XCH_OFF + 2 * NQ * BQ * 2;
@@ -113,10 +116,10 @@ constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 // the row's tile sum stays below this (each p <= 2^14, far from overflow:
 // bf16 and fp32 keep their relative precision at any such magnitude).
 constexpr float SUM_LIMIT = 16384.0f;
-// Key ranges of at most this many tiles run on persistent CTAs (one per SM,
-// each walking several items so that one item's start overlaps the previous
-// one's end); longer ones use one CTA per item, whose fixed cost is small
-// next to the item.
+// Key ranges of at most this many 128-key tiles run on attn_tc_kernel's
+// persistent CTAs (one per SM, each walking several items so that one item's
+// start overlaps the previous one's end); longer ones on attn_wide_kernel,
+// one CTA per item, whose fixed cost is small next to the item.
 constexpr int PERSIST_MAX_KV_TILES = 64;
 
 // tcgen05.ld of 64 columns (one instruction) straight into float registers
@@ -157,19 +160,17 @@ DIT_DEV float exp_tile(const float (&s)[NV], uint32_t (&pk)[NV / 2], float scale
 }  // namespace fa
 
 // tmO[0] / tmO[1]: the outputs o1 / o2 as [B][rows][H*128] in boxes of
-// 64 channels x 32 rows, used when bit 0 / bit 1 of o_tma is set (persistent
-// mode only).
+// 64 channels x 32 rows, used when bit 0 / bit 1 of o_tma is set.
 struct AttnOutMaps {
   CUtensorMap m[2];
 };
 
-template <bool PERSIST>
 __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ AttnOutMaps tmO, int o_tma,
                    AttnArgs a, float scale_log2, int* err) {
   using namespace fa;
-  using Lay = Layout<PERSIST>;
+  using Lay = Layout;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023) {  // uniform across the CTA: nothing has started yet
     if (threadIdx.x == 0) atomicCAS(err, 0, 20);
@@ -197,30 +198,17 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
   // the key tile that has fewer than BKV keys, if any (its masked columns
   // read -inf)
   const int partial_jt = (a.Lk % BKV) ? nkv - 1 : -1;
-  // An item is one (query tile, batch*head).  A persistent CTA takes items
-  // blockIdx.x, + gridDim.x, ... (the grid never exceeds the item count);
-  // otherwise the CTA is the single item of its grid position.  Key tiles are
-  // counted over all items of the CTA (G), so every ring runs on across item
-  // boundaries.
-  int my_items = 1;
-  if constexpr (PERSIST) {
-    const int n_items = a.B * a.H * nq;
-    my_items = (n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
-  }
-  auto item_bh = [&](int k) -> int {
-    if constexpr (PERSIST) return ((int)blockIdx.x + k * (int)gridDim.x) / nq;
-    return (int)(blockIdx.z * a.H + blockIdx.y);
-  };
-  auto item_qt = [&](int k) -> int {
-    if constexpr (PERSIST) return ((int)blockIdx.x + k * (int)gridDim.x) % nq;
-    return (int)blockIdx.x;
-  };
+  // An item is one (query tile, batch*head).  The CTA takes items
+  // blockIdx.x, + gridDim.x, ... (the grid never exceeds the item count).
+  // Key tiles are counted over all items of the CTA (G), so every ring runs
+  // on across item boundaries.
+  const int n_items = a.B * a.H * nq;
+  const int my_items = (n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  auto item_bh = [&](int k) -> int { return ((int)blockIdx.x + k * (int)gridDim.x) / nq; };
+  auto item_qt = [&](int k) -> int { return ((int)blockIdx.x + k * (int)gridDim.x) % nq; };
   // Each item walks the key tiles in a rotated order (the result does not
   // depend on the order), so items running together read different K/V tiles.
-  auto item_rot = [&](int k) -> int {
-    if constexpr (PERSIST) return item_qt(k) % nkv;
-    return (int)(blockIdx.x % (unsigned)nkv);
-  };
+  auto item_rot = [&](int k) -> int { return item_qt(k) % nkv; };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -232,7 +220,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
     // tiles 0 and 1 have no PV_{j-2}: its arrival is made up front
     mbar_arrive(&tile_ready[0]);
     mbar_arrive(&tile_ready[1 % SR]);
-    if (PERSIST) mbar_init(o_free, SM_WARPS);
+    mbar_init(o_free, SM_WARPS);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_free[b], SM_WARPS);
       mbar_init(&p_ready[b], SM_WARPS);
@@ -263,7 +251,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       const CUtensorMap* tm = is_k ? &tmK : &tmV;
       uint64_t* full = is_k ? kf : vf;
       uint64_t* consumed = is_k ? s_done : pv_done;
-      const int nst = is_k ? KST : Lay::VSTAGES, ring = is_k ? SR : PR;
+      const int nst = is_k ? KST : VST, ring = is_k ? SR : PR;
       uint8_t* stages = smem + (is_k ? K_OFF : Lay::V_OFF);
       int issued[4] = {0, 0, 0, 0};
       int q_issued = 0;
@@ -272,7 +260,7 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       for (int k = 0; ok && k < my_items; ++k) {
         const int bh = item_bh(k), qt = item_qt(k), kv_rot = item_rot(k);
         if (is_k) {
-          if (PERSIST && k > 0) {
+          if (k > 0) {
             const int c = G - 1;  // the previous item's last S product
             ok = mbar_wait(&s_done[c % SR], (uint32_t)((c / SR) & 1), abort_flag, err, 21);
             if (!ok) break;
@@ -353,13 +341,13 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       for (int k = 0; ok && k < my_items; ++k) {
         for (int j = 0; ok && j < nkv; ++j, ++G) {
           ok = mbar_wait(&p_ready[G & 1], (uint32_t)((G >> 1) & 1), abort_flag, err, 26) &&
-               mbar_wait(&vf[G % Lay::VSTAGES], (uint32_t)((G / Lay::VSTAGES) & 1), abort_flag, err, 27);
+               mbar_wait(&vf[G % VST], (uint32_t)((G / VST) & 1), abort_flag, err, 27);
           // the first product of an item overwrites O: the previous item's O
           // must have been read out
-          if (PERSIST && j == 0 && k > 0) ok = ok && mbar_wait(o_free, (uint32_t)((k - 1) & 1), abort_flag, err, 28);
+          if (j == 0 && k > 0) ok = ok && mbar_wait(o_free, (uint32_t)((k - 1) & 1), abort_flag, err, 28);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t vd = umma_desc_add(v_desc, (G % Lay::VSTAGES) * TILE_BYTES);
+          const uint64_t vd = umma_desc_add(v_desc, (G % VST) * TILE_BYTES);
           const uint32_t p_tmem = tmem + TM_P + (G & 1) * 64;
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk) {
@@ -522,12 +510,10 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
       // split between o1 and o2 take the per-lane stores; rows past the last
       // token are clipped by the tensor map)
       int map = -1;
-      if constexpr (PERSIST) {
-        if (tok0 + 32 <= a.split || a.split == a.Lq)
-          map = (o_tma & 1) ? 0 : -1;
-        else if (tok0 >= a.split)
-          map = (o_tma & 2) ? 1 : -1;
-      }
+      if (tok0 + 32 <= a.split || a.split == a.Lq)
+        map = (o_tma & 1) ? 0 : -1;
+      else if (tok0 >= a.split)
+        map = (o_tma & 2) ? 1 : -1;
       if (map >= 0) {
         if (tok0 < a.Lq && DIT_BOUNDS(bh < a.B * a.H && tok0 >= 0, err, 63)) {
           uint8_t* stg = smem + Lay::STG_OFF + warp * (32 * 128);
@@ -581,16 +567,388 @@ __global__ void __launch_bounds__(fa::NUM_THREADS, 1)
         }
       }
     }
-    if constexpr (PERSIST) {
-      // O may now take the next item's products
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);
-    }
+    // O may now take the next item's products
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(o_free);
     }
     // every tensor store of this warp has landed before the CTA exits
-    if (PERSIST && lane == 0) bulk_wait0();
+    if (lane == 0) bulk_wait0();
     __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == S_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Long key ranges (self-attention over thousands of tokens): key tiles of 192.
+//
+// With 128-key tiles (the kernel above, once also used here) a long key range
+// is bound by the softmax: each tile costs its eight softmax warps a fixed
+// ~600 cycles (the wait for S, the tensor-memory load, the quadrant's barrier,
+// the P store) on top of the exponentials, ~1450 cycles in all, while the
+// tile's 16 MMAs take ~1070.  Here a tile holds 192 keys and twelve softmax
+// warps (three per lane quadrant, 64 keys each) share it: the fixed cost is
+// paid once per 192 keys.  Measured on the video self-attention (32760
+// tokens, batch 2): ~1900 cycles per 192-key tile, 7.96 ms per launch
+// against 8.42 ms with 128-key tiles.
+// Tensor memory then holds one S tile, two P slots and O:
+//     S [0,192)   P slots [192,288) [288,384)   O [384,512)
+// S_{j+1} is issued into the single S tile once every softmax warp has copied
+// S_j into registers; P_j goes to slot j%2 once PV_{j-2} has read it.  As in
+// the kernel above, two threads issue: one the S products (one chain of
+// M128 x N192 MMAs per tile), one the PV products (twelve M128 x N128 MMAs
+// into O).  A single thread issuing both was measured at ~2400 cycles per
+// tile against ~1600 of MMA work: each MMA it issues holds it for about the
+// MMA's duration, so PV_{j-1} and S_{j+1} could never overlap.  With two
+// threads the two products interleave in the pipe and both run at its full
+// rate.  (Holding PV_{j-1} back until S_{j+1} was issued, so that S_{j+1}
+// completes sooner, made the kernel 10 % slower: PV then runs as a lone
+// chain of dependent MMAs.)  The softmax of tile j makes one wait, on
+// tile_ready (two commits: S_j from the S thread, PV_{j-2} from the PV
+// thread).
+//
+// One loader thread streams Q, then K and V in two stages each (48 KB per
+// 192-key tile), in the order their stages free up: K_{t+1} once S_{t-1} has
+// completed, V_t once PV_{t-2} has.
+//
+// The softmax itself is the one above (fast path against the running
+// reference max, one bar.red.or per quadrant per tile, row max and rescale
+// only when a row's tile sum exceeds SUM_LIMIT), with NQ = 3.  O's 128
+// channels are read out (rescale, epilogue) in 32-column chunks, chunk c by
+// warp c % 3 of the quadrant.
+namespace fw {
+constexpr int BQ = 128, BKV = 192, HD = 128;
+constexpr int SM_WARPS = 12;
+constexpr int NQ = SM_WARPS / 4;   // softmax warps per lane quadrant
+constexpr int KPW = BKV / NQ;      // key columns per softmax warp
+static_assert(KPW == 64, "one 64-column tensor-memory load per warp and tile");
+constexpr int NUM_THREADS = 32 * (SM_WARPS + 3);
+constexpr int LOAD_WARP = SM_WARPS, S_WARP = SM_WARPS + 1, PV_WARP = SM_WARPS + 2;
+constexpr int Q_BYTES = BQ * HD * 2;         // 32 KB: two 16 KB boxes of 64 channels
+constexpr int KV_BOX = BKV * 64 * 2;         // 24 KB: 192 rows x 64 channels
+constexpr int KV_BYTES = 2 * KV_BOX;         // one K or V tile
+constexpr int STAGES = 2;
+constexpr int Q_OFF = 0;
+constexpr int K_OFF = Q_OFF + Q_BYTES;
+constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
+constexpr int BAR_OFF = V_OFF + STAGES * KV_BYTES;
+// bf16 row maxima [2 parities][NQ][BQ]; once the last tile is done the same
+// bytes take the float row sums [NQ][BQ] (one item per CTA)
+constexpr int XCH_OFF = BAR_OFF + 256;
+constexpr int SMEM_BYTES = XCH_OFF + 2 * NQ * BQ * 2;
+static_assert(NQ * BQ * 4 <= 2 * NQ * BQ * 2, "row-sum area larger than the row-max area it reuses");
+constexpr int SR = 4, PR = 4;  // completion rings of S_j and PV_j (powers of two)
+constexpr uint32_t TM_S = 0, TM_P = 192, TM_O = 384;
+constexpr uint32_t IDESC_S = umma_idesc_bf16(128, BKV, false);
+constexpr uint32_t IDESC_O = umma_idesc_bf16(128, 128, true);
+}  // namespace fw
+
+__global__ void __launch_bounds__(fw::NUM_THREADS, 1)
+    attn_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, AttnArgs a, float scale_log2, int* err) {
+  using namespace fw;
+  using fa::exp_tile;
+  using fa::tmem_ld64f;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023) {  // uniform across the CTA: nothing has started yet
+    if (threadIdx.x == 0) atomicCAS(err, 0, 20);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  uint64_t* q_full = bars;              // Q tile
+  uint64_t* kf = bars + 1;              // [STAGES] K stage loaded
+  uint64_t* vf = kf + STAGES;           // [STAGES] V stage loaded
+  uint64_t* s_done = vf + STAGES;       // [SR] S_j complete
+  uint64_t* pv_done = s_done + SR;      // [PR] PV_j complete
+  uint64_t* tile_ready = pv_done + PR;  // [SR] S_j and PV_{j-2} complete (two commits)
+  uint64_t* s_free = tile_ready + SR;   // softmax has copied S_j (one arrival per softmax warp)
+  uint64_t* p_ready = s_free + 1;       // [2] P slot j % 2 written (one arrival per softmax warp)
+  uint64_t* drain = p_ready + 2;        // [2] final commit of each MMA thread
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  __nv_bfloat16* xmax = reinterpret_cast<__nv_bfloat16*>(smem + XCH_OFF);
+  float* xsum = reinterpret_cast<float*>(smem + XCH_OFF);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nkv = (a.Lk + BKV - 1) / BKV;
+  const int partial_jt = (a.Lk % BKV) ? nkv - 1 : -1;
+  const int qt = (int)blockIdx.x, bh = (int)(blockIdx.z * a.H + blockIdx.y);
+  // Key tiles in a rotated order (the result does not depend on it), so the
+  // CTAs running together read different K/V tiles.
+  const int kv_rot = (int)(blockIdx.x % (unsigned)nkv);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&kf[i], 1);
+      mbar_init(&vf[i], 1);
+    }
+    for (int i = 0; i < SR; ++i) mbar_init(&s_done[i], 1);
+    for (int i = 0; i < PR; ++i) mbar_init(&pv_done[i], 1);
+    for (int i = 0; i < SR; ++i) mbar_init(&tile_ready[i], 2);
+    // tiles 0 and 1 have no PV_{j-2}: its arrival is made up front
+    mbar_arrive(&tile_ready[0]);
+    mbar_arrive(&tile_ready[1]);
+    mbar_init(s_free, SM_WARPS);
+    mbar_init(&p_ready[0], SM_WARPS);
+    mbar_init(&p_ready[1], SM_WARPS);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == LOAD_WARP && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == S_WARP) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == LOAD_WARP) {
+    // ------------------------------------------------ TMA producer (one thread)
+    if (lane == 0) {
+      int k_issued[STAGES] = {0, 0}, v_issued[STAGES] = {0, 0};
+      bool ok = DIT_BOUNDS(bh >= 0 && bh < a.B * a.H && qt >= 0 && qt * BQ < a.Lq && kv_rot < nkv, err, 62);
+      if (!ok) *abort_flag = 1;  // every other wait of the CTA returns at once
+      auto load_kv = [&](const CUtensorMap* tm, uint64_t* full, uint8_t* dst, int t) {
+        const int jt = t + kv_rot < nkv ? t + kv_rot : t + kv_rot - nkv;
+        mbar_arrive_expect_tx(full, KV_BYTES);
+        tma_load_3d(dst, tm, full, 0, jt * BKV, bh);
+        tma_load_3d(dst + KV_BOX, tm, full, 64, jt * BKV, bh);
+      };
+      if (ok) {
+        mbar_arrive_expect_tx(q_full, Q_BYTES);
+        tma_load_3d(smem + Q_OFF, &tmQ, q_full, 0, qt * BQ, bh);
+        tma_load_3d(smem + Q_OFF + Q_BYTES / 2, &tmQ, q_full, 64, qt * BQ, bh);
+        load_kv(&tmK, &kf[0], smem + K_OFF, 0);
+        ++k_issued[0];
+      }
+      for (int t = 0; ok && t < nkv; ++t) {
+        if (t + 1 < nkv) {
+          // K stage (t+1) % 2 was last read by S_{t-1}
+          if (t >= 1) {
+            ok = mbar_wait(&s_done[(t - 1) & (SR - 1)], (uint32_t)(((t - 1) / SR) & 1), abort_flag, err, 50);
+            if (!ok) break;
+          }
+          load_kv(&tmK, &kf[(t + 1) & 1], smem + K_OFF + ((t + 1) & 1) * KV_BYTES, t + 1);
+          ++k_issued[(t + 1) & 1];
+        }
+        // V stage t % 2 was last read by PV_{t-2}
+        if (t >= 2) {
+          ok = mbar_wait(&pv_done[(t - 2) & (PR - 1)], (uint32_t)(((t - 2) / PR) & 1), abort_flag, err, 51);
+          if (!ok) break;
+        }
+        load_kv(&tmV, &vf[t & 1], smem + V_OFF + (t & 1) * KV_BYTES, t);
+        ++v_issued[t & 1];
+      }
+      if (!ok) {
+        // wind down: every copy this thread started lands before the CTA exits
+        volatile int no_abort = 0;
+        if (k_issued[0] > 0) mbar_wait(q_full, 0, &no_abort, nullptr, 0);
+        for (int st = 0; st < STAGES; ++st) {
+          if (k_issued[st] > 0) mbar_wait(&kf[st], (uint32_t)((k_issued[st] - 1) & 1), &no_abort, nullptr, 0);
+          if (v_issued[st] > 0) mbar_wait(&vf[st], (uint32_t)((v_issued[st] - 1) & 1), &no_abort, nullptr, 0);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == S_WARP) {
+    // ------------------------------------------------ S = Q K^T issuer (one thread)
+    if (lane == 0) {
+      const uint64_t q_desc = umma_desc_sw128(smem_u32(smem + Q_OFF), 16, 1024);
+      const uint64_t k_desc = umma_desc_sw128(smem_u32(smem + K_OFF), 16, 1024);
+      bool ok = mbar_wait(q_full, 0, abort_flag, err, 52);
+      for (int t = 0; ok && t < nkv; ++t) {
+        // the S tile is free once every softmax warp has copied S_{t-1}
+        if (t >= 1) ok = mbar_wait(s_free, (uint32_t)((t - 1) & 1), abort_flag, err, 56);
+        ok = ok && mbar_wait(&kf[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, err, 53);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t kd = umma_desc_add(k_desc, (t & 1) * KV_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          // channels 16kk..16kk+15: 32-byte steps inside a 128-byte swizzled row, boxes of 64 channels
+          umma_ss(tmem + TM_S, umma_desc_add(q_desc, (kk >> 2) * (Q_BYTES / 2) + (kk & 3) * 32),
+                  umma_desc_add(kd, (kk >> 2) * KV_BOX + (kk & 3) * 32), IDESC_S, kk != 0);
+        }
+        umma_commit(&s_done[t & (SR - 1)]);
+        umma_commit(&tile_ready[t & (SR - 1)]);
+      }
+      // all MMAs issued by this thread complete before tensor memory is released
+      umma_commit(&drain[0]);
+      volatile int no_abort = 0;
+      mbar_wait(&drain[0], 0, &no_abort, nullptr, 0);
+    }
+    __syncwarp();
+  } else if (warp == PV_WARP) {
+    // ------------------------------------------------ O += P V issuer (one thread)
+    if (lane == 0) {
+      const uint64_t v_desc = umma_desc_sw128(smem_u32(smem + V_OFF), KV_BOX, 1024);
+      bool ok = true;
+      for (int t = 0; ok && t < nkv; ++t) {
+        ok = mbar_wait(&p_ready[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, err, 54) &&
+             mbar_wait(&vf[t & 1], (uint32_t)((t >> 1) & 1), abort_flag, err, 55);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t vd = umma_desc_add(v_desc, (t & 1) * KV_BYTES);
+        const uint32_t p_tmem = tmem + TM_P + (t & 1) * (BKV / 2);
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk)
+          // keys 16kk..16kk+15: P columns 8kk.. (bf16 pairs), V rows 16kk.. (8-row groups 1 KB apart)
+          umma_ts(tmem + TM_O, p_tmem + kk * 8, umma_desc_add(vd, kk * 2048), IDESC_O, (t | kk) != 0);
+        umma_commit(&pv_done[t & (PR - 1)]);
+        umma_commit(&tile_ready[(t + 2) & (SR - 1)]);
+      }
+      umma_commit(&drain[1]);
+      volatile int no_abort = 0;
+      mbar_wait(&drain[1], 0, &no_abort, nullptr, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ softmax warps
+    const int q = warp & 3, h = warp >> 2;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const int row = q * 32 + lane;
+    bool ok = true;
+    float m_used = -INFINITY, l = 0.f;
+    int jt = kv_rot;  // key tile of tile j
+    // The loop never breaks: after a failed wait the warp skips the work but
+    // still meets its quadrant partners at every named barrier.
+    for (int j = 0; j < nkv; ++j, jt = (jt + 1 == nkv) ? 0 : jt + 1) {
+      float s[KPW];
+      uint32_t pk[KPW / 2];
+      float tsum = 0.f;
+      bool big = true;  // a warp that skipped its work asks for the slow path
+      bool p_stored = false;
+      const uint32_t p_col = tmem + TM_P + (j & 1) * (BKV / 2) + h * (KPW / 2) + lane_off;
+      // S_j complete, and PV_{j-2}: P slot j%2 is free
+      ok = ok && mbar_wait_warp(&tile_ready[j & (SR - 1)], (uint32_t)((j / SR) & 1), abort_flag, err, 57);
+      if (ok) {
+        tc_fence_after();
+        tmem_ld64f(tmem + TM_S + h * KPW + lane_off, s);
+        tmem_ld_wait();
+        // the S tile may now take S_{j+1}
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
+        if (jt == partial_jt) {
+          const int valid = a.Lk - jt * BKV - h * KPW;
+#pragma unroll
+          for (int i = 0; i < KPW; ++i)
+            if (i >= valid) s[i] = -INFINITY;
+        }
+        if (j > 0) {
+          tsum = exp_tile(s, pk, scale_log2, m_used);
+          big = !(tsum <= fa::SUM_LIMIT);
+          tmem_st32(p_col, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+          p_stored = true;
+        }
+      }
+      if (named_bar_or(1 + q, 32 * NQ, big)) {
+        // slow path: the row max of the tile over the quadrant's warps
+        if (ok) {
+          float m4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+          for (int i = 4; i + 8 <= KPW - 4; i += 8)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], s[i + 2 * k], s[i + 2 * k + 1]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) m4[k] = fmaxf(m4[k], s[KPW - 4 + k]);
+          xmax[((j & 1) * NQ + h) * BQ + row] =
+              __float2bfloat16_rn(fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]) * scale_log2);
+        }
+        named_bar_sync(1 + q, 32 * NQ);
+        if (!ok) continue;
+        const __nv_bfloat16* xm = xmax + (j & 1) * NQ * BQ + row;
+        float m_tile = __bfloat162float(xm[0]);
+#pragma unroll
+        for (int w = 1; w < NQ; ++w) m_tile = fmaxf(m_tile, __bfloat162float(xm[w * BQ]));
+        // rows whose max grew by more than 2^8 (every row of the first tile)
+        // move to the tile max; the others keep their fast-path exponentials
+        const bool row_big = m_tile - m_used > fa::RESCALE_THRESHOLD;
+        const float alpha = row_big ? ex2_approx(m_used - m_tile) : 1.f;  // O's factor: 1 for rows kept
+        const bool any_big = __any_sync(0xffffffffu, row_big);
+        if (any_big || !p_stored) {
+          // P_j again, every lane of the warp (a row that keeps its reference
+          // recomputes the same values), from the scores still in registers:
+          // the S tile may already hold S_{j+1}
+          if (row_big) m_used = m_tile;
+          tsum = exp_tile(s, pk, scale_log2, m_used);
+          if (p_stored) tmem_st_wait();  // the early store lands before it is replaced
+          tmem_st32(p_col, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+          p_stored = true;
+        }
+        if (j > 0 && any_big) {
+          // O (and l) move to the new reference; O must hold PV_{j-1} first.
+          // (PV_j reads P_j only after p_ready, below.)
+          ok = mbar_wait_warp(&pv_done[(j - 1) & (PR - 1)], (uint32_t)(((j - 1) / PR) & 1), abort_flag, err, 57);
+          if (!ok) continue;
+          tc_fence_after();
+          l *= alpha;
+#pragma unroll 1
+          for (int c = h; c < HD / 32; c += NQ) {
+            uint32_t r[32];
+            tmem_ld32(tmem + TM_O + c * 32 + lane_off, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tmem + TM_O + c * 32 + lane_off, r);
+          }
+        }
+      }
+      if (!ok) continue;
+      l += tsum;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_ready[j & 1]);
+    }
+    tmem_st_wait();  // a P store left in flight by a failed wait lands before tensor memory is reused
+    // O is final once PV_{nkv-1} has completed
+    ok = ok && mbar_wait_warp(&pv_done[(nkv - 1) & (PR - 1)], (uint32_t)(((nkv - 1) / PR) & 1), abort_flag, err, 57);
+    // the quadrant's partial row sums (same reference max) meet in the
+    // exchange area once every warp of the quadrant is past its last tile
+    named_bar_sync(1 + q, 32 * NQ);
+    xsum[h * BQ + row] = l;
+    named_bar_sync(1 + q, 32 * NQ);
+    if (ok) {
+      tc_fence_after();
+      float lt = 0.f;
+#pragma unroll
+      for (int w = 0; w < NQ; ++w) lt += xsum[w * BQ + row];
+      const float inv = 1.f / lt;
+      const int tok = qt * BQ + row;
+      const int b = bh / a.H, head = bh - b * a.H;
+      const int D = a.H * HD;
+      __nv_bfloat16* out = nullptr;
+      if (tok < a.Lq && DIT_BOUNDS(bh < a.B * a.H && tok >= 0, err, 63)) {
+        out = (tok < a.split)
+                  ? static_cast<__nv_bfloat16*>(a.o1) + ((int64_t)b * a.split + tok) * D
+                  : static_cast<__nv_bfloat16*>(a.o2) + ((int64_t)b * (a.Lq - a.split) + (tok - a.split)) * D;
+        out += head * HD;
+      }
+#pragma unroll 1
+      for (int c = h; c < HD / 32; c += NQ) {
+        uint32_t r[32];
+        tmem_ld32(tmem + TM_O + c * 32 + lane_off, r);
+        tmem_ld_wait();
+        if (out) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * inv;
+          store_chunk<__nv_bfloat16, 32>(out + c * 32, v);
+        }
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -613,11 +971,8 @@ cudaError_t attention_bf16_tc(const AttnArgs& a, int* err, cudaStream_t s) {
   if (!make_tmap_bf16(&tq, a.q, 3, dq, sq, box) || !make_tmap_bf16(&tk, a.k, 3, dk, sk, box) ||
       !make_tmap_bf16(&tv, a.v, 3, dk, sk, box))
     return cudaErrorInvalidValue;
-  static SmemAttr attr_one, attr_persist;
-  cudaError_t e =
-      ensure_smem_attr(reinterpret_cast<const void*>(attn_tc_kernel<false>), Layout<false>::SMEM_BYTES, attr_one);
-  if (e == cudaSuccess)
-    e = ensure_smem_attr(reinterpret_cast<const void*>(attn_tc_kernel<true>), Layout<true>::SMEM_BYTES, attr_persist);
+  static SmemAttr attr_persist;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(attn_tc_kernel), Layout::SMEM_BYTES, attr_persist);
   static int sms_of[kMaxDevices] = {};
   int dev = 0;
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
@@ -644,20 +999,24 @@ cudaError_t attention_bf16_tc(const AttnArgs& a, int* err, cudaStream_t s) {
     };
     if (omap(&om.m[0], a.o1, a.split)) o_tma |= 1;
     if (omap(&om.m[1], a.o2, a.Lq - a.split)) o_tma |= 2;
-    attn_tc_kernel<true><<<grid, NUM_THREADS, Layout<true>::SMEM_BYTES, s>>>(tq, tk, tv, om, o_tma, a, scale_log2,
-                                                                           err);
+    attn_tc_kernel<<<grid, NUM_THREADS, Layout::SMEM_BYTES, s>>>(tq, tk, tv, om, o_tma, a, scale_log2, err);
   } else {
+    // long key ranges: one CTA per (query tile, batch*head), 192-key tiles
+    CUtensorMap tk_w, tv_w;
+    const uint32_t box_w[3] = {64, (uint32_t)fw::BKV, 1};
+    if (!make_tmap_bf16(&tk_w, a.k, 3, dk, sk, box_w) || !make_tmap_bf16(&tv_w, a.v, 3, dk, sk, box_w))
+      return cudaErrorInvalidValue;
+    static SmemAttr attr_wide;
+    e = ensure_smem_attr(reinterpret_cast<const void*>(attn_wide_kernel), fw::SMEM_BYTES, attr_wide);
+    if (e != cudaSuccess) return e;
     dim3 grid(nq, a.H, a.B);
-    const AttnOutMaps none{};
-    attn_tc_kernel<false><<<grid, NUM_THREADS, Layout<false>::SMEM_BYTES, s>>>(tq, tk, tv, none, 0, a, scale_log2,
-                                                                             err);
+    attn_wide_kernel<<<grid, fw::NUM_THREADS, fw::SMEM_BYTES, s>>>(tq, tk_w, tv_w, a, scale_log2, err);
   }
   return cudaGetLastError();
 }
 
 }  // namespace dit
 
-static_assert(dit::fa::Layout<false>::SMEM_BYTES <= 232448 && dit::fa::Layout<true>::SMEM_BYTES <= 232448,
+static_assert(dit::fa::Layout::SMEM_BYTES <= 232448 && dit::fw::SMEM_BYTES <= 232448,
               "attention tile set exceeds 227 KB of shared memory");
-static_assert(dit::fa::PR >= dit::fa::Layout<true>::VSTAGES, "V completion ring shorter than the V stages");
-static_assert(dit::fa::Layout<true>::STG_OFF % 1024 == 0, "swizzled staging buffers need 1024-byte alignment");
+static_assert(dit::fa::Layout::STG_OFF % 1024 == 0, "swizzled staging buffers need 1024-byte alignment");

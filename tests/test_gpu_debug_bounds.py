@@ -5,7 +5,8 @@ and records the first failure in the model's error word instead of touching
 memory; dit_synchronize then reports it.  Run over the small odd shapes of
 the CPU comparisons (ragged token counts, a single token, short and
 single-token conditions, K and N tails, both conditioning modes, GEMMs on
-single CTAs and on CTA pairs, complete loops), every check must pass and every result must still match the oracle.  Runs in a child process because
+single CTAs and on CTA pairs, a key range long enough for the 192-key-tile
+attention, complete loops), every check must pass and every result must still match the oracle.  Runs in a child process because
 the library a process loads is fixed at its first use."""
 import os
 import subprocess
@@ -76,8 +77,30 @@ for pairs, (mode, grid, L, kw) in itertools.product((1, 2), (
         n_checked += 1
     m.close()
 
-# complete loops: tiny fp32 and bf16 in both modes
+# a key range long enough for the one-CTA-per-query-tile attention (8600
+# tokens: 45 key tiles of 192, the last one partial), sampled rows
 dit.dit_debug_gemm_cta_pairs(1)
+cfg = small_bf16_cfg(synth.COND_CROSS, depth=1)
+W = synth.make_weights(cfg, seed=105)
+m = model(cfg, W)
+grid, L = (1, 86, 100), 40
+N = int(np.prod(grid))
+rng = np.random.default_rng(106)
+x0 = (rng.standard_normal((2, N, cfg["hidden"])) * 0.5).astype(np.float32)
+mods = np.stack([O.timestep_modulation(t, W, cfg) for t in (330.0, 770.0)])
+ctx = synth.make_cond(cfg, batch=2, seed=107, length=L)
+x = dev(x0)
+m.dit_block_forward(0, x, None, dev(mods), dev(ctx), 2, grid, L)
+m.dit_synchronize()
+got = host(x)
+rows = np.array(sorted(set(np.linspace(0, N - 1, 24).astype(int).tolist()) | set(range(N - 26, N))))
+for b in range(2):
+    ref = O.block_cross(x0[b], mods[b], ctx[b], W, 0, cfg, grid, rows=rows)
+    assert_block_close(got[b][rows], ref, case="debug build long key range")
+    n_checked += 1
+m.close()
+
+# complete loops: tiny fp32 and bf16 in both modes
 for name, thw, L in (("tiny", None, 16), ("cross", (2, 12, 18), 40), ("joint", (1, 24, 20), 40)):
     if name == "tiny":
         cfg = synth.config("tiny")
@@ -115,4 +138,4 @@ def test_debug_bounds_build_on_odd_shapes():
     r = subprocess.run([sys.executable, "-c", _CHILD, ROOT], cwd=ROOT, env=env, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
-    assert "debug build checked 39" in r.stdout, r.stdout[-2000:]
+    assert "debug build checked 41" in r.stdout, r.stdout[-2000:]

@@ -210,8 +210,9 @@ def test_image_block_sweep_1024_tokens(image_model):
 
 def test_image_block_sweep_65536_tokens(image_model):
     """Sweep point: 65536 image tokens (256 x 256 grid) + 512 condition tokens,
-    batch 2: 516 key tiles, so the attention runs one CTA per item rather than
-    the persistent walk used for short key ranges."""
+    batch 2: 344 key tiles of 192, so the attention runs the one-CTA-per-item
+    kernel for long key ranges rather than the persistent walk used for short
+    ones."""
     cfg, W, m = image_model
     _image_block_case(cfg, W, m, (1, 512, 512), 2, (0,), seed=25)
 

@@ -361,6 +361,61 @@ def test_bf16_attention_rescale_paths():
     m.close()
 
 
+@pytest.mark.parametrize("peaked", [False, True], ids=["flat", "peaked"])
+def test_bf16_attention_long_key_range(peaked):
+    """A key range long enough for the one-CTA-per-query-tile attention (more
+    than 64 tiles of 128 keys): 8600 tokens = 45 key tiles of 192, the last
+    one holding 152 keys (its third 64-key slice only 24), and a last query
+    tile of 24 rows.  Flat: N(0, 0.02) weights, the fast path on almost every
+    tile.  Peaked: the rescale case above at this length (query and key
+    projections equal and scaled by 8, tokens leaning more and more on one
+    direction), so the tile row max, the rescale of O and l and the redone
+    rows run on most tiles.  Sampled rows of both batch items against the
+    oracle."""
+    cfg = small_bf16_cfg(synth.COND_CROSS, depth=1, rope_axes=(0, 0, 0) if peaked else (32, 48, 48))
+    W = synth.make_weights(cfg, seed=61)
+    D = cfg["hidden"]
+    grid, L = (1, 86, 100), 40
+    N = int(np.prod(grid))
+    rng = np.random.default_rng(62)
+    if peaked:
+        wqkv = W["blocks.0.attn.qkv.weight"].copy()
+        wqkv[:D] *= 8.0
+        wqkv[D:2 * D] = wqkv[:D]
+        W["blocks.0.attn.qkv.weight"] = wqkv
+        u = rng.standard_normal(D)
+        x0 = np.stack([np.linspace(0.0, 4.0, N)[:, None] * u[None] + rng.standard_normal((N, D)),
+                       np.linspace(4.0, 0.0, N)[:, None] * u[None] + rng.standard_normal((N, D))])
+    else:
+        x0 = rng.standard_normal((2, N, D)) * 0.5
+    x0 = x0.astype(np.float32)
+    mods = np.stack([O.timestep_modulation(t, W, cfg) for t in (300.0, 800.0)])
+    if peaked:
+        # the case does what it claims: scores of sampled query rows span far
+        # more than 2^8 and grow along the keys
+        sh1, sc1 = O.block_modulation(mods[0], W["blocks.0.mod_table"], D)[:2]
+        hh = O.modulate(O.layer_norm(x0[0], cfg["ln_eps"]), sh1, sc1)
+        k = O.linear(hh, wqkv[D:2 * D], W["blocks.0.attn.qkv.bias"][D:2 * D])
+        q = O.linear(hh[::97], wqkv[:D], W["blocks.0.attn.qkv.bias"][:D])
+        sc = q[:, :128] @ k[:, :128].T * (np.log2(np.e) / np.sqrt(128))
+        assert sc.max() - sc.min() > 20
+        assert np.mean(sc[:, -192:].max(1) - sc[:, :192].max(1) > 8) > 0.5
+    m = make_model(cfg, W)
+    ctx = synth.make_cond(cfg, batch=2, seed=63, length=L)
+    x = dev(x0)
+    m.dit_block_forward(0, x, None, dev(mods), dev(ctx), 2, grid, L)
+    m.dit_synchronize()
+    got = host(x)
+    rows = np.array(sorted(set(np.linspace(0, N - 1, 48).astype(int).tolist()) | set(range(N - 26, N))))
+    angles = None if peaked else O.rope_angles(O.token_positions(grid), cfg["rope_axes"], cfg["rope_theta"])
+    for b in range(2):
+        ref = O.block_cross(x0[b], mods[b], ctx[b], W, 0, cfg, grid, rows=rows, angles=angles)
+        case = f"long keys {'peaked' if peaked else 'flat'} b{b}"
+        assert_block_close(got[b][rows], ref, case=case)
+        assert_block_close(got[b][rows] - x0[b][rows], ref - x0[b][rows], 5, case=case + " update")
+    m.close()
+
+
 @pytest.mark.parametrize("which", ["tiny_fp32", "bf16_cross", "bf16_joint"])
 def test_loop_two_requests(which, tiny, small_cross, small_joint):
     """dit_denoise_loop with batch = 2 requests, each with its own latent,
