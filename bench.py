@@ -58,10 +58,11 @@ WORKLOADS = {
 # valid only for the exact kernel source it was captured on.
 TRAFFIC = {
     # kernel source file -> (sha256 prefix of the source, workload, bytes per launch).
-    # attn_tc.cu: dram__bytes_read.sum + dram__bytes_write.sum = 604.9 + 186.3 MB
-    # for one batch-2 video self-attention launch (the launch the step runs),
-    # from an ncu capture of the block case (one launch, --clock-control none).
-    "attn_tc.cu": ("f89f3d1dfd285312", "video", 604944128 + 186342912),
+    # attn_tc.cu: dram__bytes_read.sum + dram__bytes_write.sum = 606.4 + 187.2 MB
+    # for one batch-2 video self-attention launch (attn_wide_kernel, the launch
+    # the step runs), from an ncu capture of the block case (one launch,
+    # --clock-control none).
+    "attn_tc.cu": ("8782399015da528d", "video", 606381312 + 187175168),
 }
 
 
