@@ -106,8 +106,8 @@ def measured_peaks() -> dict:
         with open(p) as f:
             d = json.load(f)
         return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sustained=d["bf16_tflops_sustained"],
-                    source="measured")
-    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+                    source="measured", sustained_sm_mhz=(d.get("clocks_under_load") or {}).get("sm_mhz_median"))
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback", sustained_sm_mhz=None)
 
 
 # ------------------------------------------------------------------ clocks
@@ -562,6 +562,12 @@ def run_gpu(args):
         "roofline": {"kernel": "attn_wide_kernel (self-attention)", "bound": "tensor",
                      "achieved": attn_achieved, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                      "frac": attn_achieved / peaks["bf16_sustained"], "traffic": traffic,
+                     # the sustained peak was measured at a lower median SM clock than
+                     # this run's: the same fraction with the peak scaled to this clock
+                     "frac_at_run_clock": (attn_achieved / (peaks["bf16_sustained"] * clk["sm_mhz"]
+                                                            / peaks["sustained_sm_mhz"])
+                                           if clk.get("sm_mhz") and peaks.get("sustained_sm_mhz") else None),
+                     "peak_sm_mhz": peaks.get("sustained_sm_mhz"), "run_sm_mhz": clk.get("sm_mhz"),
                      "peak_kind": f"bf16 sustained ({peaks['source']}), kernel timed inside a long step",
                      "per_launch_flops": fl["attn_self_per_launch"], "avg_launch_ms": attn_ms,
                      "timed_by": f"event pair per launch, separate {k_prof}-step pass after the headline"},
