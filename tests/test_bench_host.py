@@ -82,3 +82,20 @@ def test_reference_line_states_its_extrapolation(monkeypatch, capsys):
     assert line["ms_per_full_step_extrapolated"] == pytest.approx(60.0e3)
     assert line["value"] == pytest.approx(1 / 60.0)
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["extrapolated"] is True
+
+
+def test_measured_peaks_carry_the_clock_of_the_sustained_figure(tmp_path, monkeypatch):
+    """The roofline's clock-scaled fraction needs the median SM clock under
+    which the sustained bf16 peak was measured; without the file the
+    fallback figures carry none (and the fraction is then left out)."""
+    import json
+    import bench
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
+        {"hbm_gbs": 6000.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+         "clocks_under_load": {"sm_mhz_median": 1455.0}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    p = bench.measured_peaks()
+    assert p["source"] == "measured" and p["sustained_sm_mhz"] == 1455.0
+    (tmp_path / "MEASURED_PEAKS.json").unlink()
+    p = bench.measured_peaks()
+    assert p["source"] == "fallback" and p["sustained_sm_mhz"] is None
